@@ -1,0 +1,166 @@
+"""fp64 CPU oracle for the int4-g128 weight-streaming GEMV.
+
+TEST INFRASTRUCTURE ONLY.  Only tests/, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product package
+(``int4_weight_only_g128_gb300``) never imports it, and the two share no code.
+
+The oracle is plain C (``oracle.c``) computing the definition of the method in
+fp64: dequantise w = min + q*scale per 128-row group (Token Rush README,
+"Quantization" section), then y = x . w summed in ascending k.  See the header
+comment of ``oracle.c`` for the passages it follows and the readings it takes.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_BUILD = os.path.join(_HERE, "_build")
+_SRC = os.path.join(_HERE, "oracle.c")
+
+_libs = {}
+
+
+def so_path(mutant=0):
+    name = "liboracle.so" if mutant == 0 else f"liboracle_mutant{mutant}.so"
+    return os.path.join(_BUILD, name)
+
+
+def build(mutant=0):
+    """Compile the oracle (or one of its planted-mistake mutants) with gcc."""
+    os.makedirs(_BUILD, exist_ok=True)
+    out = so_path(mutant)
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-fopenmp", "-ffp-contract=off",
+           "-fno-fast-math", f"-DORACLE_MUTANT={mutant}", "-o", out, _SRC, "-lm"]
+    subprocess.check_call(cmd)
+    return out
+
+
+def _load(mutant=0):
+    if mutant in _libs:
+        return _libs[mutant]
+    path = so_path(mutant)
+    if not os.path.exists(path) or os.path.getmtime(path) < os.path.getmtime(_SRC):
+        build(mutant)
+    lib = ctypes.CDLL(path)
+    p, i = ctypes.c_void_p, ctypes.c_int
+    lib.oracle_bf16_value.restype = ctypes.c_double
+    lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_rn.restype = ctypes.c_uint16
+    lib.oracle_bf16_rn.argtypes = [ctypes.c_double]
+    lib.oracle_bf16_ulp.restype = ctypes.c_double
+    lib.oracle_bf16_ulp.argtypes = [ctypes.c_double]
+    lib.oracle_pack_canonical.argtypes = [p, i, i, p]
+    lib.oracle_unpack_canonical.argtypes = [p, i, i, p]
+    lib.oracle_gemm.argtypes = [i, i, i, p, p, p, p, p, p, i]
+    lib.oracle_max_threads.restype = i
+    lib.oracle_packed_bytes.restype = ctypes.c_size_t
+    lib.oracle_packed_bytes.argtypes = [i, i]
+    lib.oracle_pack_tiled.argtypes = [p, p, p, i, i, p]
+    lib.oracle_unpack_tiled.argtypes = [p, i, i, p, p, p]
+    _libs[mutant] = lib
+    return lib
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+class Oracle:
+    """ctypes view of one build of the oracle (mutant 0 is the real one)."""
+
+    def __init__(self, mutant=0):
+        self.lib = _load(mutant)
+        self.mutant = mutant
+
+    # bf16
+    def bf16_value(self, bits):
+        return self.lib.oracle_bf16_value(int(bits))
+
+    def bf16_rn(self, v):
+        return int(self.lib.oracle_bf16_rn(float(v)))
+
+    def bf16_ulp(self, v):
+        return self.lib.oracle_bf16_ulp(float(v))
+
+    def bf16_ulp_array(self, v):
+        """Vectorised bf16_ulp: 2^(max(floor(log2|v|), -126) - 7), 2^-133 at 0."""
+        a = np.abs(np.asarray(v, dtype=np.float64))
+        _, e = np.frexp(a)                    # a = f * 2^e, f in [0.5, 1): floor(log2 a) = e - 1
+        ex = np.maximum(e.astype(np.int64) - 1, -126)
+        return np.where(a > 0, np.ldexp(1.0, ex - 7), np.ldexp(1.0, -133))
+
+    # canonical codes
+    def pack_canonical(self, q):
+        q, qp = _c(q, np.uint8)
+        K, N = q.shape
+        out = np.empty((K // 8, N), dtype=np.uint32)
+        self.lib.oracle_pack_canonical(qp, K, N, out.ctypes.data_as(ctypes.c_void_p))
+        return out
+
+    def unpack_canonical(self, codes):
+        codes, cp = _c(codes, np.uint32)
+        K, N = codes.shape[0] * 8, codes.shape[1]
+        out = np.empty((K, N), dtype=np.uint8)
+        self.lib.oracle_unpack_canonical(cp, K, N, out.ctypes.data_as(ctypes.c_void_p))
+        return out
+
+    # dequantise-then-multiply
+    def gemm(self, x, codes, scales, mins, nthreads=0):
+        """Return (y, a): y[M][N] in fp64 and a[M][N] = sum_k |x w|."""
+        x, xp = _c(x, np.uint16)
+        codes, cp = _c(codes, np.uint32)
+        scales, sp = _c(scales, np.uint16)
+        mins, mp = _c(mins, np.uint16)
+        M, K = x.shape
+        N = codes.shape[1]
+        assert codes.shape == (K // 8, N) and scales.shape == (K // 128, N) == mins.shape
+        y = np.empty((M, N), dtype=np.float64)
+        a = np.empty((M, N), dtype=np.float64)
+        self.lib.oracle_gemm(M, K, N, xp, cp, sp, mp, y.ctypes.data_as(ctypes.c_void_p),
+                             a.ctypes.data_as(ctypes.c_void_p), int(nthreads))
+        return y, a
+
+    def max_threads(self):
+        return int(self.lib.oracle_max_threads())
+
+    # tiled device layout
+    def packed_bytes(self, K, N):
+        return int(self.lib.oracle_packed_bytes(K, N))
+
+    def pack_tiled(self, codes, scales, mins):
+        codes, cp = _c(codes, np.uint32)
+        scales, sp = _c(scales, np.uint16)
+        mins, mp = _c(mins, np.uint16)
+        K, N = codes.shape[0] * 8, codes.shape[1]
+        out = np.empty(self.packed_bytes(K, N), dtype=np.uint8)
+        self.lib.oracle_pack_tiled(cp, sp, mp, K, N, out.ctypes.data_as(ctypes.c_void_p))
+        return out
+
+    def unpack_tiled(self, packed, K, N):
+        packed, pp = _c(packed, np.uint8)
+        codes = np.empty((K // 8, N), dtype=np.uint32)
+        scales = np.empty((K // 128, N), dtype=np.uint16)
+        mins = np.empty((K // 128, N), dtype=np.uint16)
+        self.lib.oracle_unpack_tiled(pp, K, N, codes.ctypes.data_as(ctypes.c_void_p),
+                                     scales.ctypes.data_as(ctypes.c_void_p),
+                                     mins.ctypes.data_as(ctypes.c_void_p))
+        return codes, scales, mins
+
+
+def accept(y_gpu, y_ref, a, oracle=None):
+    """Per-element acceptance |y_gpu - y_ref| <= 4e-3*a + ulp_bf16(y_ref).
+
+    Returns (ok_mask, ratio) where ratio = |err| / bound (<= 1 passes)."""
+    o = oracle or Oracle()
+    bound = 4e-3 * np.asarray(a, dtype=np.float64) + o.bf16_ulp_array(y_ref)
+    err = np.abs(np.asarray(y_gpu, dtype=np.float64) - np.asarray(y_ref, dtype=np.float64))
+    return err <= bound, err / bound
+
+
+def bf16_bits_to_f64(bits):
+    """uint16 bf16 bit patterns -> float64 (exact)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)

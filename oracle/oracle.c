@@ -1,0 +1,284 @@
+/*
+ * ORACLE for the int4-g128 weight-streaming GEMV.  TEST INFRASTRUCTURE ONLY:
+ * only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline leg may
+ * load this library.  The product path (int4_weight_only_g128_gb300) never
+ * calls it and shares no code with it.
+ *
+ * What it computes, written out as the plain definition in fp64:
+ *
+ *   Format (Token Rush README, intro bullet "4.25 bits per weight" and the
+ *   "Quantization" section): group-wise asymmetric int4, 128 consecutive
+ *   K-weights of a column share one bf16 scale and one bf16 minimum,
+ *        w[k][n] = min[k/128][n] + q[k][n] * scale[k/128][n],  q in 0..15,
+ *   which costs 4 + 32/128 = 4.25 bits per weight.
+ *
+ *   Product (Token Rush README, "bandwidth ceiling" paragraph: every decode
+ *   step reads all weights once; the M-row verify of the progress table,
+ *   steps 13-14 and 28):
+ *        y[m][n] = sum_k x[m][k] * w[k][n],   m < M <= 8,
+ *   with bf16 x and bf16 y.  The oracle keeps y in fp64 (no output rounding)
+ *   and sums in ascending k.  It also returns a[m][n] = sum_k |x[m][k]*w[k][n]|,
+ *   the scale of the acceptance bound |y_gpu - y| <= 4e-3*a + ulp_bf16(y).
+ *
+ * Readings the pages leave open:
+ *   - canonical code order: code k = 8j+i sits in bits 4i..4i+3 of word j of
+ *     column n, words stored [K/8][N] row-major;
+ *   - a group is 128 consecutive k of one column, k in [128g, 128g+128);
+ *   - "minimum" is an additive bf16 offset, not an integer zero point.
+ *
+ * Every bf16 -> double widening is exact, every dequantised weight is exact
+ * in fp64 (<= 12 significant bits in the product, well inside 53), so the
+ * only rounding in y is the fp64 summation.
+ *
+ * The tiled device layout (oracle_pack_tiled) is this library's own
+ * restatement of the packed format that include/w4g128.h specifies in prose;
+ * it is written from that specification and shares no code with the device
+ * packer.
+ *
+ * Mutants for negative-control tests (compile with -DORACLE_MUTANT=n):
+ *   1 = nibbles read in reversed order within a word,
+ *   2 = group index off by one (k = 128g is assigned to group g-1),
+ *   3 = the minimum term dropped.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+/* ---- bf16 ------------------------------------------------------------- */
+
+/* bf16 bit pattern -> exact double (bf16 is the top half of an fp32). */
+static double bf16_val(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+double oracle_bf16_value(uint16_t h) { return bf16_val(h); }
+
+/* Round a double to the nearest bf16 (ties to even), returning the bits.
+ * bf16 keeps 8 significant bits; its normal range is 2^-126 .. (2-2^-7)*2^127
+ * and its subnormals are multiples of 2^-133. */
+uint16_t oracle_bf16_rn(double v) {
+    if (isnan(v)) return 0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);                    /* a = f * 2^e, f in [0.5, 1) */
+    int ex = e - 1;                  /* floor(log2 a) */
+    if (ex < -126) ex = -126;        /* subnormal quantum is 2^-133 */
+    double quantum = ldexp(1.0, ex - 7);
+    double r = nearbyint(a / quantum) * quantum;  /* a/quantum is exact; ties to even */
+    if (r >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80);
+    float f = (float)r;              /* exact: r has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return (uint16_t)(sign | (u >> 16));
+}
+
+/* One unit in the last place of bf16 at v: 2^(max(floor(log2|v|), -126) - 7);
+ * 2^-133 at v = 0. */
+double oracle_bf16_ulp(double v) {
+    double a = fabs(v);
+    if (a == 0.0) return ldexp(1.0, -133);
+    int e;
+    frexp(a, &e);
+    int ex = e - 1;
+    if (ex < -126) ex = -126;
+    return ldexp(1.0, ex - 7);
+}
+
+/* ---- canonical codes ---------------------------------------------------- */
+
+static int code_at(const uint32_t* codes, int N, int k, int n) {
+    uint32_t word = codes[(size_t)(k / 8) * (size_t)N + (size_t)n];
+    int i = k % 8;
+#if ORACLE_MUTANT == 1
+    i = 7 - i;
+#endif
+    return (int)((word >> (4 * i)) & 0xFu);
+}
+
+static int group_of(int k) {
+#if ORACLE_MUTANT == 2
+    return k == 0 ? 0 : (k - 1) / 128;
+#else
+    return k / 128;
+#endif
+}
+
+/* q[K][N] (values 0..15) -> codes[K/8][N]. */
+void oracle_pack_canonical(const uint8_t* q, int K, int N, uint32_t* codes) {
+    for (int j = 0; j < K / 8; j++)
+        for (int n = 0; n < N; n++) {
+            uint32_t w = 0;
+            for (int i = 0; i < 8; i++)
+                w |= (uint32_t)(q[(size_t)(8 * j + i) * N + n] & 0xF) << (4 * i);
+            codes[(size_t)j * N + n] = w;
+        }
+}
+
+void oracle_unpack_canonical(const uint32_t* codes, int K, int N, uint8_t* q) {
+    for (int k = 0; k < K; k++)
+        for (int n = 0; n < N; n++)
+            q[(size_t)k * N + n] = (uint8_t)code_at(codes, N, k, n);
+}
+
+/* ---- dequantise, then multiply ------------------------------------------ */
+
+/* Dequantised weight, exact in fp64. */
+static double weight(const uint32_t* codes, const uint16_t* scales, const uint16_t* mins,
+                     int N, int k, int n) {
+    int g = group_of(k);
+    double s = bf16_val(scales[(size_t)g * N + n]);
+    double mn = bf16_val(mins[(size_t)g * N + n]);
+    double q = (double)code_at(codes, N, k, n);
+#if ORACLE_MUTANT == 3
+    mn = 0.0;
+#endif
+    return mn + q * s;
+}
+
+/* y[M][N] = x[M][K] . dequant(W)[K][N] and a[M][N] = sum_k |x w|, fp64,
+ * ascending k, one column at a time (the dequantised column is formed in
+ * full before it is multiplied).  nthreads <= 0 means "all available". */
+void oracle_gemm(int M, int K, int N, const uint16_t* x, const uint32_t* codes,
+                 const uint16_t* scales, const uint16_t* mins, double* y, double* a, int nthreads) {
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        double* col = (double*)malloc(sizeof(double) * (size_t)K);
+        double* xd = (double*)malloc(sizeof(double) * (size_t)K * (size_t)M);
+        for (size_t i = 0; i < (size_t)K * (size_t)M; i++) xd[i] = bf16_val(x[i]);
+#ifdef _OPENMP
+#pragma omp for schedule(static)
+#endif
+        for (int n = 0; n < N; n++) {
+            for (int k = 0; k < K; k++) col[k] = weight(codes, scales, mins, N, k, n);
+            for (int m = 0; m < M; m++) {
+                const double* xm = xd + (size_t)m * K;
+                double acc = 0.0, abs_acc = 0.0;
+                for (int k = 0; k < K; k++) {
+                    double p = xm[k] * col[k];
+                    acc += p;
+                    abs_acc += fabs(p);
+                }
+                y[(size_t)m * N + n] = acc;
+                if (a) a[(size_t)m * N + n] = abs_acc;
+            }
+        }
+        free(col);
+        free(xd);
+    }
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ---- the tiled device layout, restated from its specification ------------ */
+/*
+ * Specification (include/w4g128.h, "packed layout"): K % 128 == 0, N % 16 == 0,
+ * G = K/128 groups, T = N/16 column tiles.  Block (t, g) is 1088 bytes at
+ * offset (t*G + g)*1088.  Bytes [0, 1024) hold codes: half h (0, 1) at 512*h,
+ * lane l (0..31) at +16*l, little-endian word j (0..3) at +4*j.  With
+ * r = l / 4 and c = l % 4, word j covers rows k0 = 128g + 64h + 16j and holds
+ * in nibble p = 4*b + 2*a + e (bits 4p..4p+3) the code of row
+ * k0 + 2c + 8a + b of column 16t + r + 8e.  Bytes [1024, 1088) hold 8 entries
+ * of 8 bytes; entry r has the little-endian bf16 values scale, min of column
+ * 16t + r and scale, min of column 16t + r + 8, all for group g.
+ */
+
+size_t oracle_packed_bytes(int K, int N) {
+    return (size_t)(N / 16) * (size_t)(K / 128) * 1088u;
+}
+
+static void put_u16(uint8_t* p, uint16_t v) { p[0] = (uint8_t)(v & 0xFF); p[1] = (uint8_t)(v >> 8); }
+static uint16_t get_u16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+
+void oracle_pack_tiled(const uint32_t* codes, const uint16_t* scales, const uint16_t* mins,
+                       int K, int N, uint8_t* out) {
+    int G = K / 128, T = N / 16;
+    for (int t = 0; t < T; t++)
+        for (int g = 0; g < G; g++) {
+            uint8_t* blk = out + ((size_t)t * G + g) * 1088u;
+            for (int h = 0; h < 2; h++)
+                for (int l = 0; l < 32; l++) {
+                    int r = l / 4, c = l % 4;
+                    for (int j = 0; j < 4; j++) {
+                        int k0 = 128 * g + 64 * h + 16 * j;
+                        uint32_t word = 0;
+                        for (int p = 0; p < 8; p++) {
+                            int b = (p >> 2) & 1, a = (p >> 1) & 1, e = p & 1;
+                            int k = k0 + 2 * c + 8 * a + b;
+                            int n = 16 * t + r + 8 * e;
+                            uint32_t q = (codes[(size_t)(k / 8) * N + n] >> (4 * (k % 8))) & 0xFu;
+                            word |= q << (4 * p);
+                        }
+                        uint8_t* wp = blk + 512 * h + 16 * l + 4 * j;
+                        wp[0] = (uint8_t)(word & 0xFF);
+                        wp[1] = (uint8_t)((word >> 8) & 0xFF);
+                        wp[2] = (uint8_t)((word >> 16) & 0xFF);
+                        wp[3] = (uint8_t)(word >> 24);
+                    }
+                }
+            for (int r = 0; r < 8; r++) {
+                uint8_t* e = blk + 1024 + 8 * r;
+                size_t lo = (size_t)g * N + 16 * t + r, hi = lo + 8;
+                put_u16(e + 0, scales[lo]);
+                put_u16(e + 2, mins[lo]);
+                put_u16(e + 4, scales[hi]);
+                put_u16(e + 6, mins[hi]);
+            }
+        }
+}
+
+void oracle_unpack_tiled(const uint8_t* packed, int K, int N, uint32_t* codes,
+                         uint16_t* scales, uint16_t* mins) {
+    int G = K / 128, T = N / 16;
+    memset(codes, 0, sizeof(uint32_t) * (size_t)(K / 8) * N);
+    for (int t = 0; t < T; t++)
+        for (int g = 0; g < G; g++) {
+            const uint8_t* blk = packed + ((size_t)t * G + g) * 1088u;
+            for (int h = 0; h < 2; h++)
+                for (int l = 0; l < 32; l++) {
+                    int r = l / 4, c = l % 4;
+                    for (int j = 0; j < 4; j++) {
+                        const uint8_t* wp = blk + 512 * h + 16 * l + 4 * j;
+                        uint32_t word = (uint32_t)wp[0] | ((uint32_t)wp[1] << 8) |
+                                        ((uint32_t)wp[2] << 16) | ((uint32_t)wp[3] << 24);
+                        int k0 = 128 * g + 64 * h + 16 * j;
+                        for (int p = 0; p < 8; p++) {
+                            int b = (p >> 2) & 1, a = (p >> 1) & 1, e = p & 1;
+                            int k = k0 + 2 * c + 8 * a + b;
+                            int n = 16 * t + r + 8 * e;
+                            uint32_t q = (word >> (4 * p)) & 0xFu;
+                            codes[(size_t)(k / 8) * N + n] |= q << (4 * (k % 8));
+                        }
+                    }
+                }
+            for (int r = 0; r < 8; r++) {
+                const uint8_t* e = blk + 1024 + 8 * r;
+                size_t lo = (size_t)g * N + 16 * t + r, hi = lo + 8;
+                scales[lo] = get_u16(e + 0);
+                mins[lo] = get_u16(e + 2);
+                scales[hi] = get_u16(e + 4);
+                mins[hi] = get_u16(e + 6);
+            }
+        }
+}
