@@ -1,0 +1,172 @@
+/*
+ * w4g128 -- int4 weight-only, group-128 (int4-g128) weight-streaming GEMV for
+ * one NVIDIA GB300 GPU (sm_103a).  Plain C ABI: host/device pointers, sizes
+ * and a CUDA stream passed as void*.  No C++ exceptions cross it.
+ *
+ * The operation (Token Rush README: intro bullet "4.25 bits per weight" and
+ * the "Quantization" section define the format; the "bandwidth ceiling"
+ * paragraph and the progress table -- steps 3, 8-9, 13-14, 20, 28 -- define
+ * the decode GEMV, its split-K form, the M-row speculative verify and the
+ * lm_head row slice):
+ *
+ *     y[m][n] = bf16( sum_k x[m][k] * w[k][n] ),   w[k][n] = min[g][n] + q[k][n] * scale[g][n],
+ *     g = k / 128,  q in 0..15,  1 <= M <= 8,
+ *
+ * with bf16 x, scale, min and y, fp32 accumulation and one final
+ * round-to-nearest-even to bf16.  Results are accepted when
+ * |y - y_exact| <= 4e-3 * sum_k |x[m][k] w[k][n]| + one bf16 ulp of y_exact.
+ *
+ * ---------------------------------------------------------------------------
+ * CANONICAL INPUT FORMAT (what callers hand to w4g128_pack)
+ *   codes  uint32 [K/8][N] row-major: code of row k = 8j + i of column n is in
+ *          bits 4i..4i+3 of word (j, n).
+ *   scales bf16   [K/128][N] row-major, mins bf16 [K/128][N] row-major.
+ *   x      bf16   [M][K] row-major;  y  bf16 [M][N] row-major.
+ *   Shapes: K % 128 == 0, N % 16 == 0, 128 <= K <= 65536, 16 <= N <= 2^24.
+ *
+ * PACKED LAYOUT (what the kernels stream; exactly 4.25 bits per weight)
+ *   G = K/128 groups, T = N/16 column tiles of 16 columns, grouped into
+ *   quads of 4 tiles (64 columns); quad q holds nt(q) = min(4, T - 4q) tiles.
+ *   Each (tile t, group g) is a block of 1088 bytes.  Block (t, g), with
+ *   q = t / 4 and i = t % 4, starts at byte
+ *        q*G*4352 + g*nt(q)*1088 + i*1088,
+ *   so one quad's blocks for one group are contiguous, a quad is one
+ *   contiguous run over all groups, and the whole matrix is one sequential
+ *   stream in (quad, group) order.  The columns of the first Q' quads are a
+ *   contiguous byte prefix: a column slice of N' = 64*Q' columns (such as the
+ *   first 131072 lm_head rows) is used in place by passing N'.
+ *   Block bytes [0, 1024): codes.  Half h (0, 1) starts at 512*h; lane l
+ *   (0..31) at +16*l; little-endian uint32 word j (0..3) at +4*j.  With
+ *   r = l / 4, c = l % 4 and k0 = 128g + 64h + 16j, nibble p = 4b + 2a + e
+ *   (bits 4p..4p+3) of that word holds the code of row k0 + 2c + 8a + b of
+ *   column 16t + r + 8e.  (So one word is exactly the 16x16 weight operand
+ *   fragment one lane holds for a 16x8x16 warp MMA, and nibbles p and p+4 are
+ *   the two rows of one 32-bit operand register.)
+ *   Block bytes [1024, 1088): 8 entries of 8 bytes; entry r holds the
+ *   little-endian bf16 values scale, min of column 16t + r and scale, min of
+ *   column 16t + r + 8, for group g.
+ *
+ * WORKSPACE
+ *   Every compute call takes a caller-owned device workspace `ws` (16-byte
+ *   aligned, size from the matching *_workspace_bytes query).  It holds the
+ *   per-call activation package, split-K partial sums, arrival tickets and a
+ *   status word.  Each call re-initialises what it needs: no zeroing is
+ *   required, and the content after a call is unspecified except for the
+ *   status word (w4g128_workspace_status).  A workspace must not be used by
+ *   two calls that can run at the same time (e.g. on two streams).
+ *
+ * CONVENTIONS
+ *   - All array pointers are device pointers owned by the caller; nothing is
+ *     allocated by the library.  packed, ws: 16-byte aligned; x, y, codes,
+ *     scales, mins: 4-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  Argument errors are returned before anything is
+ *     launched.  Launch failures return W4G128_ERR_CUDA.
+ *   - Output is bitwise deterministic for a given shape and M (independent of
+ *     the grid size and of the SM count).
+ *   - x and y must not overlap; y must not overlap packed or ws.
+ *   - Finite inputs.  Products are exact in fp32 for every finite bf16 x.
+ */
+#ifndef W4G128_H
+#define W4G128_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define W4G128_API __attribute__((visibility("default")))
+#else
+#define W4G128_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  W4G128_OK = 0,
+  W4G128_ERR_INVALID_ARG = 1, /* null pointer, M outside 1..8, count outside 1..W4G128_MAX_MATRICES */
+  W4G128_ERR_SHAPE = 2,       /* K % 128, N % 16, or a size outside the limits above */
+  W4G128_ERR_ALIGN = 3,       /* a pointer is not aligned as required */
+  W4G128_ERR_WORKSPACE = 4,   /* ws_bytes smaller than the workspace query returns */
+  W4G128_ERR_CUDA = 5,        /* a CUDA runtime call or a launch failed */
+  W4G128_ERR_DEVICE = 6,      /* the current device is not compute capability 10.3 */
+  W4G128_ERR_TIMEOUT = 7      /* (status word only) a bounded device-side wait gave up */
+} w4g128_status;
+
+#define W4G128_MAX_M 8
+#define W4G128_MAX_MATRICES 512
+
+/* Raw bf16 bit pattern. */
+typedef uint16_t w4g128_bf16;
+
+/* Human-readable name of a status code (static string). */
+W4G128_API const char* w4g128_status_string(int status);
+
+/* Exact byte size of the packed form of a K x N matrix: K*N/2 + 4*(K/128)*N.
+ * Returns 0 for an invalid shape. */
+W4G128_API size_t w4g128_packed_bytes(int K, int N);
+
+/* Canonical -> packed layout (a bit permutation; bit-exact).  codes, scales,
+ * mins and packed are device pointers; packed must hold
+ * w4g128_packed_bytes(K, N) bytes.  Runs once per weight matrix, not per
+ * decode step. */
+W4G128_API int w4g128_pack(const uint32_t* codes, const w4g128_bf16* scales, const w4g128_bf16* mins,
+                           int K, int N, void* packed, void* stream);
+
+/* Exact inverse of w4g128_pack (for round-trip checks and export). */
+W4G128_API int w4g128_unpack(const void* packed, int K, int N, uint32_t* codes, w4g128_bf16* scales,
+                             w4g128_bf16* mins, void* stream);
+
+/* Workspace bytes needed by w4g128_gemm_verify(M, K, N) on the current
+ * device (w4g128_gemv is M = 1).  Returns 0 for invalid arguments. */
+W4G128_API size_t w4g128_workspace_bytes(int M, int K, int N);
+
+/* y[1][N] = x[1][K] . dequant(W): the batch-1 decode GEMV (CUDA cores,
+ * streamed by TMA bulk copies, split-K with a deterministic last-arriver
+ * reduction).  Token Rush README, progress table steps 3 and 8-9. */
+W4G128_API int w4g128_gemv(const void* packed, const w4g128_bf16* x, w4g128_bf16* y, int K, int N,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/* y[M][N] = x[M][K] . dequant(W) for 1 <= M <= 8: the speculative M-row
+ * verify step (one weight pass for M draft rows; tensor cores via warp MMA
+ * for M >= 2; M = 1 is the same computation as w4g128_gemv).  Token Rush
+ * README, progress table steps 13-14 and 28. */
+W4G128_API int w4g128_gemm_verify(const void* packed, const w4g128_bf16* x, w4g128_bf16* y, int M, int K,
+                                  int N, void* ws, size_t ws_bytes, void* stream);
+
+/* One matrix of a multi-matrix weight stream. */
+typedef struct {
+  const void* packed;     /* packed weights (device) */
+  const w4g128_bf16* x;   /* [M][K] activations (device) */
+  w4g128_bf16* y;         /* [M][N] output (device) */
+  int K;
+  int N;
+} w4g128_matrix;
+
+/* Workspace bytes for w4g128_decode_step over these matrices at this M. */
+W4G128_API size_t w4g128_decode_step_workspace_bytes(const w4g128_matrix* mats, int count, int M);
+
+/* Streams every matrix of `mats` (a HOST array of `count` descriptors,
+ * 1 <= count <= W4G128_MAX_MATRICES) in one persistent launch: y_i = x_i .
+ * dequant(W_i) for each i, as a whole decode step reads every weight once
+ * (Token Rush README, progress table step 4 and the "bandwidth ceiling"
+ * paragraph).  M = 1 uses the CUDA-core kernel, M >= 2 the warp-MMA kernel.
+ * The split-K segments (512 rows) and their summation order depend only on
+ * each matrix's shape, so every y_i is bitwise identical to what a separate
+ * w4g128_gemv (M = 1) or w4g128_gemm_verify call returns, whatever the SM
+ * count or the other matrices.  The descriptor array is read during the call
+ * and may be reused afterwards. */
+W4G128_API int w4g128_decode_step(const w4g128_matrix* mats, int count, int M, void* ws, size_t ws_bytes,
+                                  void* stream);
+
+/* Reads the status word the last call on `ws` left (W4G128_OK, or
+ * W4G128_ERR_TIMEOUT if a bounded device wait gave up).  Synchronises
+ * `stream`. */
+W4G128_API int w4g128_workspace_status(const void* ws, int* status_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4G128_H */

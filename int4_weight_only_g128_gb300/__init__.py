@@ -1,0 +1,190 @@
+"""Python binding of libw4g128, the int4-g128 weight-streaming GEMV for GB300.
+
+Argument marshalling only: every function forwards to the C entry point of
+the same name in ``include/*.h``; every step of the computation runs in the
+library's CUDA kernels.  Tensors are passed as device pointers taken from
+``torch.Tensor.data_ptr()`` (plain integers are accepted as raw pointers), and
+the stream defaults to torch's current CUDA stream.  There is no CPU fallback:
+if the library cannot be built or loaded, the first call raises.
+"""
+import ctypes
+import os
+
+__all__ = [
+    "W4G128Error", "lib", "exported_symbols",
+    "w4g128_status_string", "w4g128_packed_bytes", "w4g128_pack", "w4g128_unpack",
+    "w4g128_workspace_bytes", "w4g128_gemv", "w4g128_gemm_verify",
+    "w4g128_decode_step_workspace_bytes", "w4g128_decode_step", "w4g128_workspace_status",
+    "w4g128_probe_read", "w4g128_probe_copy", "w4g128_probe_sink_bytes",
+    "MAX_M", "MAX_MATRICES",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
+MAX_M = 8
+MAX_MATRICES = 512
+
+_lib = None
+
+
+class W4G128Error(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {status} ({w4g128_status_string(status)})")
+
+
+class _Matrix(ctypes.Structure):
+    _fields_ = [("packed", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("K", ctypes.c_int), ("N", ctypes.c_int)]
+
+
+def exported_symbols():
+    """Names of every function the public headers (include/*.h) declare."""
+    names = []
+    for fn in sorted(os.listdir(_INCLUDE)):
+        if not fn.endswith(".h"):
+            continue
+        with open(os.path.join(_INCLUDE, fn)) as f:
+            for line in f:
+                line = line.strip()
+                if line.startswith("W4G128_API") and "(" in line:
+                    names.append(line.split("(")[0].split()[-1].lstrip("*"))
+    return names
+
+
+def lib():
+    """Load libw4g128.so (building it in-tree if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    from . import build as _build
+    path = _build.LIB
+    if not os.path.exists(path):
+        _build.build()
+    L = ctypes.CDLL(path)
+    p, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    L.w4g128_status_string.restype = ctypes.c_char_p
+    L.w4g128_status_string.argtypes = [i]
+    L.w4g128_packed_bytes.restype = sz
+    L.w4g128_packed_bytes.argtypes = [i, i]
+    L.w4g128_pack.restype = i
+    L.w4g128_pack.argtypes = [p, p, p, i, i, p, p]
+    L.w4g128_unpack.restype = i
+    L.w4g128_unpack.argtypes = [p, i, i, p, p, p, p]
+    L.w4g128_workspace_bytes.restype = sz
+    L.w4g128_workspace_bytes.argtypes = [i, i, i]
+    L.w4g128_gemv.restype = i
+    L.w4g128_gemv.argtypes = [p, p, p, i, i, p, sz, p]
+    L.w4g128_gemm_verify.restype = i
+    L.w4g128_gemm_verify.argtypes = [p, p, p, i, i, i, p, sz, p]
+    L.w4g128_decode_step_workspace_bytes.restype = sz
+    L.w4g128_decode_step_workspace_bytes.argtypes = [ctypes.POINTER(_Matrix), i, i]
+    L.w4g128_decode_step.restype = i
+    L.w4g128_decode_step.argtypes = [ctypes.POINTER(_Matrix), i, i, p, sz, p]
+    L.w4g128_workspace_status.restype = i
+    L.w4g128_workspace_status.argtypes = [p, ctypes.POINTER(ctypes.c_int), p]
+    L.w4g128_probe_read.restype = i
+    L.w4g128_probe_read.argtypes = [p, sz, p, p]
+    L.w4g128_probe_copy.restype = i
+    L.w4g128_probe_copy.argtypes = [p, p, sz, p]
+    L.w4g128_probe_sink_bytes.restype = sz
+    L.w4g128_probe_sink_bytes.argtypes = []
+    _lib = L
+    return L
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise W4G128Error(fn, rc)
+
+
+def w4g128_status_string(status):
+    return lib().w4g128_status_string(int(status)).decode()
+
+
+def w4g128_packed_bytes(K, N):
+    return int(lib().w4g128_packed_bytes(K, N))
+
+
+def w4g128_pack(codes, scales, mins, K, N, packed, stream=None):
+    _check("w4g128_pack", lib().w4g128_pack(_ptr(codes), _ptr(scales), _ptr(mins), K, N, _ptr(packed),
+                                            _stream(stream)))
+
+
+def w4g128_unpack(packed, K, N, codes, scales, mins, stream=None):
+    _check("w4g128_unpack", lib().w4g128_unpack(_ptr(packed), K, N, _ptr(codes), _ptr(scales), _ptr(mins),
+                                                _stream(stream)))
+
+
+def w4g128_workspace_bytes(M, K, N):
+    return int(lib().w4g128_workspace_bytes(M, K, N))
+
+
+def w4g128_gemv(packed, x, y, K, N, ws, ws_bytes=None, stream=None):
+    wb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    _check("w4g128_gemv", lib().w4g128_gemv(_ptr(packed), _ptr(x), _ptr(y), K, N, _ptr(ws), wb, _stream(stream)))
+
+
+def w4g128_gemm_verify(packed, x, y, M, K, N, ws, ws_bytes=None, stream=None):
+    wb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    _check("w4g128_gemm_verify", lib().w4g128_gemm_verify(_ptr(packed), _ptr(x), _ptr(y), M, K, N, _ptr(ws), wb,
+                                                          _stream(stream)))
+
+
+def _matrices(mats):
+    arr = (_Matrix * len(mats))()
+    for i, (packed, x, y, K, N) in enumerate(mats):
+        arr[i] = _Matrix(_ptr(packed), _ptr(x), _ptr(y), K, N)
+    return arr
+
+
+def w4g128_decode_step_workspace_bytes(mats, M):
+    """mats: sequence of (packed, x, y, K, N)."""
+    arr = _matrices(mats)
+    return int(lib().w4g128_decode_step_workspace_bytes(arr, len(mats), M))
+
+
+def w4g128_decode_step(mats, M, ws, ws_bytes=None, stream=None):
+    """mats: sequence of (packed, x, y, K, N); one persistent launch for all."""
+    arr = _matrices(mats)
+    wb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    _check("w4g128_decode_step", lib().w4g128_decode_step(arr, len(mats), M, _ptr(ws), wb, _stream(stream)))
+
+
+def w4g128_workspace_status(ws, stream=None):
+    out = ctypes.c_int(0)
+    _check("w4g128_workspace_status", lib().w4g128_workspace_status(_ptr(ws), ctypes.byref(out), _stream(stream)))
+    return out.value
+
+
+def w4g128_probe_sink_bytes():
+    return int(lib().w4g128_probe_sink_bytes())
+
+
+def w4g128_probe_read(buf, nbytes, sink, stream=None):
+    _check("w4g128_probe_read", lib().w4g128_probe_read(_ptr(buf), nbytes, _ptr(sink), _stream(stream)))
+
+
+def w4g128_probe_copy(src, dst, nbytes, stream=None):
+    _check("w4g128_probe_copy", lib().w4g128_probe_copy(_ptr(src), _ptr(dst), nbytes, _stream(stream)))

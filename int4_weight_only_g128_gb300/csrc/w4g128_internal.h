@@ -1,0 +1,55 @@
+// Internal declarations shared by the translation units of libw4g128.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "w4g128.h"
+
+namespace w4g128 {
+
+constexpr int kGroup = 128;          // K-rows per scale/min group
+constexpr int kTileN = 16;           // columns per packed tile
+constexpr int kCodeBytes = 1024;     // codes of one (tile, group) block
+constexpr int kBlockBytes = 1088;    // codes + 8 metadata entries of 8 bytes
+constexpr int kQuadTiles = 4;        // tiles a warp streams together (64 columns)
+constexpr int kSegGroups = 4;        // groups per fixed split-K segment (512 rows)
+constexpr int kQuadBytes = kQuadTiles * kBlockBytes;  // one full quad, one group
+
+// Byte offset of block (tile t, group g) in the packed layout: quads of 4
+// tiles are contiguous runs over all groups, and one quad's tiles for one
+// group are adjacent.  T = N/16 tiles, G = K/128 groups.
+__host__ __device__ inline long long block_offset(int t, int g, int G, int T) {
+  const int q = t / kQuadTiles, i = t % kQuadTiles;
+  const int nt = (T - kQuadTiles * q) < kQuadTiles ? (T - kQuadTiles * q) : kQuadTiles;
+  return static_cast<long long>(q) * G * kQuadBytes + static_cast<long long>(g) * nt * kBlockBytes +
+         static_cast<long long>(i) * kBlockBytes;
+}
+
+int launch_pack(const uint32_t* codes, const uint16_t* scales, const uint16_t* mins, int K, int N,
+                void* packed, cudaStream_t stream);
+int launch_unpack(const void* packed, int K, int N, uint32_t* codes, uint16_t* scales, uint16_t* mins,
+                  cudaStream_t stream);
+
+// One matrix of a streaming call, as the host hands it over.
+struct HostMatrix {
+  const void* packed;
+  const uint16_t* x;
+  uint16_t* y;
+  int K, N;
+};
+
+// Workspace bytes for streaming these matrices at this M on the current device.
+// Returns 0 on invalid arguments.
+size_t stream_workspace_bytes(const HostMatrix* mats, int count, int M);
+
+// Launches the prep and streaming kernels; the API layer validates arguments.
+int launch_stream(const HostMatrix* mats, int count, int M, void* ws, size_t ws_bytes,
+                  cudaStream_t stream);
+
+int read_workspace_status(const void* ws, int* status_out, cudaStream_t stream);
+
+// Current device is compute capability 10.3; caches per device.
+bool device_is_sm103();
+
+}  // namespace w4g128

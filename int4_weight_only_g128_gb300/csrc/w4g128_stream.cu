@@ -1,0 +1,797 @@
+// The weight-streaming kernels: y_i = x_i . dequant(W_i) for a list of
+// int4-g128 matrices, M = 1 on CUDA cores and M <= 8 on the warp-level MMA.
+//
+// Design (sm_103a, one GPU):
+//  * The work is a flat list of items (matrix, 64-column quad, segment of 4
+//    groups = 512 rows).  A persistent grid gives each warp a contiguous,
+//    balanced range of items ("stream-K").  Segment boundaries are fixed by
+//    the shape alone, and every output is the left fold, over segments in
+//    order, of fixed-order segment sums -- so y depends on neither the grid,
+//    the SM count nor which other matrices share the call.
+//  * Each warp streams its chunks (one group x one quad = up to 4 adjacent
+//    blocks of 1088 bytes, plus that group's activation package) through a
+//    private ring of shared-memory slots filled by 1-D TMA bulk copies
+//    (cp.async.bulk) and completed on per-slot mbarriers.  Within a matrix a
+//    warp's range is one sequential byte stream.  No block-wide barrier exists
+//    after launch, so warps never wait on each other.
+//  * A quad owned wholly by one warp is written straight to y.  A quad split
+//    between warps is reduced by whichever warp arrives last (an atomic
+//    ticket; nobody waits): it folds the segment partials in segment order.
+//  * A small prep kernel (launched first; the streaming kernel overlaps it by
+//    programmatic dependent launch) turns x into per-group packages in the
+//    order the lanes consume them, with the group sums the factorised
+//    dequantisation needs, and zeroes the tickets and the status word.
+//
+// Dequantisation uses the factorised form of w = min + q*scale over a group g:
+//     sum_{k in g} x_k w_kn = scale_gn * sum_k x_k q_kn + min_gn * X_g,
+//     X_g = sum_{k in g} x_k
+// (Token Rush README, "Quantization": 128 weights per bf16 scale and minimum).
+// Codes are turned into the bf16 values 128 + q with one LOP3 per pair (a
+// magic-number conversion), so sum_k x_k (128 + q_k) is accumulated with exact
+// products and the 128 X_g offset is folded into the minimum term:
+//     scale * S_g + (min - 128 scale) * X_g,   S_g = sum_k x_k (128 + q_k).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+#include <vector>
+
+#include "w4g128_internal.h"
+#include "w4g128_ptx.cuh"
+
+namespace w4g128 {
+namespace {
+
+// ----------------------------------------------------------------- modes
+
+enum Mode : int {
+  kM1 = 0,   // M = 1, CUDA cores: bf16 x bf16 -> fp32 FMA on the dequantised pairs
+  kMMA = 1,  // M <= 8, warp MMA m16n8k16 bf16 -> f32 with the weights as the 16-row operand
+};
+
+#ifndef W4G128_WARPS_PER_CTA
+#define W4G128_WARPS_PER_CTA 8
+#endif
+#ifndef W4G128_RING_DEPTH
+#define W4G128_RING_DEPTH 2
+#endif
+constexpr int kNW = W4G128_WARPS_PER_CTA;  // warps per CTA
+constexpr int kDepth = W4G128_RING_DEPTH;  // ring slots per warp
+
+// Activation package per group: rows x 4 lane classes c x (16 bf16-pair
+// words + X_c + 3 pad) = rows x 320 bytes, then 8 fp32 group sums X_g[row].
+// Row (m, c) word 2i holds x[m][k0+2c], x[m][k0+2c+1] and word 2i+1 holds
+// x[m][k0+2c+8], x[m][k0+2c+9] for k0 = 128g + 16i: exactly the bf16 operand
+// pairs lane class c multiplies (the MMA B fragment of row m).  The 80-byte
+// stride keeps the 16-byte loads of 8 lanes on distinct bank groups.
+template <int MODE> struct Pkg;
+template <> struct Pkg<kM1> { static constexpr int kRows = 1, kRowBytes = 320, kBytes = 352; };
+template <> struct Pkg<kMMA> { static constexpr int kRows = 8, kRowBytes = 320, kBytes = 2592; };
+
+template <int MODE>
+__host__ __device__ constexpr int slot_bytes() { return kQuadTiles * kBlockBytes + Pkg<MODE>::kBytes; }
+constexpr int kBarBytes = ((kNW * kDepth * 8 + 127) / 128) * 128;  // kNW * kDepth mbarriers
+template <int MODE>
+__host__ __device__ constexpr int smem_bytes() { return kBarBytes + kNW * kDepth * slot_bytes<MODE>(); }
+
+static_assert(slot_bytes<kM1>() % 16 == 0 && slot_bytes<kMMA>() % 16 == 0, "bulk copies need 16-byte slots");
+static_assert((kDepth & (kDepth - 1)) == 0, "ring depth must be a power of two");
+
+// ----------------------------------------------------------------- parameters
+
+struct MatParams {
+  const uint8_t* packed;
+  uint8_t* xpkg;        // this matrix's activation packages (in the workspace)
+  const uint16_t* x;
+  uint16_t* y;
+  long long item_begin;  // first item of this matrix in the flat list
+  int K, N;
+  int quad_begin;        // first ticket of this matrix
+  int g_begin;           // first (matrix, group) package index of this matrix
+};
+
+template <int MAXMAT>
+struct StreamParams {
+  long long total_items;
+  float* partials;       // [total_items][rows][64]: one slot per (matrix, quad, segment)
+  unsigned* tickets;     // [total_quads]
+  unsigned* status;
+  int count, M, W, total_quads, total_groups;
+  MatParams mats[MAXMAT];
+};
+
+static_assert(sizeof(StreamParams<W4G128_MAX_MATRICES>) <= 32000, "kernel parameter limit");
+
+__host__ __device__ constexpr int div_up(int a, int b) { return (a + b - 1) / b; }
+
+// ----------------------------------------------------------------- cursor
+
+// Position of one chunk (matrix mi, quad q, segment s, group g) in the flat
+// list, with the current matrix's sizes and both source pointers cached so
+// that moving to the next chunk is a few increments: within a matrix the
+// packed bytes are read strictly sequentially.
+struct Cursor {
+  long long item;
+  const uint8_t* src;   // this chunk's weight blocks
+  const uint8_t* xsrc;  // this chunk's activation package
+  int mi, q, s, g, g_end;
+  int G, S, NQ, T, ntiles;
+};
+
+template <int MAXMAT>
+__device__ __forceinline__ void cursor_load(Cursor& c, const StreamParams<MAXMAT>& p, int mi) {
+  const MatParams& m = p.mats[mi];
+  c.mi = mi;
+  c.G = m.K / kGroup;
+  c.S = div_up(c.G, kSegGroups);
+  c.T = m.N / kTileN;
+  c.NQ = div_up(c.T, kQuadTiles);
+}
+
+template <int MODE, int MAXMAT>
+__device__ __forceinline__ void cursor_seek(Cursor& c, const StreamParams<MAXMAT>& p, long long item) {
+  int lo = 0, hi = p.count - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.mats[mid].item_begin <= item) lo = mid; else hi = mid - 1;
+  }
+  cursor_load(c, p, lo);
+  const long long local = item - p.mats[lo].item_begin;
+  c.item = item;
+  c.q = static_cast<int>(local / c.S);
+  c.s = static_cast<int>(local - static_cast<long long>(c.q) * c.S);
+  c.g = c.s * kSegGroups;
+  c.g_end = min(c.g + kSegGroups, c.G);
+  c.ntiles = min(kQuadTiles, c.T - kQuadTiles * c.q);
+  c.src = p.mats[lo].packed + static_cast<long long>(c.q) * c.G * kQuadBytes +
+          static_cast<long long>(c.g) * c.ntiles * kBlockBytes;
+  c.xsrc = p.mats[lo].xpkg + static_cast<long long>(c.g) * Pkg<MODE>::kBytes;
+}
+
+template <int MODE, int MAXMAT>
+__device__ __forceinline__ void cursor_next(Cursor& c, const StreamParams<MAXMAT>& p) {
+  c.src += c.ntiles * kBlockBytes;
+  c.xsrc += Pkg<MODE>::kBytes;
+  if (++c.g < c.g_end) return;
+  ++c.item;
+  if (++c.s < c.S) {
+    c.g_end = min(c.g + kSegGroups, c.G);
+    return;
+  }
+  c.s = 0;
+  c.g = 0;
+  if (++c.q < c.NQ) {  // the next quad starts where this one ended
+    c.ntiles = min(kQuadTiles, c.T - kQuadTiles * c.q);
+    c.xsrc = p.mats[c.mi].xpkg;
+    c.g_end = min(kSegGroups, c.G);
+    return;
+  }
+  if (c.mi + 1 == p.count) return;  // past the end; never dereferenced
+  cursor_load(c, p, c.mi + 1);
+  c.q = 0;
+  c.ntiles = min(kQuadTiles, c.T);
+  c.src = p.mats[c.mi].packed;
+  c.xsrc = p.mats[c.mi].xpkg;
+  c.g_end = min(kSegGroups, c.G);
+}
+
+// Owner warp of an item under the balanced split [floor(wI/W), floor((w+1)I/W)).
+__device__ __forceinline__ int owner_of(long long item, long long I, int W) {
+  return static_cast<int>(((item + 1) * W + I - 1) / I) - 1;
+}
+
+// ----------------------------------------------------------------- chunk copy
+
+// The chunk (quad q, group g) is nt(q) adjacent blocks: one bulk copy.
+template <int MODE>
+__device__ __forceinline__ void issue_weights(const Cursor& c, uint32_t slot, uint32_t bar, uint64_t pol) {
+  mbar_arrive_expect_tx(bar, c.ntiles * kBlockBytes + Pkg<MODE>::kBytes);
+  bulk_g2s(slot, c.src, c.ntiles * kBlockBytes, bar, pol);
+}
+
+template <int MODE>
+__device__ __forceinline__ void issue_package(const Cursor& c, uint32_t slot, uint32_t bar, uint64_t pol) {
+  bulk_g2s(slot + kQuadTiles * kBlockBytes, c.xsrc, Pkg<MODE>::kBytes, bar, pol);
+}
+
+// ----------------------------------------------------------------- in-register dequantisation
+
+// Word layout (per lane r = l/4, c = l%4): nibble p = 4b + 2a + e holds row
+// 2c + 8a + b of column r + 8e.  LOP3 with the bf16 magic 0x4300 turns the
+// nibbles at bits 0..3 and 16..19 of (w >> 4s) into the bf16 pair
+// (128 + q_lo, 128 + q_hi); each half is multiplied by the matching bf16 x and
+// accumulated in fp32 (the products are exact).
+__device__ __forceinline__ float fma_bf16_pair(uint32_t wq, uint32_t xx, float acc) {
+  asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+      "mov.b32 {wl, wh}, %1;\n\t"
+      "mov.b32 {xl, xh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, wl, xl, %0;\n\t"
+      "fma.rn.f32.bf16 %0, wh, xh, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(wq), "r"(xx));
+  return acc;
+}
+
+__device__ __forceinline__ void dq_word(uint32_t w, uint32_t xa, uint32_t xb, float& lo, float& hi) {
+  const uint32_t r0 = lop3_and_or(w, 0x000F000Fu, 0x43004300u);        // rows 2c, 2c+1   col r
+  const uint32_t r1 = lop3_and_or(w >> 4, 0x000F000Fu, 0x43004300u);   // rows 2c, 2c+1   col r+8
+  const uint32_t r2 = lop3_and_or(w >> 8, 0x000F000Fu, 0x43004300u);   // rows 2c+8, 2c+9 col r
+  const uint32_t r3 = lop3_and_or(w >> 12, 0x000F000Fu, 0x43004300u);  // rows 2c+8, 2c+9 col r+8
+  lo = fma_bf16_pair(r0, xa, lo);
+  hi = fma_bf16_pair(r1, xa, hi);
+  lo = fma_bf16_pair(r2, xb, lo);
+  hi = fma_bf16_pair(r3, xb, hi);
+}
+
+// Warp MMA: D[16 cols x 8 rows] += A[16 cols x 16 k] * B[16 k x 8 rows]; the
+// four LOP3 outputs of one packed word are exactly this lane's A fragment.
+__device__ __forceinline__ void mma_word(uint32_t w, uint32_t xa, uint32_t xb, float (&d)[4]) {
+  const uint32_t a0 = lop3_and_or(w, 0x000F000Fu, 0x43004300u);
+  const uint32_t a1 = lop3_and_or(w >> 4, 0x000F000Fu, 0x43004300u);
+  const uint32_t a2 = lop3_and_or(w >> 8, 0x000F000Fu, 0x43004300u);
+  const uint32_t a3 = lop3_and_or(w >> 12, 0x000F000Fu, 0x43004300u);
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(xa), "r"(xb));
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ uint16_t to_bf16(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+
+// Rows of the per-lane accumulators: M = 1 keeps (column r, column r+8);
+// the MMA keeps (r, 2c), (r, 2c+1), (r+8, 2c), (r+8, 2c+1).
+template <int MODE> struct Acc { static constexpr int kN = (MODE == kMMA) ? 4 : 2; };
+
+// One chunk: every tile of the quad for one group, added into seg[t][*].
+// FULL: the quad has all 4 tiles, so the tiles form one straight-line block
+// the compiler can interleave.
+template <int MODE, bool FULL>
+__device__ __forceinline__ void compute_chunk(const uint8_t* sl, int ntiles, int lane,
+                                              float (&seg)[kQuadTiles][Acc<MODE>::kN]) {
+  const int r = lane >> 2, c = lane & 3;
+  const uint8_t* pk = sl + kQuadTiles * kBlockBytes;
+  const int row = (MODE == kMMA) ? r : 0;
+  const uint32_t* xr = reinterpret_cast<const uint32_t*>(pk + row * Pkg<MODE>::kRowBytes + c * 80);
+  uint32_t xw[16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 v = reinterpret_cast<const uint4*>(xr)[i];
+    xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
+  }
+  if constexpr (MODE == kM1) {
+    const float Xc = __uint_as_float(xr[16]);
+#pragma unroll
+    for (int t = 0; t < kQuadTiles; ++t) {
+      if (FULL || t < ntiles) {
+        const uint8_t* blk = sl + t * kBlockBytes;
+        const uint4 u0 = *reinterpret_cast<const uint4*>(blk + 16 * lane);
+        const uint4 u1 = *reinterpret_cast<const uint4*>(blk + 512 + 16 * lane);
+        const uint2 me = *reinterpret_cast<const uint2*>(blk + kCodeBytes + 8 * r);
+        float lo = 0.f, hi = 0.f;  // sum_k x_k (128 + q_k) over this lane's rows, columns r and r+8
+        dq_word(u0.x, xw[0], xw[1], lo, hi);
+        dq_word(u0.y, xw[2], xw[3], lo, hi);
+        dq_word(u0.z, xw[4], xw[5], lo, hi);
+        dq_word(u0.w, xw[6], xw[7], lo, hi);
+        dq_word(u1.x, xw[8], xw[9], lo, hi);
+        dq_word(u1.y, xw[10], xw[11], lo, hi);
+        dq_word(u1.z, xw[12], xw[13], lo, hi);
+        dq_word(u1.w, xw[14], xw[15], lo, hi);
+        const float sl0 = bf16_lo(me.x), sh0 = bf16_lo(me.y);
+        const float ml0 = fmaf(-128.f, sl0, bf16_hi(me.x));   // min - 128 scale, exact
+        const float mh0 = fmaf(-128.f, sh0, bf16_hi(me.y));
+        seg[t][0] = fmaf(sl0, lo, fmaf(ml0, Xc, seg[t][0]));
+        seg[t][1] = fmaf(sh0, hi, fmaf(mh0, Xc, seg[t][1]));
+      }
+    }
+  } else {
+    const float2 Xg = *reinterpret_cast<const float2*>(pk + Pkg<MODE>::kRows * Pkg<MODE>::kRowBytes + 8 * c);
+#pragma unroll
+    for (int t = 0; t < kQuadTiles; ++t) {
+      if (FULL || t < ntiles) {
+        const uint8_t* blk = sl + t * kBlockBytes;
+        const uint4 u0 = *reinterpret_cast<const uint4*>(blk + 16 * lane);
+        const uint4 u1 = *reinterpret_cast<const uint4*>(blk + 512 + 16 * lane);
+        const uint2 me = *reinterpret_cast<const uint2*>(blk + kCodeBytes + 8 * r);
+        // sum_k (128 + q) x over the group as (column, row) fragments, two chains
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_word(u0.x, xw[0], xw[1], d0);
+        mma_word(u0.y, xw[2], xw[3], d1);
+        mma_word(u0.z, xw[4], xw[5], d0);
+        mma_word(u0.w, xw[6], xw[7], d1);
+        mma_word(u1.x, xw[8], xw[9], d0);
+        mma_word(u1.y, xw[10], xw[11], d1);
+        mma_word(u1.z, xw[12], xw[13], d0);
+        mma_word(u1.w, xw[14], xw[15], d1);
+        const float sl0 = bf16_lo(me.x), sh0 = bf16_lo(me.y);
+        const float ml0 = fmaf(-128.f, sl0, bf16_hi(me.x));
+        const float mh0 = fmaf(-128.f, sh0, bf16_hi(me.y));
+        seg[t][0] = fmaf(sl0, d0[0] + d1[0], fmaf(ml0, Xg.x, seg[t][0]));
+        seg[t][1] = fmaf(sl0, d0[1] + d1[1], fmaf(ml0, Xg.y, seg[t][1]));
+        seg[t][2] = fmaf(sh0, d0[2] + d1[2], fmaf(mh0, Xg.x, seg[t][2]));
+        seg[t][3] = fmaf(sh0, d0[3] + d1[3], fmaf(mh0, Xg.y, seg[t][3]));
+      }
+    }
+  }
+}
+
+// Select v[t][e] for a runtime t without local memory.
+template <int NA>
+__device__ __forceinline__ float pick(const float (&v)[kQuadTiles][NA], int t, int e) {
+  float out = v[0][e];
+#pragma unroll
+  for (int i = 1; i < kQuadTiles; ++i) out = (t == i) ? v[i][e] : out;
+  return out;
+}
+
+// ----------------------------------------------------------------- the streaming kernel
+
+template <int MODE, int MAXMAT>
+__global__ void __launch_bounds__(kNW * 32, 2) stream_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int NA = Acc<MODE>::kN;
+  constexpr int kSlot = slot_bytes<MODE>();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = lane >> 2, c = lane & 3;
+  const int wg = blockIdx.x * kNW + warp;
+  if (wg >= p.W) return;  // whole warp; there are no block-wide barriers
+
+  const long long I = p.total_items;
+  const long long it_a = I * wg / p.W, it_b = I * (wg + 1) / p.W;
+
+  const uint32_t bar0 = smem_addr(smem) + warp * kDepth * 8;
+  const uint32_t ring0 = smem_addr(smem) + kBarBytes + warp * kDepth * kSlot;
+  const uint8_t* ring = smem + kBarBytes + warp * kDepth * kSlot;
+
+  uint64_t pol_w = 0, pol_x = 0;
+  if (lane == 0) {
+#pragma unroll
+    for (int d = 0; d < kDepth; ++d) mbar_init(bar0 + 8 * d, 1);
+    fence_mbar_init();
+    pol_w = l2_policy_evict_first();
+    pol_x = l2_policy_evict_last();
+  }
+  __syncwarp();
+
+  Cursor cc, ic;  // compute cursor, issue cursor
+  cursor_seek<MODE>(cc, p, it_a);
+  ic = cc;
+  // Prologue: the weight bytes do not depend on the prep kernel, so start them
+  // before waiting for it; the activation packages follow after the wait.
+  // Every lane walks the cursors; lane 0 alone issues copies.
+  Cursor pre[kDepth];
+  int n_pre = 0;
+#pragma unroll
+  for (int d = 0; d < kDepth; ++d) {
+    if (ic.item < it_b) {
+      if (lane == 0) issue_weights<MODE>(ic, ring0 + d * kSlot, bar0 + 8 * d, pol_w);
+      pre[d] = ic;
+      ++n_pre;
+      cursor_next<MODE>(ic, p);
+    }
+  }
+  grid_dependency_wait();
+  if (lane == 0) {
+#pragma unroll
+    for (int d = 0; d < kDepth; ++d)
+      if (d < n_pre) issue_package<MODE>(pre[d], ring0 + d * kSlot, bar0 + 8 * d, pol_x);
+  }
+  unsigned issued = static_cast<unsigned>(n_pre);
+
+  float seg[kQuadTiles][NA];
+  float tot[kQuadTiles][NA];
+#pragma unroll
+  for (int t = 0; t < kQuadTiles; ++t)
+#pragma unroll
+    for (int e = 0; e < NA; ++e) seg[t][e] = tot[t][e] = 0.f;
+
+  unsigned done = 0;  // chunks consumed
+  while (cc.item < it_b) {
+    const int slot = static_cast<int>(done % kDepth);
+    const uint32_t parity = (done / kDepth) & 1u;
+    if (!mbar_wait_bounded(bar0 + 8 * slot, parity)) {
+      // Give up: record the timeout, drain this warp's copies in flight
+      // (again bounded) and leave.  Quads this warp shared stay unreduced.
+      if (lane == 0) {
+        atomicCAS(p.status, 0u, static_cast<unsigned>(W4G128_ERR_TIMEOUT));
+        for (unsigned k = done + 1; k < issued; ++k)
+          (void)mbar_wait_bounded(bar0 + 8 * static_cast<int>(k % kDepth), (k / kDepth) & 1u);
+      }
+      __syncwarp();
+      return;
+    }
+    const int ntiles = cc.ntiles;
+    // M = 1: a straight-line body for full quads lets the compiler interleave
+    // the four tiles; the MMA path keeps per-tile blocks (register budget).
+    if (MODE != kMMA && ntiles == kQuadTiles)
+      compute_chunk<MODE, true>(ring + slot * kSlot, ntiles, lane, seg);
+    else
+      compute_chunk<MODE, false>(ring + slot * kSlot, ntiles, lane, seg);
+
+    // Slot consumed: refill it with the chunk kDepth ahead.
+    __syncwarp();
+    if (ic.item < it_b) {
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        const uint32_t sa = ring0 + slot * kSlot, ba = bar0 + 8 * slot;
+        issue_weights<MODE>(ic, sa, ba, pol_w);
+        issue_package<MODE>(ic, sa, ba, pol_x);
+      }
+      cursor_next<MODE>(ic, p);
+      ++issued;
+    }
+    ++done;
+
+    if (cc.g + 1 == cc.g_end) {
+      // ---- end of a segment
+      const MatParams& m = p.mats[cc.mi];
+      const int S = cc.S;
+      const long long q_first = m.item_begin + static_cast<long long>(cc.q) * S;
+      const long long q_last = q_first + S - 1;
+      const bool owned = (q_first >= it_a) && (q_last < it_b);
+      if constexpr (MODE != kMMA) {
+        // reduce the 4 lane classes c of each column (same tree on every lane)
+#pragma unroll
+        for (int t = 0; t < kQuadTiles; ++t)
+#pragma unroll
+          for (int e = 0; e < NA; ++e) {
+            float v = seg[t][e];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            seg[t][e] = v;
+          }
+      }
+      const int rows = (MODE == kMMA) ? p.M : 1;
+      if (owned) {
+#pragma unroll
+        for (int t = 0; t < kQuadTiles; ++t)
+#pragma unroll
+          for (int e = 0; e < NA; ++e) tot[t][e] = (cc.s == 0) ? seg[t][e] : tot[t][e] + seg[t][e];
+      } else {
+        float* part = p.partials + cc.item * rows * 64;  // one slot per (matrix, quad, segment)
+        if constexpr (MODE != kMMA) {
+          // lane (r, c) stores tile c's columns r and r + 8
+          if (c < ntiles) {
+            part[16 * c + r] = pick(seg, c, 0);
+            part[16 * c + r + 8] = pick(seg, c, 1);
+          }
+        } else {
+#pragma unroll
+          for (int t = 0; t < kQuadTiles; ++t) {
+            if (t < ntiles) {
+              if (2 * c < rows) {
+                part[(2 * c) * 64 + 16 * t + r] = seg[t][0];
+                part[(2 * c) * 64 + 16 * t + r + 8] = seg[t][2];
+              }
+              if (2 * c + 1 < rows) {
+                part[(2 * c + 1) * 64 + 16 * t + r] = seg[t][1];
+                part[(2 * c + 1) * 64 + 16 * t + r + 8] = seg[t][3];
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kQuadTiles; ++t)
+#pragma unroll
+        for (int e = 0; e < NA; ++e) seg[t][e] = 0.f;
+
+      const bool quad_end = (cc.s == S - 1) || (cc.item + 1 == it_b);
+      if (quad_end) {
+        const int n0 = kQuadTiles * kTileN * cc.q;
+        if (owned) {
+          if constexpr (MODE != kMMA) {
+            if (c < ntiles) {
+              m.y[n0 + 16 * c + r] = to_bf16(pick(tot, c, 0));
+              m.y[n0 + 16 * c + r + 8] = to_bf16(pick(tot, c, 1));
+            }
+          } else {
+#pragma unroll
+            for (int t = 0; t < kQuadTiles; ++t) {
+              if (t < ntiles) {
+                const int n = n0 + 16 * t + r;
+                if (2 * c < rows) {
+                  m.y[(2 * c) * m.N + n] = to_bf16(tot[t][0]);
+                  m.y[(2 * c) * m.N + n + 8] = to_bf16(tot[t][2]);
+                }
+                if (2 * c + 1 < rows) {
+                  m.y[(2 * c + 1) * m.N + n] = to_bf16(tot[t][1]);
+                  m.y[(2 * c + 1) * m.N + n + 8] = to_bf16(tot[t][3]);
+                }
+              }
+            }
+          }
+        } else {
+          // Split quad: publish, take a ticket; the last arriver folds the
+          // segment partials in segment order and writes y.
+          __threadfence();
+          __syncwarp();
+          const int wf = owner_of(q_first, I, p.W), wl = owner_of(q_last, I, p.W);
+          const unsigned expected = static_cast<unsigned>(wl - wf + 1);
+          unsigned* ticket = p.tickets + m.quad_begin + cc.q;
+          unsigned prev = 0;
+          if (lane == 0) prev = atomicAdd(ticket, 1u);
+          prev = __shfl_sync(0xffffffffu, prev, 0);
+          if (prev + 1 == expected) {
+            __threadfence();
+            const float* part = p.partials + q_first * rows * 64;
+            const int ncols = ntiles * kTileN;
+            for (int rr = 0; rr < rows; ++rr) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int col = lane + 32 * h;
+                if (col < ncols) {
+                  // issue the loads of 8 segments at a time, then fold them in segment order
+                  float acc = 0.f;
+                  for (int s0 = 0; s0 < S; s0 += 8) {
+                    float v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                      v[u] = (s0 + u < S) ? __ldcg(part + (static_cast<long long>(s0 + u) * rows + rr) * 64 + col)
+                                          : 0.f;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                      if (s0 + u < S) acc = (s0 + u == 0) ? v[u] : acc + v[u];
+                  }
+                  m.y[static_cast<long long>(rr) * m.N + n0 + col] = to_bf16(acc);
+                }
+              }
+            }
+            if (lane == 0) *ticket = 0u;  // ready for the next call
+          }
+        }
+      }
+    }
+    cursor_next<MODE>(cc, p);
+  }
+}
+
+// ----------------------------------------------------------------- prep kernel
+
+// One warp per (matrix, group): lane (row, c) builds row `row` / lane class c
+// of the group's activation package; lanes c == 0 add the group sum X_g.
+template <int MODE, int MAXMAT>
+__global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
+  grid_dependents_launch();
+  const int tid = blockIdx.x * blockDim.x + threadIdx.x, nthreads = gridDim.x * blockDim.x;
+  for (int i = tid; i < p.total_quads; i += nthreads) p.tickets[i] = 0u;
+  if (tid == 0) *p.status = 0u;
+
+  constexpr int kRows = Pkg<MODE>::kRows;
+  const int lane = threadIdx.x & 31;
+  const int row = lane >> 2, c = lane & 3;
+  const int warp0 = tid >> 5, nwarps = nthreads >> 5;
+  for (int wg = warp0; wg < p.total_groups; wg += nwarps) {
+    int lo = 0, hi = p.count - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.mats[mid].g_begin <= wg) lo = mid; else hi = mid - 1;
+    }
+    const MatParams& m = p.mats[lo];
+    const int g = wg - m.g_begin;
+    uint8_t* out = m.xpkg + static_cast<long long>(g) * Pkg<MODE>::kBytes;
+    float X = 0.f;
+    if (row < kRows) {
+      uint32_t w[20];
+      if (row < p.M) {
+        const uint16_t* xr = m.x + static_cast<long long>(row) * m.K;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int k0 = kGroup * g + 16 * i;
+          const uint16_t x0 = xr[k0 + 2 * c], x1 = xr[k0 + 2 * c + 1];
+          const uint16_t x8 = xr[k0 + 2 * c + 8], x9 = xr[k0 + 2 * c + 9];
+          w[2 * i] = static_cast<uint32_t>(x0) | (static_cast<uint32_t>(x1) << 16);
+          w[2 * i + 1] = static_cast<uint32_t>(x8) | (static_cast<uint32_t>(x9) << 16);
+          X = (((X + bf16_lo(x0)) + bf16_lo(x1)) + bf16_lo(x8)) + bf16_lo(x9);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = 0u;
+      }
+      w[16] = __float_as_uint(X);
+      w[17] = w[18] = w[19] = 0u;
+      uint4* o = reinterpret_cast<uint4*>(out + row * Pkg<MODE>::kRowBytes + c * 80);
+#pragma unroll
+      for (int i = 0; i < 5; ++i) o[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    }
+    // group sum of row `row`: ((X_0 + X_1) + X_2) + X_3 over its four lane classes
+    const float X0 = __shfl_sync(0xffffffffu, X, lane & ~3);
+    const float X1 = __shfl_sync(0xffffffffu, X, (lane & ~3) + 1);
+    const float X2 = __shfl_sync(0xffffffffu, X, (lane & ~3) + 2);
+    const float X3 = __shfl_sync(0xffffffffu, X, (lane & ~3) + 3);
+    if (c == 0) {
+      float* xg = reinterpret_cast<float*>(out + kRows * Pkg<MODE>::kRowBytes);
+      xg[row] = (row < kRows) ? ((X0 + X1) + X2) + X3 : 0.f;
+    }
+  }
+}
+
+// ----------------------------------------------------------------- host planning
+
+struct DeviceInfo {
+  int sms = 0;
+  int occ[2] = {0, 0};  // CTAs per SM per mode
+  bool ok = false;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+bool g_dev_init[64] = {false};
+
+template <int MODE>
+void setup_mode(DeviceInfo& d) {
+  const int smem = smem_bytes<MODE>();
+  cudaFuncSetAttribute(stream_kernel<MODE, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaFuncSetAttribute(stream_kernel<MODE, W4G128_MAX_MATRICES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       smem);
+  int occ1 = 0, occ2 = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ1, stream_kernel<MODE, 1>, kNW * 32, smem);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, stream_kernel<MODE, W4G128_MAX_MATRICES>, kNW * 32, smem);
+  const int occ = std::min(occ1, occ2);
+  d.occ[MODE] = occ > 0 ? occ : 1;
+}
+
+const DeviceInfo* device_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_dev_init[dev]) {
+    DeviceInfo d;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    d.ok = (major == 10 && minor == 3);
+    if (d.ok) {
+      setup_mode<kM1>(d);
+      setup_mode<kMMA>(d);
+      if (cudaGetLastError() != cudaSuccess) d.ok = false;
+    }
+    g_dev[dev] = d;
+    g_dev_init[dev] = true;
+  }
+  return &g_dev[dev];
+}
+
+struct Plan {
+  int mode = 0, rows = 1, pkg = 0;
+  long long items = 0;
+  int W = 0, grid = 0, total_quads = 0, total_groups = 0;
+  size_t off_tickets = 0, off_xpkg = 0, off_partials = 0, bytes = 0;
+  std::vector<long long> item_begin, xpkg_off;
+  std::vector<int> quad_begin, g_begin;
+};
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool make_plan(const HostMatrix* mats, int count, int M, const DeviceInfo& dev, Plan& pl) {
+  pl.mode = (M == 1) ? kM1 : kMMA;
+  pl.rows = M;
+  pl.pkg = (pl.mode == kM1) ? Pkg<kM1>::kBytes : Pkg<kMMA>::kBytes;
+  pl.item_begin.resize(count);
+  pl.quad_begin.resize(count);
+  pl.g_begin.resize(count);
+  pl.xpkg_off.resize(count);
+  long long items = 0, xbytes = 0, quads = 0, groups = 0;
+  for (int i = 0; i < count; ++i) {
+    const int G = mats[i].K / kGroup, S = div_up(G, kSegGroups), NQ = div_up(mats[i].N, kTileN * kQuadTiles);
+    pl.item_begin[i] = items;
+    pl.quad_begin[i] = static_cast<int>(quads);
+    pl.g_begin[i] = static_cast<int>(groups);
+    pl.xpkg_off[i] = xbytes;
+    items += static_cast<long long>(NQ) * S;
+    quads += NQ;
+    groups += G;
+    xbytes += static_cast<long long>(G) * pl.pkg;
+    if (quads > 0x7FFFFFFF || groups > 0x7FFFFFFF) return false;
+  }
+  pl.items = items;
+  pl.total_quads = static_cast<int>(quads);
+  pl.total_groups = static_cast<int>(groups);
+  const long long max_warps = static_cast<long long>(dev.sms) * dev.occ[pl.mode] * kNW;
+  pl.W = static_cast<int>(std::min<long long>(items, max_warps));
+  pl.grid = div_up(pl.W, kNW);
+  pl.off_tickets = 256;
+  pl.off_xpkg = align_up(pl.off_tickets + sizeof(unsigned) * static_cast<size_t>(quads), 256);
+  pl.off_partials = align_up(pl.off_xpkg + static_cast<size_t>(xbytes), 256);
+  pl.bytes = align_up(pl.off_partials + sizeof(float) * static_cast<size_t>(items) * pl.rows * 64, 256);
+  return true;
+}
+
+template <int MAXMAT>
+void fill_params(StreamParams<MAXMAT>& sp, const HostMatrix* mats, int count, int M, const Plan& pl, void* ws) {
+  auto* base = static_cast<uint8_t*>(ws);
+  sp.total_items = pl.items;
+  sp.partials = reinterpret_cast<float*>(base + pl.off_partials);
+  sp.tickets = reinterpret_cast<unsigned*>(base + pl.off_tickets);
+  sp.status = reinterpret_cast<unsigned*>(base);
+  sp.count = count;
+  sp.M = M;
+  sp.W = pl.W;
+  sp.total_quads = pl.total_quads;
+  sp.total_groups = pl.total_groups;
+  for (int i = 0; i < count; ++i) {
+    MatParams& m = sp.mats[i];
+    m.packed = static_cast<const uint8_t*>(mats[i].packed);
+    m.xpkg = base + pl.off_xpkg + pl.xpkg_off[i];
+    m.x = mats[i].x;
+    m.y = mats[i].y;
+    m.item_begin = pl.item_begin[i];
+    m.K = mats[i].K;
+    m.N = mats[i].N;
+    m.quad_begin = pl.quad_begin[i];
+    m.g_begin = pl.g_begin[i];
+  }
+}
+
+template <int MODE, int MAXMAT>
+int launch_mode(const StreamParams<MAXMAT>& sp, int grid, cudaStream_t stream) {
+  const int prep_blocks = std::max(1, std::min(div_up(sp.total_groups * 32, 256), 1024));
+  prep_kernel<MODE, MAXMAT><<<prep_blocks, 256, 0, stream>>>(sp);
+  if (cudaGetLastError() != cudaSuccess) return W4G128_ERR_CUDA;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kNW * 32);
+  cfg.dynamicSmemBytes = smem_bytes<MODE>();
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, stream_kernel<MODE, MAXMAT>, sp) != cudaSuccess) {
+    cudaGetLastError();
+    return W4G128_ERR_CUDA;
+  }
+  return W4G128_OK;
+}
+
+template <int MAXMAT>
+int launch_with(const HostMatrix* mats, int count, int M, const Plan& pl, void* ws, cudaStream_t stream) {
+  static thread_local StreamParams<MAXMAT> sp;  // large for MAXMAT = 512: keep it off the stack
+  fill_params(sp, mats, count, M, pl, ws);
+  if (pl.mode == kMMA) return launch_mode<kMMA>(sp, pl.grid, stream);
+  return launch_mode<kM1>(sp, pl.grid, stream);
+}
+
+}  // namespace
+
+bool device_is_sm103() {
+  const DeviceInfo* d = device_info();
+  return d != nullptr && d->ok;
+}
+
+size_t stream_workspace_bytes(const HostMatrix* mats, int count, int M) {
+  const DeviceInfo* d = device_info();
+  if (d == nullptr || !d->ok) return 0;
+  Plan pl;
+  if (!make_plan(mats, count, M, *d, pl)) return 0;
+  return pl.bytes;
+}
+
+int launch_stream(const HostMatrix* mats, int count, int M, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  const DeviceInfo* d = device_info();
+  if (d == nullptr || !d->ok) return W4G128_ERR_DEVICE;
+  Plan pl;
+  if (!make_plan(mats, count, M, *d, pl)) return W4G128_ERR_SHAPE;
+  if (ws_bytes < pl.bytes) return W4G128_ERR_WORKSPACE;
+  if (count == 1) return launch_with<1>(mats, count, M, pl, ws, stream);
+  return launch_with<W4G128_MAX_MATRICES>(mats, count, M, pl, ws, stream);
+}
+
+int read_workspace_status(const void* ws, int* status_out, cudaStream_t stream) {
+  unsigned v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return W4G128_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return W4G128_ERR_CUDA;
+  *status_out = static_cast<int>(v);
+  return W4G128_OK;
+}
+
+}  // namespace w4g128

@@ -194,15 +194,23 @@ int oracle_max_threads(void) {
 /* ---- the tiled device layout, restated from its specification ------------ */
 /*
  * Specification (include/w4g128.h, "packed layout"): K % 128 == 0, N % 16 == 0,
- * G = K/128 groups, T = N/16 column tiles.  Block (t, g) is 1088 bytes at
- * offset (t*G + g)*1088.  Bytes [0, 1024) hold codes: half h (0, 1) at 512*h,
- * lane l (0..31) at +16*l, little-endian word j (0..3) at +4*j.  With
- * r = l / 4 and c = l % 4, word j covers rows k0 = 128g + 64h + 16j and holds
- * in nibble p = 4*b + 2*a + e (bits 4p..4p+3) the code of row
- * k0 + 2c + 8a + b of column 16t + r + 8e.  Bytes [1024, 1088) hold 8 entries
- * of 8 bytes; entry r has the little-endian bf16 values scale, min of column
- * 16t + r and scale, min of column 16t + r + 8, all for group g.
+ * G = K/128 groups, T = N/16 column tiles, quads of 4 tiles, quad q holding
+ * nt(q) = min(4, T - 4q) tiles.  Block (t, g) is 1088 bytes at offset
+ * q*G*4352 + g*nt(q)*1088 + i*1088 with q = t/4, i = t%4.  Bytes [0, 1024)
+ * hold codes: half h (0, 1) at 512*h, lane l (0..31) at +16*l, little-endian
+ * word j (0..3) at +4*j.  With r = l / 4 and c = l % 4, word j covers rows
+ * k0 = 128g + 64h + 16j and holds in nibble p = 4*b + 2*a + e (bits 4p..4p+3)
+ * the code of row k0 + 2c + 8a + b of column 16t + r + 8e.  Bytes
+ * [1024, 1088) hold 8 entries of 8 bytes; entry r has the little-endian bf16
+ * values scale, min of column 16t + r and scale, min of column 16t + r + 8,
+ * all for group g.
  */
+
+static size_t block_offset(int t, int g, int G, int T) {
+    int q = t / 4, i = t % 4;
+    int nt = T - 4 * q < 4 ? T - 4 * q : 4;
+    return (size_t)q * (size_t)G * 4352u + (size_t)g * (size_t)nt * 1088u + (size_t)i * 1088u;
+}
 
 size_t oracle_packed_bytes(int K, int N) {
     return (size_t)(N / 16) * (size_t)(K / 128) * 1088u;
@@ -216,7 +224,7 @@ void oracle_pack_tiled(const uint32_t* codes, const uint16_t* scales, const uint
     int G = K / 128, T = N / 16;
     for (int t = 0; t < T; t++)
         for (int g = 0; g < G; g++) {
-            uint8_t* blk = out + ((size_t)t * G + g) * 1088u;
+            uint8_t* blk = out + block_offset(t, g, G, T);
             for (int h = 0; h < 2; h++)
                 for (int l = 0; l < 32; l++) {
                     int r = l / 4, c = l % 4;
@@ -254,7 +262,7 @@ void oracle_unpack_tiled(const uint8_t* packed, int K, int N, uint32_t* codes,
     memset(codes, 0, sizeof(uint32_t) * (size_t)(K / 8) * N);
     for (int t = 0; t < T; t++)
         for (int g = 0; g < G; g++) {
-            const uint8_t* blk = packed + ((size_t)t * G + g) * 1088u;
+            const uint8_t* blk = packed + block_offset(t, g, G, T);
             for (int h = 0; h < 2; h++)
                 for (int l = 0; l < 32; l++) {
                     int r = l / 4, c = l % 4;

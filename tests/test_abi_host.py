@@ -1,0 +1,106 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and loads,
+exports every function the headers declare, and rejects bad arguments
+synchronously, before anything is launched."""
+import ctypes
+
+import pytest
+
+import int4_weight_only_g128_gb300 as w
+
+E_INVALID, E_SHAPE, E_ALIGN, E_WS, E_CUDA, E_DEVICE, E_TIMEOUT = 1, 2, 3, 4, 5, 6, 7
+
+
+@pytest.fixture(scope="module")
+def L():
+    return w.lib()
+
+
+def test_every_header_symbol_is_exported(L):
+    names = w.exported_symbols()
+    assert len(names) == 13
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_packed_bytes_exact():
+    assert w.w4g128_packed_bytes(4096, 4096) == 4096 * 4096 // 2 + 4 * 32 * 4096 == 8912896
+    assert w.w4g128_packed_bytes(5120, 248320) == 675430400
+    assert w.w4g128_packed_bytes(5120, 131072) == 356515840
+    assert w.w4g128_packed_bytes(17408, 5120) == 47349760
+    for K, N in [(128, 16), (5120, 34816)]:
+        assert w.w4g128_packed_bytes(K, N) * 32 == K * N * 17
+    for K, N in [(100, 16), (128, 8), (0, 16), (128, 0), (128, 24), (65536 + 128, 16)]:
+        assert w.w4g128_packed_bytes(K, N) == 0
+
+
+def test_status_strings():
+    for s in range(8):
+        assert isinstance(w.w4g128_status_string(s), str) and w.w4g128_status_string(s)
+    assert "unknown" in w.w4g128_status_string(99)
+
+
+FAKE = 0x10000  # a 16-byte-aligned non-null address that is never dereferenced on these paths
+
+
+def test_gemv_argument_errors(L):
+    assert L.w4g128_gemv(None, FAKE, FAKE, 128, 16, FAKE, 1 << 20, None) == E_INVALID
+    assert L.w4g128_gemv(FAKE, FAKE, FAKE, 100, 16, FAKE, 1 << 20, None) == E_SHAPE
+    assert L.w4g128_gemv(FAKE, FAKE, FAKE, 128, 24, FAKE, 1 << 20, None) == E_SHAPE
+    assert L.w4g128_gemv(FAKE + 8, FAKE, FAKE, 128, 16, FAKE, 1 << 20, None) == E_ALIGN
+    assert L.w4g128_gemv(FAKE, FAKE + 2, FAKE, 128, 16, FAKE, 1 << 20, None) == E_ALIGN
+    assert L.w4g128_gemv(FAKE, FAKE, FAKE, 128, 16, FAKE + 4, 1 << 20, None) == E_ALIGN
+    assert L.w4g128_gemv(FAKE, FAKE, FAKE, 128, 16, None, 1 << 20, None) == E_INVALID
+
+
+def test_verify_argument_errors(L):
+    for M in (0, 9, -1):
+        assert L.w4g128_gemm_verify(FAKE, FAKE, FAKE, M, 128, 16, FAKE, 1 << 20, None) == E_INVALID
+
+
+def test_decode_step_argument_errors(L):
+    mats = (w._Matrix * 2)()
+    mats[0] = w._Matrix(FAKE, FAKE, FAKE, 128, 16)
+    mats[1] = w._Matrix(FAKE, FAKE, FAKE, 256, 48)
+    assert L.w4g128_decode_step(mats, 0, 1, FAKE, 1 << 20, None) == E_INVALID
+    assert L.w4g128_decode_step(mats, 513, 1, FAKE, 1 << 20, None) == E_INVALID
+    assert L.w4g128_decode_step(None, 1, 1, FAKE, 1 << 20, None) == E_INVALID
+    mats[1] = w._Matrix(FAKE, FAKE, FAKE, 256, 40)
+    assert L.w4g128_decode_step(mats, 2, 1, FAKE, 1 << 20, None) == E_SHAPE
+    mats[1] = w._Matrix(FAKE, FAKE, None, 256, 48)
+    assert L.w4g128_decode_step(mats, 2, 1, FAKE, 1 << 20, None) == E_INVALID
+
+
+def test_pack_argument_errors(L):
+    assert L.w4g128_pack(None, FAKE, FAKE, 128, 16, FAKE, None) == E_INVALID
+    assert L.w4g128_pack(FAKE, FAKE, FAKE, 128, 17, FAKE, None) == E_SHAPE
+    assert L.w4g128_pack(FAKE, FAKE, FAKE, 128, 16, FAKE + 4, None) == E_ALIGN
+    assert L.w4g128_unpack(FAKE, 128, 16, FAKE, FAKE + 1, FAKE, None) == E_ALIGN
+
+
+def test_probe_argument_errors(L):
+    assert L.w4g128_probe_read(None, 16, FAKE, None) == E_INVALID
+    assert L.w4g128_probe_read(FAKE, 15, FAKE, None) == E_SHAPE
+    assert L.w4g128_probe_copy(FAKE, FAKE + 8, 16, None) == E_ALIGN
+
+
+def test_workspace_queries_reject_bad_shapes(L):
+    assert w.w4g128_workspace_bytes(0, 128, 16) == 0
+    assert w.w4g128_workspace_bytes(1, 127, 16) == 0
+    assert w.w4g128_decode_step_workspace_bytes([(FAKE, FAKE, FAKE, 128, 15)], 1) == 0
+
+
+def test_no_device_is_reported_not_faked():
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    L = w.lib()
+    assert L.w4g128_gemv(FAKE, FAKE, FAKE, 128, 16, FAKE, 1 << 20, None) == E_DEVICE
+    assert L.w4g128_pack(FAKE, FAKE, FAKE, 128, 16, FAKE, None) == E_DEVICE
+    assert w.w4g128_workspace_bytes(1, 128, 16) == 0
+
+
+def test_error_raises_in_binding():
+    with pytest.raises(w.W4G128Error) as ei:
+        w.w4g128_gemv(FAKE, FAKE, FAKE, 100, 16, FAKE, ws_bytes=1 << 20, stream=0)
+    assert ei.value.status == E_SHAPE
+    assert ctypes.sizeof(w._Matrix) == 32

@@ -309,7 +309,7 @@ def read_tiled_golden():
 
 
 def test_tiled_hand_positions(O):
-    K, N = 256, 32
+    K, N = 256, 96
     code_rows, meta_rows = read_tiled_golden()
     for k, n, byte, half in code_rows:
         q = np.zeros((K, N), dtype=np.uint8)
@@ -342,16 +342,29 @@ def test_tiled_round_trip_and_size(O):
 
 
 def test_tiled_column_prefix_is_byte_prefix(O):
-    """Packing the first N' columns gives the first bytes of the full packing."""
+    """Packing the first N' = 64*Q' columns gives the first bytes of the full packing."""
     rng = np.random.default_rng(14)
-    K, N = 256, 64
+    K, N = 256, 208
     c = rng.integers(0, 2**32, size=(K // 8, N), dtype=np.uint32)
     s = rng.integers(0, 2**16, size=(K // 128, N), dtype=np.uint16)
     m = rng.integers(0, 2**16, size=(K // 128, N), dtype=np.uint16)
     full = O.pack_tiled(c, s, m)
-    for Np in (16, 32, 48):
+    for Np in (64, 128, 192):
         pre = O.pack_tiled(c[:, :Np], s[:, :Np], m[:, :Np])
         assert np.array_equal(pre, full[:pre.size])
+
+
+def test_tiled_quad_is_one_contiguous_run(O):
+    """All bytes of the columns of quad q occupy [q*G*4352, (q+1)*G*4352)."""
+    K, N = 384, 128
+    G = K // 128
+    for q in range(N // 64):
+        cc = np.zeros((K // 8, N), np.uint32)
+        cc[:, 64 * q:64 * q + 64] = 0xFFFFFFFF
+        z = np.zeros((G, N), np.uint16)
+        packed = O.pack_tiled(cc, z, z)
+        nz = np.nonzero(packed)[0]
+        assert nz.min() >= q * G * 4352 and nz.max() < (q + 1) * G * 4352
 
 
 def test_tiled_each_word_holds_two_columns_of_one_lane(O):
