@@ -1,0 +1,74 @@
+"""M-row speculative verify (w4g128_gemm_verify, 1 <= M <= 8) against the fp64
+oracle, plus exact cases and row consistency."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+import synth  # noqa: E402
+from gpu_helpers import SEED, DevMatrix, check_against_oracle, run  # noqa: E402
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M", [2, 3, 4, 5, 7, 8])
+@pytest.mark.parametrize("K,N", [(128, 16), (640, 80), (1152, 208), (4096, 4096)])
+def test_verify_matches_oracle(M, K, N):
+    mat = DevMatrix(K, N, matrix_id=N + M)
+    x = synth.x(SEED, 1000 + M, M, K)
+    check_against_oracle(run(mat, x), x, mat.codes, mat.scales, mat.mins)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("K,N", [(5120, 6144), (6144, 5120), (5120, 34816), (17408, 5120)])
+def test_verify_projection_shapes_m8(K, N):
+    mat = DevMatrix(K, N, matrix_id=N + 8)
+    x = synth.x(SEED, 2000 + K, 8, K)
+    check_against_oracle(run(mat, x), x, mat.codes, mat.scales, mat.mins)
+
+
+@pytest.mark.gpu
+def test_verify_exact_integer_case_bit_exact():
+    rng = np.random.default_rng(31)
+    O = oracle.Oracle()
+    K, N, M = 1024, 144, 8
+    q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
+    codes = O.pack_canonical(q)
+    s = np.full((K // 128, N), 0x3F80, np.uint16)
+    m = np.full((K // 128, N), 0xC100, np.uint16)  # -8.0
+    x = (rng.integers(-4, 5, size=(M, K)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    y = run(DevMatrix(K, N, codes, s, m), x)
+    y_ref, _ = O.gemm(x, codes, s, m)
+    expect = np.array([O.bf16_rn(v) for v in y_ref.ravel()], dtype=np.uint16).reshape(M, N)
+    assert np.array_equal(y, expect)
+
+
+@pytest.mark.gpu
+def test_verify_identical_rows_give_identical_outputs():
+    K, N = 2048, 512
+    mat = DevMatrix(K, N, matrix_id=4)
+    x1 = synth.x(SEED, 4, 1, K)
+    x = np.repeat(x1, 8, axis=0)
+    y = run(mat, x)
+    for r in range(1, 8):
+        assert np.array_equal(y[r], y[0])
+
+
+@pytest.mark.gpu
+def test_verify_rows_independent_of_m():
+    """Row m of an M-row verify does not depend on the other rows or on M (M >= 2)."""
+    K, N = 1152, 208
+    mat = DevMatrix(K, N, matrix_id=6)
+    x8 = synth.x(SEED, 6, 8, K)
+    y8 = run(mat, x8)
+    for M in (2, 5):
+        yM = run(mat, x8[:M])
+        assert np.array_equal(yM, y8[:M])
+
+
+@pytest.mark.gpu
+def test_verify_deterministic():
+    K, N = 5120, 6144
+    mat = DevMatrix(K, N, matrix_id=8)
+    x = synth.x(SEED, 8, 8, K)
+    assert np.array_equal(run(mat, x), run(mat, x))
