@@ -56,9 +56,10 @@
  *   two calls that can run at the same time (e.g. on two streams).
  *
  * CONVENTIONS
- *   - All array pointers are device pointers owned by the caller; nothing is
- *     allocated by the library.  packed, ws: 16-byte aligned; x, y, codes,
- *     scales, mins: 4-byte aligned.
+ *   - All array pointers are device pointers owned by the caller; the library
+ *     allocates nothing per call (the only device memory it holds is the
+ *     fixed scratch array behind w4g128_gemv_noalloc).  packed, ws: 16-byte
+ *     aligned; x, y, codes, scales, mins: 4-byte aligned.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream).  Argument errors are returned before anything is
  *     launched.  Launch failures return W4G128_ERR_CUDA.
@@ -159,6 +160,28 @@ W4G128_API size_t w4g128_decode_step_workspace_bytes(const w4g128_matrix* mats, 
  * and may be reused afterwards. */
 W4G128_API int w4g128_decode_step(const w4g128_matrix* mats, int count, int M, void* ws, size_t ws_bytes,
                                   void* stream);
+
+/* Size of the fixed device scratch array behind w4g128_gemv_noalloc (16 MiB). */
+#define W4G128_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* The pages have no counterpart to this entry point; it is a convenience of
+ * this library.  Same result as w4g128_gemv (the same kernels, bit for bit),
+ * for callers that cannot give the library a workspace because they must not
+ * allocate device memory: plugin hooks of another runtime that owns the
+ * device memory budget, fixed-pool serving processes, and latency-critical
+ * threads that must not call cudaMalloc/cudaFree (those calls can synchronise
+ * the device).  It allocates no device memory: the workspace is a fixed
+ * W4G128_NOALLOC_SCRATCH_BYTES array that every GPU loading the library holds
+ * until the process exits.  Shapes whose workspace would exceed it (the
+ * limit is reached near K*N = 2^31 weights; a 5120 x 248320 lm_head needs
+ * 10 MB) return W4G128_ERR_WORKSPACE before anything is launched.  The first
+ * call on each device looks up the array's device address; make that first
+ * call before any stream capture.  All calls share the one array, so calls
+ * that can overlap on the GPU (other streams, other host threads) race and
+ * corrupt each other; serialise them.  The status word of the last call is
+ * not readable through w4g128_workspace_status. */
+W4G128_API int w4g128_gemv_noalloc(const void* packed, const w4g128_bf16* x, w4g128_bf16* y, int K, int N,
+                                   void* stream);
 
 /* Reads the status word the last call on `ws` left (W4G128_OK, or
  * W4G128_ERR_TIMEOUT if a bounded device wait gave up).  Synchronises

@@ -15,7 +15,7 @@ __all__ = [
     "w4g128_status_string", "w4g128_packed_bytes", "w4g128_pack", "w4g128_unpack",
     "w4g128_workspace_bytes", "w4g128_gemv", "w4g128_gemm_verify",
     "w4g128_decode_step_workspace_bytes", "w4g128_decode_step", "w4g128_workspace_status",
-    "w4g128_probe_read", "w4g128_probe_copy", "w4g128_probe_sink_bytes",
+    "w4g128_probe_read", "w4g128_probe_copy", "w4g128_probe_sink_bytes", "w4g128_gemv_noalloc",
     "MAX_M", "MAX_MATRICES",
 ]
 
@@ -89,6 +89,8 @@ def lib():
     L.w4g128_probe_copy.argtypes = [p, p, sz, p]
     L.w4g128_probe_sink_bytes.restype = sz
     L.w4g128_probe_sink_bytes.argtypes = []
+    L.w4g128_gemv_noalloc.restype = i
+    L.w4g128_gemv_noalloc.argtypes = [p, p, p, i, i, p]
     _lib = L
     return L
 
@@ -188,3 +190,10 @@ def w4g128_probe_read(buf, nbytes, sink, stream=None):
 
 def w4g128_probe_copy(src, dst, nbytes, stream=None):
     _check("w4g128_probe_copy", lib().w4g128_probe_copy(_ptr(src), _ptr(dst), nbytes, _stream(stream)))
+
+
+def w4g128_gemv_noalloc(packed, x, y, K, N, stream=None):
+    """w4g128_gemv without a workspace argument: for callers that must not
+    allocate device memory (see include/w4g128.h)."""
+    _check("w4g128_gemv_noalloc", lib().w4g128_gemv_noalloc(_ptr(packed), _ptr(x), _ptr(y), K, N,
+                                                            _stream(stream)))

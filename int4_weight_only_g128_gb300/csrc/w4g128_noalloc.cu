@@ -1,0 +1,76 @@
+// w4g128_gemv_noalloc: the M = 1 GEMV for callers that cannot hand the
+// library a device workspace.
+//
+// Who needs it: code that is only given a stream and must not allocate device
+// memory itself -- plugin hooks of another runtime that owns the device
+// memory budget, fixed-pool serving processes, and latency-critical threads
+// that must not call cudaMalloc/cudaFree (they can synchronise the device and
+// stall every other stream).  Such callers pass only weights, input and
+// output; the split-K partials, tickets, activation packages and status word
+// live in one fixed scratch array that the library reserves on every GPU that
+// loads it, for the life of the process.
+//
+// The scratch array is a plain __device__ variable.  In host code its name is
+// a host-side stand-in, not a device address, so the address is fetched once
+// per device with cudaGetSymbolAddress (with that device current) and passed
+// to the kernels like any caller-owned workspace.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "w4g128.h"
+#include "w4g128_internal.h"
+
+// Every call on a device shares this array; it keeps the previous call's
+// contents.  What must start at zero (the arrival tickets and the status word)
+// is cleared by each call's first kernel, so nothing else needs resetting.
+static __device__ __align__(256) unsigned char g_w4g128_scratch[W4G128_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (the first call on each device does this set-up).
+int scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return W4G128_ERR_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_w4g128_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return W4G128_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return W4G128_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" int w4g128_gemv_noalloc(const void* packed, const w4g128_bf16* x, w4g128_bf16* y, int K, int N,
+                                   void* stream) {
+  if (packed == nullptr || x == nullptr || y == nullptr) return W4G128_ERR_INVALID_ARG;
+  if (!(K >= 128 && K <= 65536 && K % 128 == 0 && N >= 16 && N <= (1 << 24) && N % 16 == 0))
+    return W4G128_ERR_SHAPE;
+  if (!aligned(packed, 16) || !aligned(x, 4) || !aligned(y, 4)) return W4G128_ERR_ALIGN;
+  if (!w4g128::device_is_sm103()) return W4G128_ERR_DEVICE;
+  const w4g128::HostMatrix m{packed, x, y, K, N};
+  const size_t need = w4g128::stream_workspace_bytes(&m, 1, 1);
+  if (need == 0) return W4G128_ERR_SHAPE;
+  if (need > W4G128_NOALLOC_SCRATCH_BYTES) return W4G128_ERR_WORKSPACE;  // shape too large for the scratch
+  void* scratch = nullptr;
+  const int rc = scratch_address(&scratch);
+  if (rc != W4G128_OK) return rc;
+  return w4g128::launch_stream(&m, 1, 1, scratch, W4G128_NOALLOC_SCRATCH_BYTES, static_cast<cudaStream_t>(stream));
+}
