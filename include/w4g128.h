@@ -49,9 +49,10 @@
  * WORKSPACE
  *   Every compute call takes a caller-owned device workspace `ws` (16-byte
  *   aligned, size from the matching *_workspace_bytes query).  It holds the
- *   per-call activation package, split-K partial sums, arrival tickets and a
- *   status word.  Each call re-initialises what it needs: no zeroing is
- *   required, and the content after a call is unspecified except for the
+ *   per-call activation package, the split-K partial sums, the arrival
+ *   counters of the M = 1 fold and a status word.  Each call re-initialises
+ *   what it needs: no zeroing is required, and the content after a call is
+ *   unspecified except for the
  *   status word (w4g128_workspace_status).  A workspace must not be used by
  *   two calls that can run at the same time (e.g. on two streams).
  *

@@ -6,7 +6,7 @@
 // memory budget, fixed-pool serving processes, and latency-critical threads
 // that must not call cudaMalloc/cudaFree (they can synchronise the device and
 // stall every other stream).  Such callers pass only weights, input and
-// output; the split-K partials, tickets, activation packages and status word
+// output; the split-K partials, activation packages and status word
 // live in one fixed scratch array that the library reserves on every GPU that
 // loads it, for the life of the process.
 //
@@ -23,8 +23,9 @@
 #include "w4g128_internal.h"
 
 // Every call on a device shares this array; it keeps the previous call's
-// contents.  What must start at zero (the arrival tickets and the status word)
-// is cleared by each call's first kernel, so nothing else needs resetting.
+// contents.  The parts that must start at zero, the status word and the
+// split-K arrival counters, are cleared by each call's first kernel;
+// everything else is written before it is read within the call.
 static __device__ __align__(256) unsigned char g_w4g128_scratch[W4G128_NOALLOC_SCRATCH_BYTES];
 
 namespace {

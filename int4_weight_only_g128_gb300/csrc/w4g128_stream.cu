@@ -14,13 +14,18 @@
 //    (cp.async.bulk) and completed on per-slot mbarriers.  Within a matrix a
 //    warp's range is one sequential byte stream.  No block-wide barrier exists
 //    after launch, so warps never wait on each other.
-//  * A quad owned wholly by one warp is written straight to y.  A quad split
-//    between warps is reduced by whichever warp arrives last (an atomic
-//    ticket; nobody waits): it folds the segment partials in segment order.
+//  * A quad owned wholly by one warp is written straight to y.  For a quad
+//    split between warps every segment sum goes to its own fp32 partial
+//    slot, and the partials are folded in segment order:
+//      - M = 1: by whichever warp of the quad arrives last (an atomic ticket;
+//        nobody waits) -- 64 outputs, cheap enough to overlap the stream;
+//      - M >= 2: by a small reduce kernel launched right behind the streaming
+//        kernel (programmatic dependent launch), one thread per output with
+//        its loads in flight, since 64*M outputs would stall one warp.
 //  * A small prep kernel (launched first; the streaming kernel overlaps it by
 //    programmatic dependent launch) turns x into per-group packages in the
 //    order the lanes consume them, with the group sums the factorised
-//    dequantisation needs, and zeroes the tickets and the status word.
+//    dequantisation needs, and clears the status word and the tickets.
 //
 // Dequantisation uses the factorised form of w = min + q*scale over a group g:
 //     sum_{k in g} x_k w_kn = scale_gn * sum_k x_k q_kn + min_gn * X_g,
@@ -88,7 +93,7 @@ struct MatParams {
   uint16_t* y;
   long long item_begin;  // first item of this matrix in the flat list
   int K, N;
-  int quad_begin;        // first ticket of this matrix
+  int quad_begin;        // first quad (and ticket) of this matrix in the flat quad list
   int g_begin;           // first (matrix, group) package index of this matrix
 };
 
@@ -96,7 +101,7 @@ template <int MAXMAT>
 struct StreamParams {
   long long total_items;
   float* partials;       // [total_items][rows][64]: one slot per (matrix, quad, segment)
-  unsigned* tickets;     // [total_quads]
+  unsigned* tickets;     // [total_quads] arrival counters (M = 1)
   unsigned* status;
   int count, M, W, total_quads, total_groups;
   MatParams mats[MAXMAT];
@@ -238,6 +243,21 @@ __device__ __forceinline__ void mma_word(uint32_t w, uint32_t xa, uint32_t xb, f
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(xa), "r"(xb));
 }
 
+// Two IEEE fp32 FMAs in one instruction (Blackwell packed f32x2); each lane of
+// the pair rounds exactly like fmaf.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 A, B, C;\n\t"
+      "mov.b64 A, {%2, %3};\n\t"
+      "mov.b64 B, {%4, %5};\n\t"
+      "mov.b64 C, {%6, %7};\n\t"
+      "fma.rn.f32x2 C, A, B, C;\n\t"
+      "mov.b64 {%0, %1}, C;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 __device__ __forceinline__ uint16_t to_bf16(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
@@ -280,11 +300,13 @@ __device__ __forceinline__ void compute_chunk(const uint8_t* sl, int ntiles, int
         dq_word(u1.y, xw[10], xw[11], lo, hi);
         dq_word(u1.z, xw[12], xw[13], lo, hi);
         dq_word(u1.w, xw[14], xw[15], lo, hi);
-        const float sl0 = bf16_lo(me.x), sh0 = bf16_lo(me.y);
-        const float ml0 = fmaf(-128.f, sl0, bf16_hi(me.x));   // min - 128 scale, exact
-        const float mh0 = fmaf(-128.f, sh0, bf16_hi(me.y));
-        seg[t][0] = fmaf(sl0, lo, fmaf(ml0, Xc, seg[t][0]));
-        seg[t][1] = fmaf(sh0, hi, fmaf(mh0, Xc, seg[t][1]));
+        // columns r and r+8 side by side: seg += scale * S + (min - 128 scale) * X_c
+        const float2 s2 = make_float2(bf16_lo(me.x), bf16_lo(me.y));
+        const float2 m2 = ffma2(make_float2(-128.f, -128.f), s2, make_float2(bf16_hi(me.x), bf16_hi(me.y)));
+        float2 a2 = ffma2(m2, make_float2(Xc, Xc), make_float2(seg[t][0], seg[t][1]));
+        a2 = ffma2(s2, make_float2(lo, hi), a2);
+        seg[t][0] = a2.x;
+        seg[t][1] = a2.y;
       }
     }
   } else {
@@ -380,6 +402,9 @@ __global__ void __launch_bounds__(kNW * 32, 2) stream_kernel(const __grid_consta
       if (d < n_pre) issue_package<MODE>(pre[d], ring0 + d * kSlot, bar0 + 8 * d, pol_x);
   }
   unsigned issued = static_cast<unsigned>(n_pre);
+  // The reduce kernel may start launching now; it waits for this grid to
+  // finish before it reads any partial.
+  grid_dependents_launch();
 
   float seg[kQuadTiles][NA];
   float tot[kQuadTiles][NA];
@@ -504,9 +529,9 @@ __global__ void __launch_bounds__(kNW * 32, 2) stream_kernel(const __grid_consta
               }
             }
           }
-        } else {
-          // Split quad: publish, take a ticket; the last arriver folds the
-          // segment partials in segment order and writes y.
+        } else if constexpr (MODE == kM1) {
+          // Split quad at M = 1: publish, take a ticket; the last arriver folds
+          // the segment partials in segment order and writes y.
           __threadfence();
           __syncwarp();
           const int wf = owner_of(q_first, I, p.W), wl = owner_of(q_last, I, p.W);
@@ -517,29 +542,28 @@ __global__ void __launch_bounds__(kNW * 32, 2) stream_kernel(const __grid_consta
           prev = __shfl_sync(0xffffffffu, prev, 0);
           if (prev + 1 == expected) {
             __threadfence();
-            const float* part = p.partials + q_first * rows * 64;
+            const float* part = p.partials + q_first * 64;
             const int ncols = ntiles * kTileN;
-            for (int rr = 0; rr < rows; ++rr) {
+            const bool c0 = lane < ncols, c1 = lane + 32 < ncols;
+            float a0 = 0.f, a1 = 0.f;
+            for (int s0 = 0; s0 < S; s0 += 8) {  // both columns' loads of 8 segments in flight
+              float v0[8], v1[8];
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const int col = lane + 32 * h;
-                if (col < ncols) {
-                  // issue the loads of 8 segments at a time, then fold them in segment order
-                  float acc = 0.f;
-                  for (int s0 = 0; s0 < S; s0 += 8) {
-                    float v[8];
+              for (int u = 0; u < 8; ++u) {
+                const bool ok = s0 + u < S;
+                v0[u] = (ok && c0) ? __ldcg(part + static_cast<long long>(s0 + u) * 64 + lane) : 0.f;
+                v1[u] = (ok && c1) ? __ldcg(part + static_cast<long long>(s0 + u) * 64 + lane + 32) : 0.f;
+              }
 #pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                      v[u] = (s0 + u < S) ? __ldcg(part + (static_cast<long long>(s0 + u) * rows + rr) * 64 + col)
-                                          : 0.f;
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                      if (s0 + u < S) acc = (s0 + u == 0) ? v[u] : acc + v[u];
-                  }
-                  m.y[static_cast<long long>(rr) * m.N + n0 + col] = to_bf16(acc);
+              for (int u = 0; u < 8; ++u) {
+                if (s0 + u < S) {
+                  a0 = (s0 + u == 0) ? v0[u] : a0 + v0[u];
+                  a1 = (s0 + u == 0) ? v1[u] : a1 + v1[u];
                 }
               }
             }
+            if (c0) m.y[n0 + lane] = to_bf16(a0);
+            if (c1) m.y[n0 + lane + 32] = to_bf16(a1);
             if (lane == 0) *ticket = 0u;  // ready for the next call
           }
         }
@@ -557,7 +581,8 @@ template <int MODE, int MAXMAT>
 __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
   grid_dependents_launch();
   const int tid = blockIdx.x * blockDim.x + threadIdx.x, nthreads = gridDim.x * blockDim.x;
-  for (int i = tid; i < p.total_quads; i += nthreads) p.tickets[i] = 0u;
+  if (MODE == kM1)
+    for (int i = tid; i < p.total_quads; i += nthreads) p.tickets[i] = 0u;
   if (tid == 0) *p.status = 0u;
 
   constexpr int kRows = Pkg<MODE>::kRows;
@@ -606,6 +631,51 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Strea
       float* xg = reinterpret_cast<float*>(out + kRows * Pkg<MODE>::kRowBytes);
       xg[row] = (row < kRows) ? ((X0 + X1) + X2) + X3 : 0.f;
     }
+  }
+}
+
+// ----------------------------------------------------------------- reduce kernel
+
+// M >= 2: folds the segment partials of every quad the schedule split between warps:
+// one thread per output (row, column), its S partial loads issued 16 at a
+// time, summed in segment order exactly as a single warp would have.  Quads
+// owned by one warp were written by the streaming kernel and are skipped.
+template <int MAXMAT>
+__global__ void __launch_bounds__(256) reduce_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
+  grid_dependency_wait();  // every partial of the streaming kernel is written and visible
+  const int rows = p.M;
+  const int per_quad = rows * 64;
+  const long long I = p.total_items;
+  const long long total = static_cast<long long>(p.total_quads) * per_quad;
+  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int gq = static_cast<int>(idx / per_quad);
+    const int o = static_cast<int>(idx - static_cast<long long>(gq) * per_quad);
+    int lo = 0, hi = p.count - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.mats[mid].quad_begin <= gq) lo = mid; else hi = mid - 1;
+    }
+    const MatParams& m = p.mats[lo];
+    const int q = gq - m.quad_begin;
+    const int G = m.K / kGroup, S = div_up(G, kSegGroups), T = m.N / kTileN;
+    const int ncols = kTileN * min(kQuadTiles, T - kQuadTiles * q);
+    const int row = o / 64, col = o % 64;
+    if (col >= ncols) continue;
+    const long long q_first = m.item_begin + static_cast<long long>(q) * S;
+    if (owner_of(q_first, I, p.W) == owner_of(q_first + S - 1, I, p.W)) continue;  // owned quad
+    const float* part = p.partials + q_first * per_quad + o;
+    float acc = 0.f;
+    for (int s0 = 0; s0 < S; s0 += 16) {  // up to 16 loads in flight, then fold in order
+      float v[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        v[u] = (s0 + u < S) ? __ldcg(part + static_cast<long long>(s0 + u) * per_quad) : 0.f;
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        if (s0 + u < S) acc = (s0 + u == 0) ? v[u] : acc + v[u];
+    }
+    m.y[static_cast<long long>(row) * m.N + kQuadTiles * kTileN * q + col] = to_bf16(acc);
   }
 }
 
@@ -697,7 +767,7 @@ bool make_plan(const HostMatrix* mats, int count, int M, const DeviceInfo& dev, 
   const long long max_warps = static_cast<long long>(dev.sms) * dev.occ[pl.mode] * kNW;
   pl.W = static_cast<int>(std::min<long long>(items, max_warps));
   pl.grid = div_up(pl.W, kNW);
-  pl.off_tickets = 256;
+  pl.off_tickets = 256;  // after the status word
   pl.off_xpkg = align_up(pl.off_tickets + sizeof(unsigned) * static_cast<size_t>(quads), 256);
   pl.off_partials = align_up(pl.off_xpkg + static_cast<size_t>(xbytes), 256);
   pl.bytes = align_up(pl.off_partials + sizeof(float) * static_cast<size_t>(items) * pl.rows * 64, 256);
@@ -747,6 +817,16 @@ int launch_mode(const StreamParams<MAXMAT>& sp, int grid, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, stream_kernel<MODE, MAXMAT>, sp) != cudaSuccess) {
+    cudaGetLastError();
+    return W4G128_ERR_CUDA;
+  }
+
+  if (MODE == kM1) return W4G128_OK;  // M = 1 folds split quads inside the streaming kernel
+  const long long outputs = static_cast<long long>(sp.total_quads) * sp.M * 64;
+  cfg.gridDim = dim3(static_cast<unsigned>(std::max(1LL, std::min((outputs + 255) / 256, 4096LL))));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  if (cudaLaunchKernelEx(&cfg, reduce_kernel<MAXMAT>, sp) != cudaSuccess) {
     cudaGetLastError();
     return W4G128_ERR_CUDA;
   }
