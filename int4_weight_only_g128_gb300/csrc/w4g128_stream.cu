@@ -31,11 +31,21 @@
 //     sum_{k in g} x_k w_kn = scale_gn * sum_k x_k q_kn + min_gn * X_g,
 //     X_g = sum_{k in g} x_k
 // (Token Rush README, "Quantization": 128 weights per bf16 scale and minimum).
-// Codes are turned into the bf16 values 128 + q with one LOP3 per pair (a
-// magic-number conversion), so sum_k x_k (128 + q_k) is accumulated with exact
-// products and the 128 X_g offset is folded into the minimum term:
-//     scale * S_g + (min - 128 scale) * X_g,   S_g = sum_k x_k (128 + q_k).
+// Codes become fp16 values with one LOP3 per pair (a magic-number
+// conversion): with the fp16 pattern of 1024 OR-ed in, a nibble at bits 0..3
+// of a 16-bit half reads as 1024 + q and a nibble at bits 4..7 as 1024 + 16q,
+// so a packed word needs one shift and four LOP3s (bf16, whose mantissa has
+// only 7 bits, would need three shifts).  Of each lane's four pairs, the two
+// of column r come out as 1024 + q and the two of column r + 8 as 1024 + 16q.
+// The activations enter as fp16 too: the prep kernel scales each (group, row)
+// of x by a power of two 2^s that puts its largest magnitude in [2^14, 2^15)
+// (exact for every value within 2^29 of that largest one), so every product
+// x' (1024 + q) is exact in fp32.  With f = 2^-s and X_g the true sum of x,
+//     column r:     scale * f * S_g + (min - 1024 scale) * X_g,
+//     column r + 8: (scale / 16) * f * S_g + (min - 64 scale) * X_g,
+// where S_g is the fp32 sum of x' times the converted code.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -57,7 +67,7 @@ enum Mode : int {
 };
 
 #ifndef W4G128_WARPS_PER_CTA
-#define W4G128_WARPS_PER_CTA 8
+#define W4G128_WARPS_PER_CTA 16
 #endif
 #ifndef W4G128_RING_DEPTH
 #define W4G128_RING_DEPTH 2
@@ -65,15 +75,18 @@ enum Mode : int {
 constexpr int kNW = W4G128_WARPS_PER_CTA;  // warps per CTA
 constexpr int kDepth = W4G128_RING_DEPTH;  // ring slots per warp
 
-// Activation package per group: rows x 4 lane classes c x (16 bf16-pair
-// words + X_c + 3 pad) = rows x 320 bytes, then 8 fp32 group sums X_g[row].
-// Row (m, c) word 2i holds x[m][k0+2c], x[m][k0+2c+1] and word 2i+1 holds
-// x[m][k0+2c+8], x[m][k0+2c+9] for k0 = 128g + 16i: exactly the bf16 operand
-// pairs lane class c multiplies (the MMA B fragment of row m).  The 80-byte
-// stride keeps the 16-byte loads of 8 lanes on distinct bank groups.
+// Activation package per group: rows x 4 lane classes c x (16 fp16-pair
+// words + X_c + f + 2 pad) = rows x 320 bytes, then per row m the pair
+// (X_g[m], f[m]) as fp32.  Row (m, c) word 2i holds x'[m][k0+2c],
+// x'[m][k0+2c+1] and word 2i+1 holds x'[m][k0+2c+8], x'[m][k0+2c+9] for
+// k0 = 128g + 16i: exactly the fp16 operand pairs lane class c multiplies (the
+// MMA B fragment of row m).  x' = x * 2^s is the scaled copy, f = 2^-s, X_c the
+// true sum of the 32 values of lane class c and X_g = sum of x over the group.
+// The 80-byte stride keeps the 16-byte loads of 8 lanes on distinct bank
+// groups.
 template <int MODE> struct Pkg;
-template <> struct Pkg<kM1> { static constexpr int kRows = 1, kRowBytes = 320, kBytes = 352; };
-template <> struct Pkg<kMMA> { static constexpr int kRows = 8, kRowBytes = 320, kBytes = 2592; };
+template <> struct Pkg<kM1> { static constexpr int kRows = 1, kRowBytes = 320, kBytes = 336; };
+template <> struct Pkg<kMMA> { static constexpr int kRows = 8, kRowBytes = 320, kBytes = 2624; };
 
 template <int MODE>
 __host__ __device__ constexpr int slot_bytes() { return kQuadTiles * kBlockBytes + Pkg<MODE>::kBytes; }
@@ -82,6 +95,7 @@ template <int MODE>
 __host__ __device__ constexpr int smem_bytes() { return kBarBytes + kNW * kDepth * slot_bytes<MODE>(); }
 
 static_assert(slot_bytes<kM1>() % 16 == 0 && slot_bytes<kMMA>() % 16 == 0, "bulk copies need 16-byte slots");
+static_assert(Pkg<kM1>::kBytes % 16 == 0 && Pkg<kMMA>::kBytes % 16 == 0, "bulk copies need 16-byte packages");
 static_assert((kDepth & (kDepth - 1)) == 0, "ring depth must be a power of two");
 
 // ----------------------------------------------------------------- parameters
@@ -204,40 +218,46 @@ __device__ __forceinline__ void issue_package(const Cursor& c, uint32_t slot, ui
 // ----------------------------------------------------------------- in-register dequantisation
 
 // Word layout (per lane r = l/4, c = l%4): nibble p = 4b + 2a + e holds row
-// 2c + 8a + b of column r + 8e.  LOP3 with the bf16 magic 0x4300 turns the
-// nibbles at bits 0..3 and 16..19 of (w >> 4s) into the bf16 pair
-// (128 + q_lo, 128 + q_hi); each half is multiplied by the matching bf16 x and
+// 2c + 8a + b of column r + 8e.  With v = w >> 8, LOP3 with the fp16 magic
+// 0x6400 (1024) turns
+//   w & 0x000F000F -> nibbles 0, 4 (rows 2c, 2c+1, column r)      as 1024 + q
+//   w & 0x00F000F0 -> nibbles 1, 5 (rows 2c, 2c+1, column r+8)    as 1024 + 16q
+//   v & 0x000F000F -> nibbles 2, 6 (rows 2c+8, 2c+9, column r)    as 1024 + q
+//   v & 0x00F000F0 -> nibbles 3, 7 (rows 2c+8, 2c+9, column r+8)  as 1024 + 16q
+// into fp16 pairs; each half is multiplied by the matching fp16 x' and
 // accumulated in fp32 (the products are exact).
-__device__ __forceinline__ float fma_bf16_pair(uint32_t wq, uint32_t xx, float acc) {
+__device__ __forceinline__ float fma_f16_pair(uint32_t wq, uint32_t xx, float acc) {
   asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
       "mov.b32 {wl, wh}, %1;\n\t"
       "mov.b32 {xl, xh}, %2;\n\t"
-      "fma.rn.f32.bf16 %0, wl, xl, %0;\n\t"
-      "fma.rn.f32.bf16 %0, wh, xh, %0;\n\t}"
+      "fma.rn.f32.f16 %0, wl, xl, %0;\n\t"
+      "fma.rn.f32.f16 %0, wh, xh, %0;\n\t}"
       : "+f"(acc)
       : "r"(wq), "r"(xx));
   return acc;
 }
 
+constexpr uint32_t kMagic = 0x64006400u;  // fp16 1024.0 in both halves
+
+// lo: column r (1024 + q), hi: column r + 8 (1024 + 16q)
 __device__ __forceinline__ void dq_word(uint32_t w, uint32_t xa, uint32_t xb, float& lo, float& hi) {
-  const uint32_t r0 = lop3_and_or(w, 0x000F000Fu, 0x43004300u);        // rows 2c, 2c+1   col r
-  const uint32_t r1 = lop3_and_or(w >> 4, 0x000F000Fu, 0x43004300u);   // rows 2c, 2c+1   col r+8
-  const uint32_t r2 = lop3_and_or(w >> 8, 0x000F000Fu, 0x43004300u);   // rows 2c+8, 2c+9 col r
-  const uint32_t r3 = lop3_and_or(w >> 12, 0x000F000Fu, 0x43004300u);  // rows 2c+8, 2c+9 col r+8
-  lo = fma_bf16_pair(r0, xa, lo);
-  hi = fma_bf16_pair(r1, xa, hi);
-  lo = fma_bf16_pair(r2, xb, lo);
-  hi = fma_bf16_pair(r3, xb, hi);
+  const uint32_t v = w >> 8;
+  lo = fma_f16_pair(lop3_and_or(w, 0x000F000Fu, kMagic), xa, lo);
+  hi = fma_f16_pair(lop3_and_or(w, 0x00F000F0u, kMagic), xa, hi);
+  lo = fma_f16_pair(lop3_and_or(v, 0x000F000Fu, kMagic), xb, lo);
+  hi = fma_f16_pair(lop3_and_or(v, 0x00F000F0u, kMagic), xb, hi);
 }
 
 // Warp MMA: D[16 cols x 8 rows] += A[16 cols x 16 k] * B[16 k x 8 rows]; the
-// four LOP3 outputs of one packed word are exactly this lane's A fragment.
+// four LOP3 outputs of one packed word are exactly this lane's A fragment
+// (columns r + 8 carry 1024 + 16q, so their D rows are scaled accordingly).
 __device__ __forceinline__ void mma_word(uint32_t w, uint32_t xa, uint32_t xb, float (&d)[4]) {
-  const uint32_t a0 = lop3_and_or(w, 0x000F000Fu, 0x43004300u);
-  const uint32_t a1 = lop3_and_or(w >> 4, 0x000F000Fu, 0x43004300u);
-  const uint32_t a2 = lop3_and_or(w >> 8, 0x000F000Fu, 0x43004300u);
-  const uint32_t a3 = lop3_and_or(w >> 12, 0x000F000Fu, 0x43004300u);
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+  const uint32_t v = w >> 8;
+  const uint32_t a0 = lop3_and_or(w, 0x000F000Fu, kMagic);
+  const uint32_t a1 = lop3_and_or(w, 0x00F000F0u, kMagic);
+  const uint32_t a2 = lop3_and_or(v, 0x000F000Fu, kMagic);
+  const uint32_t a3 = lop3_and_or(v, 0x00F000F0u, kMagic);
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(xa), "r"(xb));
@@ -255,6 +275,18 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
       "mov.b64 {%0, %1}, C;\n\t}"
       : "=f"(d.x), "=f"(d.y)
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 A, B;\n\t"
+      "mov.b64 A, {%2, %3};\n\t"
+      "mov.b64 B, {%4, %5};\n\t"
+      "mul.rn.f32x2 A, A, B;\n\t"
+      "mov.b64 {%0, %1}, A;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return d;
 }
 
@@ -283,7 +315,9 @@ __device__ __forceinline__ void compute_chunk(const uint8_t* sl, int ntiles, int
     xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
   }
   if constexpr (MODE == kM1) {
-    const float Xc = __uint_as_float(xr[16]);
+    const float2 xf = *reinterpret_cast<const float2*>(xr + 16);  // (X_c, f)
+    const float Xc = xf.x;
+    const float2 ff = make_float2(xf.y, xf.y * 0.0625f);          // x' -> x for columns r and r + 8
 #pragma unroll
     for (int t = 0; t < kQuadTiles; ++t) {
       if (FULL || t < ntiles) {
@@ -291,7 +325,7 @@ __device__ __forceinline__ void compute_chunk(const uint8_t* sl, int ntiles, int
         const uint4 u0 = *reinterpret_cast<const uint4*>(blk + 16 * lane);
         const uint4 u1 = *reinterpret_cast<const uint4*>(blk + 512 + 16 * lane);
         const uint2 me = *reinterpret_cast<const uint2*>(blk + kCodeBytes + 8 * r);
-        float lo = 0.f, hi = 0.f;  // sum_k x_k (128 + q_k) over this lane's rows, columns r and r+8
+        float lo = 0.f, hi = 0.f;  // sum_k x'_k (1024 + q_k), sum_k x'_k (1024 + 16 q_k): columns r, r+8
         dq_word(u0.x, xw[0], xw[1], lo, hi);
         dq_word(u0.y, xw[2], xw[3], lo, hi);
         dq_word(u0.z, xw[4], xw[5], lo, hi);
@@ -300,17 +334,22 @@ __device__ __forceinline__ void compute_chunk(const uint8_t* sl, int ntiles, int
         dq_word(u1.y, xw[10], xw[11], lo, hi);
         dq_word(u1.z, xw[12], xw[13], lo, hi);
         dq_word(u1.w, xw[14], xw[15], lo, hi);
-        // columns r and r+8 side by side: seg += scale * S + (min - 128 scale) * X_c
+        // columns r and r+8 side by side:
+        //   seg += scale f S + (min - 1024 scale) X_c,  seg += (scale/16) f S + (min - 64 scale) X_c
         const float2 s2 = make_float2(bf16_lo(me.x), bf16_lo(me.y));
-        const float2 m2 = ffma2(make_float2(-128.f, -128.f), s2, make_float2(bf16_hi(me.x), bf16_hi(me.y)));
+        const float2 m2 = ffma2(make_float2(-1024.f, -64.f), s2, make_float2(bf16_hi(me.x), bf16_hi(me.y)));
         float2 a2 = ffma2(m2, make_float2(Xc, Xc), make_float2(seg[t][0], seg[t][1]));
-        a2 = ffma2(s2, make_float2(lo, hi), a2);
+        a2 = ffma2(fmul2(s2, ff), make_float2(lo, hi), a2);
         seg[t][0] = a2.x;
         seg[t][1] = a2.y;
       }
     }
   } else {
-    const float2 Xg = *reinterpret_cast<const float2*>(pk + Pkg<MODE>::kRows * Pkg<MODE>::kRowBytes + 8 * c);
+    // (X_g, f) of rows 2c and 2c + 1
+    const float4 xq = *reinterpret_cast<const float4*>(pk + Pkg<MODE>::kRows * Pkg<MODE>::kRowBytes + 16 * c);
+    const float2 Xab = make_float2(xq.x, xq.z);
+    const float2 fab = make_float2(xq.y, xq.w);
+    const float2 fab16 = make_float2(xq.y * 0.0625f, xq.w * 0.0625f);
 #pragma unroll
     for (int t = 0; t < kQuadTiles; ++t) {
       if (FULL || t < ntiles) {
@@ -318,7 +357,8 @@ __device__ __forceinline__ void compute_chunk(const uint8_t* sl, int ntiles, int
         const uint4 u0 = *reinterpret_cast<const uint4*>(blk + 16 * lane);
         const uint4 u1 = *reinterpret_cast<const uint4*>(blk + 512 + 16 * lane);
         const uint2 me = *reinterpret_cast<const uint2*>(blk + kCodeBytes + 8 * r);
-        // sum_k (128 + q) x over the group as (column, row) fragments, two chains
+        // sum_k (1024 + q) x' (columns r) and (1024 + 16q) x' (columns r + 8) as
+        // (column, row) fragments, two chains
         float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
         mma_word(u0.x, xw[0], xw[1], d0);
         mma_word(u0.y, xw[2], xw[3], d1);
@@ -329,12 +369,16 @@ __device__ __forceinline__ void compute_chunk(const uint8_t* sl, int ntiles, int
         mma_word(u1.z, xw[12], xw[13], d0);
         mma_word(u1.w, xw[14], xw[15], d1);
         const float sl0 = bf16_lo(me.x), sh0 = bf16_lo(me.y);
-        const float ml0 = fmaf(-128.f, sl0, bf16_hi(me.x));
-        const float mh0 = fmaf(-128.f, sh0, bf16_hi(me.y));
-        seg[t][0] = fmaf(sl0, d0[0] + d1[0], fmaf(ml0, Xg.x, seg[t][0]));
-        seg[t][1] = fmaf(sl0, d0[1] + d1[1], fmaf(ml0, Xg.y, seg[t][1]));
-        seg[t][2] = fmaf(sh0, d0[2] + d1[2], fmaf(mh0, Xg.x, seg[t][2]));
-        seg[t][3] = fmaf(sh0, d0[3] + d1[3], fmaf(mh0, Xg.y, seg[t][3]));
+        const float ml0 = fmaf(-1024.f, sl0, bf16_hi(me.x));
+        const float mh0 = fmaf(-64.f, sh0, bf16_hi(me.y));
+        float2 lo2 = ffma2(make_float2(ml0, ml0), Xab, make_float2(seg[t][0], seg[t][1]));
+        lo2 = ffma2(fmul2(make_float2(sl0, sl0), fab), make_float2(d0[0] + d1[0], d0[1] + d1[1]), lo2);
+        float2 hi2 = ffma2(make_float2(mh0, mh0), Xab, make_float2(seg[t][2], seg[t][3]));
+        hi2 = ffma2(fmul2(make_float2(sh0, sh0), fab16), make_float2(d0[2] + d1[2], d0[3] + d1[3]), hi2);
+        seg[t][0] = lo2.x;
+        seg[t][1] = lo2.y;
+        seg[t][2] = hi2.x;
+        seg[t][3] = hi2.y;
       }
     }
   }
@@ -352,7 +396,7 @@ __device__ __forceinline__ float pick(const float (&v)[kQuadTiles][NA], int t, i
 // ----------------------------------------------------------------- the streaming kernel
 
 template <int MODE, int MAXMAT>
-__global__ void __launch_bounds__(kNW * 32, 2) stream_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
+__global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int NA = Acc<MODE>::kN;
   constexpr int kSlot = slot_bytes<MODE>();
@@ -576,7 +620,10 @@ __global__ void __launch_bounds__(kNW * 32, 2) stream_kernel(const __grid_consta
 // ----------------------------------------------------------------- prep kernel
 
 // One warp per (matrix, group): lane (row, c) builds row `row` / lane class c
-// of the group's activation package; lanes c == 0 add the group sum X_g.
+// of the group's activation package.  The four lanes of a row agree on the
+// row's scale 2^s (from the largest magnitude among their 128 values), store
+// x' = x 2^s as fp16 pairs with their class sum X_c and f = 2^-s, and lane
+// c == 0 adds the row's (X_g, f) to the package tail.
 template <int MODE, int MAXMAT>
 __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
   grid_dependents_launch();
@@ -598,38 +645,59 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Strea
     const MatParams& m = p.mats[lo];
     const int g = wg - m.g_begin;
     uint8_t* out = m.xpkg + static_cast<long long>(g) * Pkg<MODE>::kBytes;
-    float X = 0.f;
-    if (row < kRows) {
-      uint32_t w[20];
-      if (row < p.M) {
-        const uint16_t* xr = m.x + static_cast<long long>(row) * m.K;
+    uint32_t w[16];  // bf16 pairs in operand order
+    float X = 0.f;   // sum of this lane's 32 values
+    uint32_t amax = 0u;  // largest |x| among them, as bf16 magnitude bits
+    if (row < kRows && row < p.M) {
+      // x rows start 4-byte aligned (K even, x 4-byte aligned): one 32-bit
+      // load per operand pair
+      const uint32_t* xr = reinterpret_cast<const uint32_t*>(m.x + static_cast<long long>(row) * m.K + kGroup * g);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int k0 = kGroup * g + 16 * i;
-          const uint16_t x0 = xr[k0 + 2 * c], x1 = xr[k0 + 2 * c + 1];
-          const uint16_t x8 = xr[k0 + 2 * c + 8], x9 = xr[k0 + 2 * c + 9];
-          w[2 * i] = static_cast<uint32_t>(x0) | (static_cast<uint32_t>(x1) << 16);
-          w[2 * i + 1] = static_cast<uint32_t>(x8) | (static_cast<uint32_t>(x9) << 16);
-          X = (((X + bf16_lo(x0)) + bf16_lo(x1)) + bf16_lo(x8)) + bf16_lo(x9);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) w[i] = 0u;
+      for (int i = 0; i < 8; ++i) {
+        w[2 * i] = xr[8 * i + c];
+        w[2 * i + 1] = xr[8 * i + c + 4];
       }
-      w[16] = __float_as_uint(X);
-      w[17] = w[18] = w[19] = 0u;
+      uint32_t mag2 = 0u;  // per-half maxima of |x| bits
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        X = (((X + bf16_lo(w[2 * i])) + bf16_hi(w[2 * i])) + bf16_lo(w[2 * i + 1])) + bf16_hi(w[2 * i + 1]);
+        mag2 = __vmaxu2(mag2, __vmaxu2(w[2 * i] & 0x7FFF7FFFu, w[2 * i + 1] & 0x7FFF7FFFu));
+      }
+      amax = max(mag2 & 0xFFFFu, mag2 >> 16);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) w[i] = 0u;
+    }
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    // biased exponent e of the row's largest |x|: x 2^(141 - e) lies in
+    // [2^14, 2^15); the cap keeps 2^s a normal fp32 for zero or tiny rows.
+    const int sft = min(141 - static_cast<int>(amax >> 7), 126);
+    const float up = __int_as_float((127 + sft) << 23);
+    const float f = __int_as_float((127 - sft) << 23);
+    if (row < kRows) {
+      uint32_t h[20];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float2 v = fmul2(make_float2(bf16_lo(w[i]), bf16_hi(w[i])), make_float2(up, up));
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h[i]) : "f"(v.y), "f"(v.x));  // (hi, lo)
+      }
+      h[16] = __float_as_uint(X);
+      h[17] = __float_as_uint(f);
+      h[18] = h[19] = 0u;
       uint4* o = reinterpret_cast<uint4*>(out + row * Pkg<MODE>::kRowBytes + c * 80);
 #pragma unroll
-      for (int i = 0; i < 5; ++i) o[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      for (int i = 0; i < 5; ++i) o[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
     }
     // group sum of row `row`: ((X_0 + X_1) + X_2) + X_3 over its four lane classes
     const float X0 = __shfl_sync(0xffffffffu, X, lane & ~3);
     const float X1 = __shfl_sync(0xffffffffu, X, (lane & ~3) + 1);
     const float X2 = __shfl_sync(0xffffffffu, X, (lane & ~3) + 2);
     const float X3 = __shfl_sync(0xffffffffu, X, (lane & ~3) + 3);
-    if (c == 0) {
-      float* xg = reinterpret_cast<float*>(out + kRows * Pkg<MODE>::kRowBytes);
-      xg[row] = (row < kRows) ? ((X0 + X1) + X2) + X3 : 0.f;
+    if (c == 0 && row < kRows) {
+      float* tail = reinterpret_cast<float*>(out + kRows * Pkg<MODE>::kRowBytes);
+      tail[2 * row] = ((X0 + X1) + X2) + X3;
+      tail[2 * row + 1] = f;
     }
   }
 }

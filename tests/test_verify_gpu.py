@@ -72,3 +72,30 @@ def test_verify_deterministic():
     mat = DevMatrix(K, N, matrix_id=8)
     x = synth.x(SEED, 8, 8, K)
     assert np.array_equal(run(mat, x), run(mat, x))
+
+
+def _wide_range_x(rng, M, K):
+    """bf16 bits of x whose magnitudes span 2^-100 .. 2^100 within and across
+    groups and rows; group 1 of every row is all zeros, and row 1 (when
+    present) is a single large value per group."""
+    mag = np.exp2(rng.integers(-100, 101, size=(M, K)).astype(np.float64))
+    x = (rng.standard_normal((M, K)) * mag).astype(np.float32)
+    x[:, 128:256] = 0.0
+    if M > 1:
+        x[1] = 0.0
+        x[1, ::128] = 3.0e20
+    return (x.view(np.uint32) >> 16).astype(np.uint16)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M", [1, 2, 8])
+def test_wide_dynamic_range_x(M):
+    """The kernels carry x into fp16 with one power of two per (group, row);
+    values far below a group's largest, zero groups and huge values must all
+    stay within the bound (M = 1 also through w4g128_gemv)."""
+    K, N = 1024, 208
+    mat = DevMatrix(K, N, matrix_id=77)
+    x = _wide_range_x(np.random.default_rng(5 + M), M, K)
+    check_against_oracle(run(mat, x), x, mat.codes, mat.scales, mat.mins)
+    if M == 1:
+        check_against_oracle(run(mat, x, verify=True), x, mat.codes, mat.scales, mat.mins)
