@@ -12,6 +12,9 @@ min = -8 scale (1 + U(-0.1, 0.1)), x ~ N(0, 1)).
 Before timing, sampled outputs of both M = 1 and M = 8 are checked against the
 fp64 oracle; a mismatch voids the run (exit status 1, no number printed).
 
+`--target layer|lm_head` instead runs a few untimed calls of one workload
+and exits: the launch target for profiler captures (no JSON line).
+
 Prints ONE JSON line.  `--impl reference` times the fp64 CPU oracle instead
 (the reference arm: the plain dequantise-then-multiply definition on the host
 cores).  Under torchrun (N > 1) every rank streams its own copy of the layer
@@ -509,6 +512,52 @@ def run_ours(args):
     return 0
 
 
+def run_target(args):
+    """Untimed calls of one workload for a profiler to capture: the layer set
+    through w4g128_decode_step, or the 5120 x 248320 lm_head through
+    w4g128_gemv (M = 1) / w4g128_gemm_verify (M > 1); each M in --m in turn."""
+    import numpy as np
+    import torch
+
+    import int4_weight_only_g128_gb300 as w
+    import synth
+
+    st = torch.cuda.current_stream().cuda_stream
+    shapes = [(K, N) for _, K, N in LAYER] if args.target == "layer" else [(5120, 248320)]
+    packed = []
+    for i, (K, N) in enumerate(shapes):
+        codes = torch.empty((K // 8) * N, dtype=torch.int32, device="cuda")
+        s = torch.empty((K // 128) * N, dtype=torch.int16, device="cuda")
+        m = torch.empty_like(s)
+        synth.fill_device(SEED, i, K, N, codes.data_ptr(), s.data_ptr(), m.data_ptr(), st)
+        pk = torch.empty(w.w4g128_packed_bytes(K, N), dtype=torch.uint8, device="cuda")
+        w.w4g128_pack(codes, s, m, K, N, pk)
+        packed.append(pk)
+        del codes, s, m
+    for M in [int(v) for v in args.m.split(",")]:
+        xs = [torch.from_numpy(synth.x(SEED, 100 + i, M, K).view(np.int16)).cuda() for i, (K, _) in enumerate(shapes)]
+        ys = [torch.empty(M * N, dtype=torch.int16, device="cuda") for _, N in shapes]
+        descs = [(packed[i], xs[i], ys[i], K, N) for i, (K, N) in enumerate(shapes)]
+        if args.target == "layer":
+            ws = torch.empty(w.w4g128_decode_step_workspace_bytes(descs, M), dtype=torch.uint8, device="cuda")
+            for _ in range(args.calls):
+                w.w4g128_decode_step(descs, M, ws, stream=st)
+        else:
+            (pk, x, y, K, N), = descs
+            ws = torch.empty(w.w4g128_workspace_bytes(M, K, N), dtype=torch.uint8, device="cuda")
+            for _ in range(args.calls):
+                if M == 1:
+                    w.w4g128_gemv(pk, x, y, K, N, ws, stream=st)
+                else:
+                    w.w4g128_gemm_verify(pk, x, y, M, K, N, ws, stream=st)
+        torch.cuda.synchronize()
+        if w.w4g128_workspace_status(ws, st) != 0:
+            print("device status word set", file=sys.stderr)
+            return 1
+    print("ok")
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -518,7 +567,12 @@ def main():
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of identical untimed steps before timing")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--target", choices=["layer", "lm_head"], help="profiler target: untimed calls, no JSON")
+    ap.add_argument("--m", default="1", help="with --target: comma-separated M values")
+    ap.add_argument("--calls", type=int, default=2, help="with --target: calls per M")
     args = ap.parse_args()
+    if args.target:
+        return run_target(args)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":

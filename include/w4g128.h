@@ -67,7 +67,12 @@
  *   - Output is bitwise deterministic for a given shape and M (independent of
  *     the grid size and of the SM count).
  *   - x and y must not overlap; y must not overlap packed or ws.
- *   - Finite inputs.  Products are exact in fp32 for every finite bf16 x.
+ *   - Finite inputs whose sums stay within fp32 range.  The kernels carry x
+ *     as fp16 scaled by one power of two per (128-row group, row): every
+ *     x within 2^29 of its group's largest magnitude is exact there, and
+ *     every product x * code is exact in fp32.  When all weights of a column
+ *     are zero (min = -q * scale exactly) the factorised sum leaves a
+ *     rounding residual of order 2^-24 * 1024 * scale * sum|x| instead of 0.
  */
 #ifndef W4G128_H
 #define W4G128_H
@@ -158,7 +163,8 @@ W4G128_API size_t w4g128_decode_step_workspace_bytes(const w4g128_matrix* mats, 
  * each matrix's shape, so every y_i is bitwise identical to what a separate
  * w4g128_gemv (M = 1) or w4g128_gemm_verify call returns, whatever the SM
  * count or the other matrices.  The descriptor array is read during the call
- * and may be reused afterwards. */
+ * and may be reused afterwards.  The matrices' N may sum to at most 2^30
+ * (W4G128_ERR_SHAPE beyond). */
 W4G128_API int w4g128_decode_step(const w4g128_matrix* mats, int count, int M, void* ws, size_t ws_bytes,
                                   void* stream);
 

@@ -704,21 +704,24 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Strea
 
 // ----------------------------------------------------------------- reduce kernel
 
-// M >= 2: folds the segment partials of every quad the schedule split between warps:
-// one thread per output (row, column), its S partial loads issued 16 at a
-// time, summed in segment order exactly as a single warp would have.  Quads
-// owned by one warp were written by the streaming kernel and are skipped.
+// M >= 2: folds the segment partials of every quad the schedule split between
+// warps.  One thread per 4 adjacent outputs of one row (16-byte loads), its S
+// partials loaded kRedBatch segments at a time and summed per output in
+// segment order exactly as a single warp would have.  Quads owned by one warp
+// were written by the streaming kernel and are skipped.
+constexpr int kRedBatch = 8;
+constexpr int kRedBlocksPerSM = 4;
 template <int MAXMAT>
-__global__ void __launch_bounds__(256) reduce_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
+__global__ void __launch_bounds__(256, kRedBlocksPerSM) reduce_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
   grid_dependency_wait();  // every partial of the streaming kernel is written and visible
-  const int rows = p.M;
-  const int per_quad = rows * 64;
+  const int units_per_quad = p.M * 16;  // (row, 4-column group) units
+  const int per_quad = p.M * 64;        // floats per partial slot
   const long long I = p.total_items;
-  const long long total = static_cast<long long>(p.total_quads) * per_quad;
-  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int gq = static_cast<int>(idx / per_quad);
-    const int o = static_cast<int>(idx - static_cast<long long>(gq) * per_quad);
+  const int total = p.total_quads * units_per_quad;
+  for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < total; u += gridDim.x * blockDim.x) {
+    const int gq = u / units_per_quad;
+    const int rem = u - gq * units_per_quad;
+    const int row = rem >> 4, col = 4 * (rem & 15);
     int lo = 0, hi = p.count - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -727,23 +730,31 @@ __global__ void __launch_bounds__(256) reduce_kernel(const __grid_constant__ Str
     const MatParams& m = p.mats[lo];
     const int q = gq - m.quad_begin;
     const int G = m.K / kGroup, S = div_up(G, kSegGroups), T = m.N / kTileN;
-    const int ncols = kTileN * min(kQuadTiles, T - kQuadTiles * q);
-    const int row = o / 64, col = o % 64;
-    if (col >= ncols) continue;
+    if (col >= kTileN * min(kQuadTiles, T - kQuadTiles * q)) continue;  // ragged last quad
     const long long q_first = m.item_begin + static_cast<long long>(q) * S;
     if (owner_of(q_first, I, p.W) == owner_of(q_first + S - 1, I, p.W)) continue;  // owned quad
-    const float* part = p.partials + q_first * per_quad + o;
-    float acc = 0.f;
-    for (int s0 = 0; s0 < S; s0 += 16) {  // up to 16 loads in flight, then fold in order
-      float v[16];
+    const float4* part = reinterpret_cast<const float4*>(p.partials + q_first * per_quad + row * 64 + col);
+    const int stride = per_quad / 4;  // float4s between consecutive segments
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < S; s0 += kRedBatch) {  // a batch of segments in flight, then fold in order
+      float4 v[kRedBatch];
 #pragma unroll
-      for (int u = 0; u < 16; ++u)
-        v[u] = (s0 + u < S) ? __ldcg(part + static_cast<long long>(s0 + u) * per_quad) : 0.f;
+      for (int k = 0; k < kRedBatch; ++k)
+        v[k] = (s0 + k < S) ? __ldcg(part + static_cast<long long>(s0 + k) * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int u = 0; u < 16; ++u)
-        if (s0 + u < S) acc = (s0 + u == 0) ? v[u] : acc + v[u];
+      for (int k = 0; k < kRedBatch; ++k) {
+        if (s0 + k < S) {
+          if (s0 + k == 0) {
+            acc = v[k];
+          } else {
+            acc.x += v[k].x; acc.y += v[k].y; acc.z += v[k].z; acc.w += v[k].w;
+          }
+        }
+      }
     }
-    m.y[static_cast<long long>(row) * m.N + kQuadTiles * kTileN * q + col] = to_bf16(acc);
+    uint32_t* yo = reinterpret_cast<uint32_t*>(m.y + static_cast<long long>(row) * m.N + kQuadTiles * kTileN * q + col);
+    yo[0] = static_cast<uint32_t>(to_bf16(acc.x)) | (static_cast<uint32_t>(to_bf16(acc.y)) << 16);
+    yo[1] = static_cast<uint32_t>(to_bf16(acc.z)) | (static_cast<uint32_t>(to_bf16(acc.w)) << 16);
   }
 }
 
@@ -827,7 +838,7 @@ bool make_plan(const HostMatrix* mats, int count, int M, const DeviceInfo& dev, 
     quads += NQ;
     groups += G;
     xbytes += static_cast<long long>(G) * pl.pkg;
-    if (quads > 0x7FFFFFFF || groups > 0x7FFFFFFF) return false;
+    if (quads > (1 << 24) || groups > 0x7FFFFFFF) return false;  // reduce_kernel indexes quads * 128 in int
   }
   pl.items = items;
   pl.total_quads = static_cast<int>(quads);
@@ -890,8 +901,10 @@ int launch_mode(const StreamParams<MAXMAT>& sp, int grid, cudaStream_t stream) {
   }
 
   if (MODE == kM1) return W4G128_OK;  // M = 1 folds split quads inside the streaming kernel
-  const long long outputs = static_cast<long long>(sp.total_quads) * sp.M * 64;
-  cfg.gridDim = dim3(static_cast<unsigned>(std::max(1LL, std::min((outputs + 255) / 256, 4096LL))));
+  // one thread per (quad, row, 4 columns), at most one resident wave
+  const long long units = static_cast<long long>(sp.total_quads) * sp.M * 16;
+  const long long wave = static_cast<long long>(device_info()->sms) * kRedBlocksPerSM;
+  cfg.gridDim = dim3(static_cast<unsigned>(std::max(1LL, std::min((units + 255) / 256, wave))));
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   if (cudaLaunchKernelEx(&cfg, reduce_kernel<MAXMAT>, sp) != cudaSuccess) {
