@@ -37,6 +37,14 @@ sys.path.insert(0, ROOT)
 METRIC = "int4-g128 GEMV HBM GB/s & % of GB300 peak at M=1 and M=8; µs/call"
 LAYER = [("q", 5120, 6144), ("k", 5120, 6144), ("v", 5120, 6144), ("o", 6144, 5120),
          ("gate_up", 5120, 34816), ("down", 17408, 5120)]
+# Single-call shapes timed for us/call: the square case, the four distinct
+# layer shapes, the full-vocabulary lm_head and its first 131072 columns
+# (a prefix view of the same packed buffer).
+SHAPES = [("square", 4096, 4096), ("q_k_v", 5120, 6144), ("o", 6144, 5120), ("gate_up", 5120, 34816),
+          ("down", 17408, 5120), ("lm_head", 5120, 248320), ("lm_head_slice", 5120, 131072)]
+LM_HEAD = (5120, 248320)
+N_LAYERS = 64
+L2_BYTES = 129 * 1024 * 1024
 SEED = 20260001
 NCOPY = 4
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0}
@@ -294,13 +302,14 @@ def run_ours(args):
         ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
         return xs_h, xs, ys, descs, ws
 
-    io = {M: make_io(M) for M in (1, 8)}
+    MS = (1, 2, 4, 8)
+    io = {M: make_io(M) for M in MS}
 
     # ---- parity gate on sampled outputs (first and last weight copy)
     import oracle
     O = oracle.Oracle()
     worst = {}
-    for M in (1, 8):
+    for M in MS:
         xs_h, xs, ys, descs, ws = io[M]
         for c in (0, NCOPY - 1):
             w.w4g128_decode_step(descs[c], M, ws, stream=st)
@@ -372,43 +381,117 @@ def run_ours(args):
             w.w4g128_decode_step(descs1[k % NCOPY], 1, ws1, stream=st)
             k += 1
         torch.cuda.synchronize()
-    total1 = timed_graph(1, args.steps, args.warmup)
-    total8 = timed_graph(8, args.steps, args.warmup)
+    totals = {}
+    for M in MS:
+        totals[M] = timed_graph(M, args.steps, args.warmup)
     clk = clocks.stop()
+    total1, total8 = totals[1], totals[8]
     launch1, launch8 = total1 / args.steps, total8 / args.steps
 
     bytes1, bytes8 = algorithmic_bytes(1), algorithmic_bytes(8)
     value = world * args.steps * bytes1 / total1 / 1e9
     value8 = world * args.steps * bytes8 / total8 / 1e9
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
+    by_m = {}
+    for M in MS:
+        gbs = algorithmic_bytes(M) / (totals[M] / args.steps) / 1e9
+        by_m[str(M)] = {"us_per_step": round(1e6 * totals[M] / args.steps, 3), "GBps": round(gbs, 1),
+                        "frac": round(gbs / peak, 4), "cost_ratio_vs_M1": round(totals[M] / total1, 4)}
 
-    # ---- per-shape single-matrix calls (gemv at M = 1, verify at M = 8), us per call, graph-timed
+    def pack_device(K, N, matrix_id):
+        codes = torch.empty((K // 8) * N, dtype=torch.int32, device="cuda")
+        s_ = torch.empty((K // 128) * N, dtype=torch.int16, device="cuda")
+        m_ = torch.empty_like(s_)
+        synth.fill_device(SEED, matrix_id, K, N, codes.data_ptr(), s_.data_ptr(), m_.data_ptr(), st)
+        packed = torch.empty(w.w4g128_packed_bytes(K, N), dtype=torch.uint8, device="cuda")
+        w.w4g128_pack(codes, s_, m_, K, N, packed, stream=st)
+        return packed
+
+    def graph_us(call, reps):
+        for r in range(3):
+            call(st, r)
+        torch.cuda.synchronize()
+        g = capture([lambda cs, r=r: call(cs, r) for r in range(reps)])
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    # ---- single-matrix calls (gemv at M = 1, verify at M = 8), us per call, graph-timed over
+    # enough rotating copies to exceed twice the L2
     per_call = {}
-    for M in (1, 8):
-        _, xs, ys, _, _ = io[M]
-        for i, (name, K, N) in enumerate(LAYER[2:], start=2):  # v (q/k-shaped), o, gate_up, down
-            wsb = w.w4g128_workspace_bytes(M, K, N)
-            wsd = torch.empty(wsb, dtype=torch.uint8, device="cuda")
-            reps = 64
+    lm_packed = None
+    for si, (name, K, N) in enumerate(SHAPES):
+        if name == "lm_head_slice":
+            mats = [lm_packed]  # the first 131072 columns, in place
+        else:
+            first = pack_device(K, N, 50 + si)
+            ncopy = max(1, -(-2 * L2_BYTES // weight_bytes(K, N)))
+            mats = [first] + [first.clone() for _ in range(ncopy - 1)]
+            if name == "lm_head":
+                lm_packed = first
+        for M in (1, 8):
+            x = torch.from_numpy(synth.x(SEED, 300 + si, M, K).view(np.int16)).cuda()
+            y = torch.empty(M * N, dtype=torch.int16, device="cuda")
+            wsd = torch.empty(w.w4g128_workspace_bytes(M, K, N), dtype=torch.uint8, device="cuda")
 
-            def call(cs, r, M=M, i=i, K=K, N=N, wsd=wsd, xs=xs, ys=ys):
+            def call(cs, r, M=M, K=K, N=N, wsd=wsd, x=x, y=y, mats=mats):
                 if M == 1:
-                    w.w4g128_gemv(copies[r % NCOPY][i], xs[i], ys[i], K, N, wsd, stream=cs)
+                    w.w4g128_gemv(mats[r % len(mats)], x, y, K, N, wsd, stream=cs)
                 else:
-                    w.w4g128_gemm_verify(copies[r % NCOPY][i], xs[i], ys[i], M, K, N, wsd, stream=cs)
-            for r in range(4):
-                call(st, r)
-            torch.cuda.synchronize()
-            g = capture([lambda cs, r=r: call(cs, r) for r in range(reps)])
-            g.replay()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            g.replay()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            us = e0.elapsed_time(e1) * 1e3 / reps
-            per_call[f"{name}_{K}x{N}_M{M}"] = {"us": round(us, 3),
-                                                "weight_GBps": round(weight_bytes(K, N) / us / 1e3, 1)}
+                    w.w4g128_gemm_verify(mats[r % len(mats)], x, y, M, K, N, wsd, stream=cs)
+            us = graph_us(call, 16 if weight_bytes(K, N) > L2_BYTES else 64)
+            gbs = (weight_bytes(K, N) + 2 * M * (K + N)) / us / 1e3
+            per_call[f"{name}_{K}x{N}_M{M}"] = {"us": round(us, 3), "GBps": round(gbs, 1),
+                                                "frac": round(gbs / peak, 4), "copies": len(mats)}
+        if name != "lm_head":
+            del mats
+    del lm_packed
+    torch.cuda.synchronize()
+
+    # ---- the whole decode-step weight stream: 64 layer sets + the lm_head, one decode_step call
+    full = {}
+    fmats = [(K, N) for _ in range(N_LAYERS) for _, K, N in LAYER] + [LM_HEAD]
+    fpacked = [pack_device(K, N, 1000 + j) for j, (K, N) in enumerate(fmats)]
+    torch.cuda.synchronize()
+    fbytes_w = sum(weight_bytes(K, N) for K, N in fmats)
+    for M in (1, 8):
+        xs_f = {}
+        for K in sorted({K for K, _ in fmats}):
+            xs_f[K] = torch.from_numpy(synth.x(SEED, 400 + K, M, K).view(np.int16)).cuda()
+        ys_f = [torch.empty(M * N, dtype=torch.int16, device="cuda") for _, N in fmats]
+        descs_f = [(fpacked[j], xs_f[K], ys_f[j], K, N) for j, (K, N) in enumerate(fmats)]
+        wsf = torch.empty(w.w4g128_decode_step_workspace_bytes(descs_f, M), dtype=torch.uint8, device="cuda")
+        w.w4g128_decode_step(descs_f, M, wsf, stream=st)
+        torch.cuda.synchronize()
+        if w.w4g128_workspace_status(wsf, st) != 0:
+            print(json.dumps({"error": "device status word set in the full decode step: run void"}))
+            return 1
+        for j in (0, len(fmats) - 1):  # sampled parity: first layer matrix and the lm_head
+            K, N = fmats[j]
+            rng = np.random.default_rng(77 + M + j)
+            cols = np.unique(np.concatenate([[0, N - 1], rng.integers(0, N, 16)]))
+            cc, ss, mm = synth.columns(SEED, 1000 + j, K, N, cols)
+            y_ref, a = O.gemm(xs_f[K].cpu().numpy().view(np.uint16).reshape(M, K), cc, ss, mm)
+            yv = oracle.bf16_bits_to_f64(ys_f[j].cpu().numpy().view(np.uint16).reshape(M, N)[:, cols])
+            ok, ratio = oracle.accept(yv, y_ref, a, O)
+            if not ok.all():
+                print(json.dumps({"error": f"parity mismatch in the full decode step M={M}: run void"}))
+                return 1
+        us = graph_us(lambda cs, r: w.w4g128_decode_step(descs_f, M, wsf, stream=cs), 5)
+        fb = fbytes_w + sum(2 * M * (K + N) for K, N in fmats)
+        gbs = fb / us / 1e3
+        full[f"M{M}"] = {"matrices": len(fmats), "weight_bytes": fbytes_w, "ms_per_step": round(us / 1e3, 4),
+                         "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
+                         "steps_per_s": round(1e6 / us, 1)}
+        del descs_f, ys_f, xs_f, wsf
+    del fpacked
+    torch.cuda.synchronize()
 
     # ---- live bandwidth probes: a pure read stream and a copy
     probe = {}
@@ -464,8 +547,6 @@ def run_ours(args):
     if rank != 0:
         return 0
 
-    peaks, peak_kind = measured_peaks()
-    peak = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
     achieved = bytes1 / launch1 / 1e9
     achieved8 = bytes8 / launch8 / 1e9
     cpu = None
@@ -496,7 +577,9 @@ def run_ours(args):
         "m8": {"value": round(value8, 1), "unit": "GB/s", "ms_per_step": round(1e3 * total8 / args.steps, 5),
                "achieved": round(achieved8, 1), "frac": round(achieved8 / peak, 4),
                "verify_cost_ratio_t8_over_t1": round(total8 / total1, 4)},
+        "layer_step_by_M": by_m,
         "us_per_call": per_call,
+        "full_decode_step": full,
         "bandwidth_probes": probe,
         "frac_of_read_probe": {"m1": round(achieved / probe["read_GBps"], 4),
                                "m8": round(achieved8 / probe["read_GBps"], 4)},
@@ -507,6 +590,7 @@ def run_ours(args):
         "clocks": clk,
         "cpu_baseline": cpu,
         "equivalent_tok_per_s_ceiling_full_27B_weight_set": round(achieved * 1e9 / 14044774400, 1),
+        "measured_tok_per_s_full_decode_step_M1": full["M1"]["steps_per_s"],
     }
     print(json.dumps(out), flush=True)
     return 0

@@ -72,6 +72,9 @@ enum Mode : int {
 #ifndef W4G128_RING_DEPTH
 #define W4G128_RING_DEPTH 2
 #endif
+#ifndef W4G128_SEG_GROUPS_M1
+#define W4G128_SEG_GROUPS_M1 4
+#endif
 constexpr int kNW = W4G128_WARPS_PER_CTA;  // warps per CTA
 constexpr int kDepth = W4G128_RING_DEPTH;  // ring slots per warp
 
@@ -87,6 +90,14 @@ constexpr int kDepth = W4G128_RING_DEPTH;  // ring slots per warp
 template <int MODE> struct Pkg;
 template <> struct Pkg<kM1> { static constexpr int kRows = 1, kRowBytes = 320, kBytes = 336; };
 template <> struct Pkg<kMMA> { static constexpr int kRows = 8, kRowBytes = 320, kBytes = 2624; };
+
+// Groups per split-K segment (an item's K extent): fixed per mode, never by
+// the grid, so every summation order depends on the shape and M alone.  At
+// M = 1 a segment partial is 256 bytes, so shorter segments are cheap and give
+// small matrices enough items to occupy every SM; at M >= 2 a partial is
+// 2 KB and segments stay at 512 rows.
+template <int MODE>
+__host__ __device__ constexpr int seg_groups() { return MODE == kM1 ? W4G128_SEG_GROUPS_M1 : kSegGroups; }
 
 template <int MODE>
 __host__ __device__ constexpr int slot_bytes() { return kQuadTiles * kBlockBytes + Pkg<MODE>::kBytes; }
@@ -139,12 +150,12 @@ struct Cursor {
   int G, S, NQ, T, ntiles;
 };
 
-template <int MAXMAT>
+template <int MODE, int MAXMAT>
 __device__ __forceinline__ void cursor_load(Cursor& c, const StreamParams<MAXMAT>& p, int mi) {
   const MatParams& m = p.mats[mi];
   c.mi = mi;
   c.G = m.K / kGroup;
-  c.S = div_up(c.G, kSegGroups);
+  c.S = div_up(c.G, seg_groups<MODE>());
   c.T = m.N / kTileN;
   c.NQ = div_up(c.T, kQuadTiles);
 }
@@ -156,13 +167,13 @@ __device__ __forceinline__ void cursor_seek(Cursor& c, const StreamParams<MAXMAT
     const int mid = (lo + hi + 1) >> 1;
     if (p.mats[mid].item_begin <= item) lo = mid; else hi = mid - 1;
   }
-  cursor_load(c, p, lo);
+  cursor_load<MODE>(c, p, lo);
   const long long local = item - p.mats[lo].item_begin;
   c.item = item;
   c.q = static_cast<int>(local / c.S);
   c.s = static_cast<int>(local - static_cast<long long>(c.q) * c.S);
-  c.g = c.s * kSegGroups;
-  c.g_end = min(c.g + kSegGroups, c.G);
+  c.g = c.s * seg_groups<MODE>();
+  c.g_end = min(c.g + seg_groups<MODE>(), c.G);
   c.ntiles = min(kQuadTiles, c.T - kQuadTiles * c.q);
   c.src = p.mats[lo].packed + static_cast<long long>(c.q) * c.G * kQuadBytes +
           static_cast<long long>(c.g) * c.ntiles * kBlockBytes;
@@ -176,7 +187,7 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const StreamParams<MAXMAT
   if (++c.g < c.g_end) return;
   ++c.item;
   if (++c.s < c.S) {
-    c.g_end = min(c.g + kSegGroups, c.G);
+    c.g_end = min(c.g + seg_groups<MODE>(), c.G);
     return;
   }
   c.s = 0;
@@ -184,16 +195,16 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const StreamParams<MAXMAT
   if (++c.q < c.NQ) {  // the next quad starts where this one ended
     c.ntiles = min(kQuadTiles, c.T - kQuadTiles * c.q);
     c.xsrc = p.mats[c.mi].xpkg;
-    c.g_end = min(kSegGroups, c.G);
+    c.g_end = min(seg_groups<MODE>(), c.G);
     return;
   }
   if (c.mi + 1 == p.count) return;  // past the end; never dereferenced
-  cursor_load(c, p, c.mi + 1);
+  cursor_load<MODE>(c, p, c.mi + 1);
   c.q = 0;
   c.ntiles = min(kQuadTiles, c.T);
   c.src = p.mats[c.mi].packed;
   c.xsrc = p.mats[c.mi].xpkg;
-  c.g_end = min(kSegGroups, c.G);
+  c.g_end = min(seg_groups<MODE>(), c.G);
 }
 
 // Owner warp of an item under the balanced split [floor(wI/W), floor((w+1)I/W)).
@@ -402,7 +413,7 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
   constexpr int kSlot = slot_bytes<MODE>();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane >> 2, c = lane & 3;
-  const int wg = blockIdx.x * kNW + warp;
+  const int wg = blockIdx.x * (blockDim.x >> 5) + warp;  // CTAs hold up to kNW warps
   if (wg >= p.W) return;  // whole warp; there are no block-wide barriers
 
   const long long I = p.total_items;
@@ -729,7 +740,7 @@ __global__ void __launch_bounds__(256, kRedBlocksPerSM) reduce_kernel(const __gr
     }
     const MatParams& m = p.mats[lo];
     const int q = gq - m.quad_begin;
-    const int G = m.K / kGroup, S = div_up(G, kSegGroups), T = m.N / kTileN;
+    const int G = m.K / kGroup, S = div_up(G, seg_groups<kMMA>()), T = m.N / kTileN;
     if (col >= kTileN * min(kQuadTiles, T - kQuadTiles * q)) continue;  // ragged last quad
     const long long q_first = m.item_begin + static_cast<long long>(q) * S;
     if (owner_of(q_first, I, p.W) == owner_of(q_first + S - 1, I, p.W)) continue;  // owned quad
@@ -811,7 +822,7 @@ const DeviceInfo* device_info() {
 struct Plan {
   int mode = 0, rows = 1, pkg = 0;
   long long items = 0;
-  int W = 0, grid = 0, total_quads = 0, total_groups = 0;
+  int W = 0, grid = 0, cta_warps = kNW, total_quads = 0, total_groups = 0;
   size_t off_tickets = 0, off_xpkg = 0, off_partials = 0, bytes = 0;
   std::vector<long long> item_begin, xpkg_off;
   std::vector<int> quad_begin, g_begin;
@@ -829,7 +840,8 @@ bool make_plan(const HostMatrix* mats, int count, int M, const DeviceInfo& dev, 
   pl.xpkg_off.resize(count);
   long long items = 0, xbytes = 0, quads = 0, groups = 0;
   for (int i = 0; i < count; ++i) {
-    const int G = mats[i].K / kGroup, S = div_up(G, kSegGroups), NQ = div_up(mats[i].N, kTileN * kQuadTiles);
+    const int seg = (pl.mode == kM1) ? seg_groups<kM1>() : seg_groups<kMMA>();
+    const int G = mats[i].K / kGroup, S = div_up(G, seg), NQ = div_up(mats[i].N, kTileN * kQuadTiles);
     pl.item_begin[i] = items;
     pl.quad_begin[i] = static_cast<int>(quads);
     pl.g_begin[i] = static_cast<int>(groups);
@@ -845,7 +857,10 @@ bool make_plan(const HostMatrix* mats, int count, int M, const DeviceInfo& dev, 
   pl.total_groups = static_cast<int>(groups);
   const long long max_warps = static_cast<long long>(dev.sms) * dev.occ[pl.mode] * kNW;
   pl.W = static_cast<int>(std::min<long long>(items, max_warps));
-  pl.grid = div_up(pl.W, kNW);
+  // Spread the warps over every SM: a call with fewer items than the grid
+  // holds warps gets smaller CTAs rather than fewer SMs.
+  pl.cta_warps = std::min(kNW, div_up(pl.W, dev.sms));
+  pl.grid = div_up(pl.W, pl.cta_warps);
   pl.off_tickets = 256;  // after the status word
   pl.off_xpkg = align_up(pl.off_tickets + sizeof(unsigned) * static_cast<size_t>(quads), 256);
   pl.off_partials = align_up(pl.off_xpkg + static_cast<size_t>(xbytes), 256);
@@ -880,14 +895,14 @@ void fill_params(StreamParams<MAXMAT>& sp, const HostMatrix* mats, int count, in
 }
 
 template <int MODE, int MAXMAT>
-int launch_mode(const StreamParams<MAXMAT>& sp, int grid, cudaStream_t stream) {
+int launch_mode(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, cudaStream_t stream) {
   const int prep_blocks = std::max(1, std::min(div_up(sp.total_groups * 32, 256), 1024));
   prep_kernel<MODE, MAXMAT><<<prep_blocks, 256, 0, stream>>>(sp);
   if (cudaGetLastError() != cudaSuccess) return W4G128_ERR_CUDA;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kNW * 32);
+  cfg.blockDim = dim3(cta_warps * 32);
   cfg.dynamicSmemBytes = smem_bytes<MODE>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -918,8 +933,8 @@ template <int MAXMAT>
 int launch_with(const HostMatrix* mats, int count, int M, const Plan& pl, void* ws, cudaStream_t stream) {
   static thread_local StreamParams<MAXMAT> sp;  // large for MAXMAT = 512: keep it off the stack
   fill_params(sp, mats, count, M, pl, ws);
-  if (pl.mode == kMMA) return launch_mode<kMMA>(sp, pl.grid, stream);
-  return launch_mode<kM1>(sp, pl.grid, stream);
+  if (pl.mode == kMMA) return launch_mode<kMMA>(sp, pl.grid, pl.cta_warps, stream);
+  return launch_mode<kM1>(sp, pl.grid, pl.cta_warps, stream);
 }
 
 }  // namespace
