@@ -126,7 +126,7 @@ W4G128_API int w4g128_unpack(const void* packed, int K, int N, uint32_t* codes, 
                              w4g128_bf16* mins, void* stream);
 
 /* Workspace bytes needed by w4g128_gemm_verify(M, K, N) on the current
- * device (w4g128_gemv is M = 1).  Returns 0 for invalid arguments. */
+ * device (and by w4g128_gemv, M = 1).  Returns 0 for invalid arguments. */
 W4G128_API size_t w4g128_workspace_bytes(int M, int K, int N);
 
 /* y[1][N] = x[1][K] . dequant(W): the batch-1 decode GEMV (CUDA cores,
@@ -136,9 +136,12 @@ W4G128_API int w4g128_gemv(const void* packed, const w4g128_bf16* x, w4g128_bf16
                            void* ws, size_t ws_bytes, void* stream);
 
 /* y[M][N] = x[M][K] . dequant(W) for 1 <= M <= 8: the speculative M-row
- * verify step (one weight pass for M draft rows; tensor cores via warp MMA
- * for M >= 2; M = 1 is the same computation as w4g128_gemv).  Token Rush
- * README, progress table steps 13-14 and 28. */
+ * verify step (one weight pass for M draft rows, on the tensor cores via
+ * warp MMA).  Row m of the result is bitwise identical to this call on row m
+ * alone (M = 1), for every M: a verify pass reproduces exactly what the same
+ * arithmetic gives one token at a time.  w4g128_gemv (CUDA cores) agrees with
+ * it within the acceptance bound, not bitwise.  Token Rush README, progress
+ * table steps 13-14 and 28. */
 W4G128_API int w4g128_gemm_verify(const void* packed, const w4g128_bf16* x, w4g128_bf16* y, int M, int K,
                                   int N, void* ws, size_t ws_bytes, void* stream);
 
@@ -151,7 +154,8 @@ typedef struct {
   int N;
 } w4g128_matrix;
 
-/* Workspace bytes for w4g128_decode_step over these matrices at this M. */
+/* Workspace bytes for w4g128_decode_step or w4g128_verify_step over these
+ * matrices at this M. */
 W4G128_API size_t w4g128_decode_step_workspace_bytes(const w4g128_matrix* mats, int count, int M);
 
 /* Streams every matrix of `mats` (a HOST array of `count` descriptors,
@@ -166,6 +170,16 @@ W4G128_API size_t w4g128_decode_step_workspace_bytes(const w4g128_matrix* mats, 
  * and may be reused afterwards.  The matrices' N may sum to at most 2^30
  * (W4G128_ERR_SHAPE beyond). */
 W4G128_API int w4g128_decode_step(const w4g128_matrix* mats, int count, int M, void* ws, size_t ws_bytes,
+                                  void* stream);
+
+/* w4g128_decode_step with the verify arithmetic at every M, M = 1 included:
+ * row m of each y_i is bitwise identical to w4g128_gemm_verify on matrix i
+ * and row m alone, so decoding with this entry point at M = 1 and verifying
+ * drafts with it at M > 1 give the same bits for the same token (the exact
+ * speculative-decoding property; Token Rush README, progress table step 28).
+ * Same arguments, workspace query and bitwise guarantees as
+ * w4g128_decode_step; at M >= 2 the two entry points compute the same thing. */
+W4G128_API int w4g128_verify_step(const w4g128_matrix* mats, int count, int M, void* ws, size_t ws_bytes,
                                   void* stream);
 
 /* Size of the fixed device scratch array behind w4g128_gemv_noalloc (16 MiB). */

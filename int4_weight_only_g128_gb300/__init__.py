@@ -14,7 +14,7 @@ __all__ = [
     "W4G128Error", "lib", "exported_symbols",
     "w4g128_status_string", "w4g128_packed_bytes", "w4g128_pack", "w4g128_unpack",
     "w4g128_workspace_bytes", "w4g128_gemv", "w4g128_gemm_verify",
-    "w4g128_decode_step_workspace_bytes", "w4g128_decode_step", "w4g128_workspace_status",
+    "w4g128_decode_step_workspace_bytes", "w4g128_decode_step", "w4g128_verify_step", "w4g128_workspace_status",
     "w4g128_probe_read", "w4g128_probe_copy", "w4g128_probe_sink_bytes", "w4g128_gemv_noalloc",
     "MAX_M", "MAX_MATRICES",
 ]
@@ -89,6 +89,8 @@ def lib():
     L.w4g128_probe_copy.argtypes = [p, p, sz, p]
     L.w4g128_probe_sink_bytes.restype = sz
     L.w4g128_probe_sink_bytes.argtypes = []
+    L.w4g128_verify_step.restype = i
+    L.w4g128_verify_step.argtypes = [ctypes.POINTER(_Matrix), i, i, p, sz, p]
     L.w4g128_gemv_noalloc.restype = i
     L.w4g128_gemv_noalloc.argtypes = [p, p, p, i, i, p]
     _lib = L
@@ -172,6 +174,13 @@ def w4g128_decode_step(mats, M, ws, ws_bytes=None, stream=None):
     arr = _matrices(mats)
     wb = _nbytes(ws) if ws_bytes is None else ws_bytes
     _check("w4g128_decode_step", lib().w4g128_decode_step(arr, len(mats), M, _ptr(ws), wb, _stream(stream)))
+
+
+def w4g128_verify_step(mats, M, ws, ws_bytes=None, stream=None):
+    """decode_step with the verify (warp-MMA) arithmetic at every M, M = 1 included."""
+    arr = _matrices(mats)
+    wb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    _check("w4g128_verify_step", lib().w4g128_verify_step(arr, len(mats), M, _ptr(ws), wb, _stream(stream)))
 
 
 def w4g128_workspace_status(ws, stream=None):

@@ -39,12 +39,15 @@ struct HostMatrix {
   int K, N;
 };
 
-// Workspace bytes for streaming these matrices at this M on the current device.
-// Returns 0 on invalid arguments.
-size_t stream_workspace_bytes(const HostMatrix* mats, int count, int M);
+// Workspace bytes for streaming these matrices at this M on the current device
+// (verify: the verify arithmetic also at M = 1).  Returns 0 on invalid
+// arguments.
+size_t stream_workspace_bytes(const HostMatrix* mats, int count, int M, bool verify);
 
-// Launches the prep and streaming kernels; the API layer validates arguments.
-int launch_stream(const HostMatrix* mats, int count, int M, void* ws, size_t ws_bytes,
+// Launches the prep, streaming and (M >= 2) reduce kernels; the API layer
+// validates arguments.  M >= 2 always uses the verify arithmetic (warp MMA);
+// at M = 1 `verify` selects it over the CUDA-core decode arithmetic.
+int launch_stream(const HostMatrix* mats, int count, int M, bool verify, void* ws, size_t ws_bytes,
                   cudaStream_t stream);
 
 int read_workspace_status(const void* ws, int* status_out, cudaStream_t stream);

@@ -63,7 +63,8 @@ namespace {
 
 enum Mode : int {
   kM1 = 0,   // M = 1, CUDA cores: bf16 x bf16 -> fp32 FMA on the dequantised pairs
-  kMMA = 1,  // M <= 8, warp MMA m16n8k16 bf16 -> f32 with the weights as the 16-row operand
+  kMMA = 1,  // M <= 8, warp MMA m16n8k16 f16 -> f32 with the weights as the 16-row operand
+  kMMA1 = 2, // M = 1 with the verify arithmetic: the warp MMA, every B column carrying the one x row
 };
 
 #ifndef W4G128_WARPS_PER_CTA
@@ -90,6 +91,7 @@ constexpr int kDepth = W4G128_RING_DEPTH;  // ring slots per warp
 template <int MODE> struct Pkg;
 template <> struct Pkg<kM1> { static constexpr int kRows = 1, kRowBytes = 320, kBytes = 336; };
 template <> struct Pkg<kMMA> { static constexpr int kRows = 8, kRowBytes = 320, kBytes = 2624; };
+template <> struct Pkg<kMMA1> { static constexpr int kRows = 1, kRowBytes = 320, kBytes = 336; };
 
 // Groups per split-K segment (an item's K extent): fixed per mode, never by
 // the grid, so every summation order depends on the shape and M alone.  At
@@ -307,7 +309,7 @@ __device__ __forceinline__ uint16_t to_bf16(float v) { return __bfloat16_as_usho
 
 // Rows of the per-lane accumulators: M = 1 keeps (column r, column r+8);
 // the MMA keeps (r, 2c), (r, 2c+1), (r+8, 2c), (r+8, 2c+1).
-template <int MODE> struct Acc { static constexpr int kN = (MODE == kMMA) ? 4 : 2; };
+template <int MODE> struct Acc { static constexpr int kN = (MODE == kM1) ? 2 : 4; };
 
 // One chunk: every tile of the quad for one group, added into seg[t][*].
 // FULL: the quad has all 4 tiles, so the tiles form one straight-line block
@@ -356,8 +358,15 @@ __device__ __forceinline__ void compute_chunk(const uint8_t* sl, int ntiles, int
       }
     }
   } else {
-    // (X_g, f) of rows 2c and 2c + 1
-    const float4 xq = *reinterpret_cast<const float4*>(pk + Pkg<MODE>::kRows * Pkg<MODE>::kRowBytes + 16 * c);
+    // (X_g, f) of rows 2c and 2c + 1; with one x row (kMMA1) every lane takes
+    // row 0's pair, and only lanes c == 0 (row 0) are ever stored
+    float4 xq;
+    if constexpr (MODE == kMMA) {
+      xq = *reinterpret_cast<const float4*>(pk + Pkg<MODE>::kRows * Pkg<MODE>::kRowBytes + 16 * c);
+    } else {
+      const float2 t0 = *reinterpret_cast<const float2*>(pk + Pkg<MODE>::kRowBytes);
+      xq = make_float4(t0.x, t0.y, t0.x, t0.y);
+    }
     const float2 Xab = make_float2(xq.x, xq.z);
     const float2 fab = make_float2(xq.y, xq.w);
     const float2 fab16 = make_float2(xq.y * 0.0625f, xq.w * 0.0625f);
@@ -486,7 +495,7 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
     const int ntiles = cc.ntiles;
     // M = 1: a straight-line body for full quads lets the compiler interleave
     // the four tiles; the MMA path keeps per-tile blocks (register budget).
-    if (MODE != kMMA && ntiles == kQuadTiles)
+    if (MODE == kM1 && ntiles == kQuadTiles)
       compute_chunk<MODE, true>(ring + slot * kSlot, ntiles, lane, seg);
     else
       compute_chunk<MODE, false>(ring + slot * kSlot, ntiles, lane, seg);
@@ -512,7 +521,7 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
       const long long q_first = m.item_begin + static_cast<long long>(cc.q) * S;
       const long long q_last = q_first + S - 1;
       const bool owned = (q_first >= it_a) && (q_last < it_b);
-      if constexpr (MODE != kMMA) {
+      if constexpr (MODE == kM1) {
         // reduce the 4 lane classes c of each column (same tree on every lane)
 #pragma unroll
         for (int t = 0; t < kQuadTiles; ++t)
@@ -524,7 +533,7 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
             seg[t][e] = v;
           }
       }
-      const int rows = (MODE == kMMA) ? p.M : 1;
+      const int rows = (MODE == kM1) ? 1 : p.M;
       if (owned) {
 #pragma unroll
         for (int t = 0; t < kQuadTiles; ++t)
@@ -532,7 +541,7 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
           for (int e = 0; e < NA; ++e) tot[t][e] = (cc.s == 0) ? seg[t][e] : tot[t][e] + seg[t][e];
       } else {
         float* part = p.partials + cc.item * rows * 64;  // one slot per (matrix, quad, segment)
-        if constexpr (MODE != kMMA) {
+        if constexpr (MODE == kM1) {
           // lane (r, c) stores tile c's columns r and r + 8
           if (c < ntiles) {
             part[16 * c + r] = pick(seg, c, 0);
@@ -563,7 +572,7 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
       if (quad_end) {
         const int n0 = kQuadTiles * kTileN * cc.q;
         if (owned) {
-          if constexpr (MODE != kMMA) {
+          if constexpr (MODE == kM1) {
             if (c < ntiles) {
               m.y[n0 + 16 * c + r] = to_bf16(pick(tot, c, 0));
               m.y[n0 + 16 * c + r + 8] = to_bf16(pick(tot, c, 1));
@@ -584,8 +593,9 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
               }
             }
           }
-        } else if constexpr (MODE == kM1) {
-          // Split quad at M = 1: publish, take a ticket; the last arriver folds
+        } else if constexpr (MODE != kMMA) {
+          // Split quad at M = 1 (both M = 1 modes leave the quad's 64 columns
+          // in order in a partial slot): publish, take a ticket; the last arriver folds
           // the segment partials in segment order and writes y.
           __threadfence();
           __syncwarp();
@@ -639,7 +649,7 @@ template <int MODE, int MAXMAT>
 __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
   grid_dependents_launch();
   const int tid = blockIdx.x * blockDim.x + threadIdx.x, nthreads = gridDim.x * blockDim.x;
-  if (MODE == kM1)
+  if (MODE != kMMA)
     for (int i = tid; i < p.total_quads; i += nthreads) p.tickets[i] = 0u;
   if (tid == 0) *p.status = 0u;
 
@@ -773,7 +783,7 @@ __global__ void __launch_bounds__(256, kRedBlocksPerSM) reduce_kernel(const __gr
 
 struct DeviceInfo {
   int sms = 0;
-  int occ[2] = {0, 0};  // CTAs per SM per mode
+  int occ[3] = {0, 0, 0};  // CTAs per SM per mode
   bool ok = false;
 };
 
@@ -811,6 +821,7 @@ const DeviceInfo* device_info() {
     if (d.ok) {
       setup_mode<kM1>(d);
       setup_mode<kMMA>(d);
+      setup_mode<kMMA1>(d);
       if (cudaGetLastError() != cudaSuccess) d.ok = false;
     }
     g_dev[dev] = d;
@@ -830,17 +841,17 @@ struct Plan {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-bool make_plan(const HostMatrix* mats, int count, int M, const DeviceInfo& dev, Plan& pl) {
-  pl.mode = (M == 1) ? kM1 : kMMA;
+bool make_plan(const HostMatrix* mats, int count, int M, bool verify, const DeviceInfo& dev, Plan& pl) {
+  pl.mode = (M > 1) ? kMMA : (verify ? kMMA1 : kM1);
   pl.rows = M;
-  pl.pkg = (pl.mode == kM1) ? Pkg<kM1>::kBytes : Pkg<kMMA>::kBytes;
+  pl.pkg = (pl.mode == kMMA) ? Pkg<kMMA>::kBytes : Pkg<kM1>::kBytes;
   pl.item_begin.resize(count);
   pl.quad_begin.resize(count);
   pl.g_begin.resize(count);
   pl.xpkg_off.resize(count);
   long long items = 0, xbytes = 0, quads = 0, groups = 0;
   for (int i = 0; i < count; ++i) {
-    const int seg = (pl.mode == kM1) ? seg_groups<kM1>() : seg_groups<kMMA>();
+    const int seg = (pl.mode == kM1) ? seg_groups<kM1>() : seg_groups<kMMA>();  // kMMA1 folds like kMMA
     const int G = mats[i].K / kGroup, S = div_up(G, seg), NQ = div_up(mats[i].N, kTileN * kQuadTiles);
     pl.item_begin[i] = items;
     pl.quad_begin[i] = static_cast<int>(quads);
@@ -915,7 +926,7 @@ int launch_mode(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, cudaStr
     return W4G128_ERR_CUDA;
   }
 
-  if (MODE == kM1) return W4G128_OK;  // M = 1 folds split quads inside the streaming kernel
+  if (MODE != kMMA) return W4G128_OK;  // M = 1 folds split quads inside the streaming kernel
   // one thread per (quad, row, 4 columns), at most one resident wave
   const long long units = static_cast<long long>(sp.total_quads) * sp.M * 16;
   const long long wave = static_cast<long long>(device_info()->sms) * kRedBlocksPerSM;
@@ -934,6 +945,7 @@ int launch_with(const HostMatrix* mats, int count, int M, const Plan& pl, void* 
   static thread_local StreamParams<MAXMAT> sp;  // large for MAXMAT = 512: keep it off the stack
   fill_params(sp, mats, count, M, pl, ws);
   if (pl.mode == kMMA) return launch_mode<kMMA>(sp, pl.grid, pl.cta_warps, stream);
+  if (pl.mode == kMMA1) return launch_mode<kMMA1>(sp, pl.grid, pl.cta_warps, stream);
   return launch_mode<kM1>(sp, pl.grid, pl.cta_warps, stream);
 }
 
@@ -944,19 +956,20 @@ bool device_is_sm103() {
   return d != nullptr && d->ok;
 }
 
-size_t stream_workspace_bytes(const HostMatrix* mats, int count, int M) {
+size_t stream_workspace_bytes(const HostMatrix* mats, int count, int M, bool verify) {
   const DeviceInfo* d = device_info();
   if (d == nullptr || !d->ok) return 0;
   Plan pl;
-  if (!make_plan(mats, count, M, *d, pl)) return 0;
+  if (!make_plan(mats, count, M, verify, *d, pl)) return 0;
   return pl.bytes;
 }
 
-int launch_stream(const HostMatrix* mats, int count, int M, void* ws, size_t ws_bytes, cudaStream_t stream) {
+int launch_stream(const HostMatrix* mats, int count, int M, bool verify, void* ws, size_t ws_bytes,
+                  cudaStream_t stream) {
   const DeviceInfo* d = device_info();
   if (d == nullptr || !d->ok) return W4G128_ERR_DEVICE;
   Plan pl;
-  if (!make_plan(mats, count, M, *d, pl)) return W4G128_ERR_SHAPE;
+  if (!make_plan(mats, count, M, verify, *d, pl)) return W4G128_ERR_SHAPE;
   if (ws_bytes < pl.bytes) return W4G128_ERR_WORKSPACE;
   if (count == 1) return launch_with<1>(mats, count, M, pl, ws, stream);
   return launch_with<W4G128_MAX_MATRICES>(mats, count, M, pl, ws, stream);

@@ -37,6 +37,38 @@ def test_decode_step_equals_separate_calls(M):
         check_against_oracle(y, x, mat.codes, mat.scales, mat.mins)
 
 
+def verify_step(mats, xs, M):
+    ys = [torch.empty(M * m.N, dtype=torch.int16, device="cuda") for m in mats]
+    descs = [(m.packed, x, y, m.K, m.N) for m, x, y in zip(mats, xs, ys)]
+    nb = w.w4g128_decode_step_workspace_bytes(descs, M)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    w.w4g128_verify_step(descs, M, ws)
+    torch.cuda.synchronize()
+    assert w.w4g128_workspace_status(ws) == 0
+    return [to_host(y, np.uint16).reshape(M, m.N) for m, y in zip(mats, ys)]
+
+
+@pytest.mark.gpu
+def test_verify_step_rows_equal_single_row_verify():
+    """w4g128_verify_step: at M = 1 each output equals gemm_verify(M = 1) on
+    its matrix; at M = 8 row m equals the M = 1 step on row m; at M >= 2 it
+    equals w4g128_decode_step -- all bit for bit, and within the bound."""
+    shapes = [(128, 16), (640, 80), (4096, 4096), (1152, 208), (384, 48), (17408, 5120)]
+    mats = [DevMatrix(K, N, matrix_id=400 + i) for i, (K, N) in enumerate(shapes)]
+    x8 = [synth.x(SEED, 500 + i, 8, K) for i, (K, N) in enumerate(shapes)]
+    y8 = verify_step(mats, [to_dev(x) for x in x8], 8)
+    d8 = decode_step(mats, [to_dev(x) for x in x8], 8)
+    for a, b in zip(y8, d8):
+        assert np.array_equal(a, b)
+    for m in range(8):
+        y1 = verify_step(mats, [to_dev(x[m:m + 1]) for x in x8], 1)
+        for mat, x, a, b in zip(mats, x8, y1, y8):
+            assert np.array_equal(a[0], b[m]), m
+            if m == 0:
+                assert np.array_equal(a, run(mat, x[:1], verify=True))
+                check_against_oracle(a, x[:1], mat.codes, mat.scales, mat.mins)
+
+
 @pytest.mark.gpu
 def test_decode_step_single_matrix_equals_gemv():
     mat = DevMatrix(6144, 5120, matrix_id=77)

@@ -11,12 +11,12 @@ from gpu_helpers import SEED, DevMatrix, check_against_oracle, run  # noqa: E402
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("M", [2, 3, 4, 5, 7, 8])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8])
 @pytest.mark.parametrize("K,N", [(128, 16), (640, 80), (1152, 208), (4096, 4096)])
 def test_verify_matches_oracle(M, K, N):
     mat = DevMatrix(K, N, matrix_id=N + M)
     x = synth.x(SEED, 1000 + M, M, K)
-    check_against_oracle(run(mat, x), x, mat.codes, mat.scales, mat.mins)
+    check_against_oracle(run(mat, x, verify=True), x, mat.codes, mat.scales, mat.mins)
 
 
 @pytest.mark.gpu
@@ -55,15 +55,17 @@ def test_verify_identical_rows_give_identical_outputs():
 
 
 @pytest.mark.gpu
-def test_verify_rows_independent_of_m():
-    """Row m of an M-row verify does not depend on the other rows or on M (M >= 2)."""
-    K, N = 1152, 208
-    mat = DevMatrix(K, N, matrix_id=6)
-    x8 = synth.x(SEED, 6, 8, K)
-    y8 = run(mat, x8)
-    for M in (2, 5):
-        yM = run(mat, x8[:M])
-        assert np.array_equal(yM, y8[:M])
+@pytest.mark.parametrize("K,N", [(128, 16), (640, 80), (1152, 208), (5120, 6144), (17408, 5120)])
+def test_verify_rows_bitwise_equal_single_row_verify(K, N):
+    """Row m of an M-row verify equals a verify of row m alone (M = 1), bit for
+    bit, for every M in 1..8: the exact speculative-decoding property."""
+    mat = DevMatrix(K, N, matrix_id=6 + K)
+    x8 = synth.x(SEED, 6 + N, 8, K)
+    single = [run(mat, x8[m:m + 1], verify=True)[0] for m in range(8)]
+    for M in range(1, 9):
+        yM = run(mat, x8[:M], verify=True)
+        for m in range(M):
+            assert np.array_equal(yM[m], single[m]), (M, m)
 
 
 @pytest.mark.gpu
