@@ -59,6 +59,7 @@ def _load(mutant=0):
     lib.oracle_packed_bytes.argtypes = [i, i]
     lib.oracle_pack_tiled.argtypes = [p, p, p, i, i, p]
     lib.oracle_unpack_tiled.argtypes = [p, i, i, p, p, p]
+    lib.oracle_quantize.argtypes = [p, i, i, i, p, p, p, p]
     _libs[mutant] = lib
     return lib
 
@@ -66,6 +67,9 @@ def _load(mutant=0):
 def _c(a, dtype):
     a = np.ascontiguousarray(a, dtype=dtype)
     return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+QUANT_CANDIDATES = 21
 
 
 class Oracle:
@@ -164,3 +168,26 @@ def bf16_bits_to_f64(bits):
     """uint16 bf16 bit patterns -> float64 (exact)."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
     return b.view(np.float32).astype(np.float64)
+
+
+def _quantize(self, w, search):
+    """Quantise bf16 weights w[K][N] (bits) to the canonical format.
+
+    Returns (codes [K/8][N] uint32, scales [K/128][N] bf16 bits,
+    mins [K/128][N] bf16 bits, errs [K/128][N][21] float32), where errs holds
+    every candidate's squared error (only the first is filled when search is
+    False: round-to-nearest alone)."""
+    w, wp = _c(w, np.uint16)
+    K, N = w.shape
+    assert K % 128 == 0
+    codes = np.empty((K // 8, N), dtype=np.uint32)
+    scales = np.empty((K // 128, N), dtype=np.uint16)
+    mins = np.empty((K // 128, N), dtype=np.uint16)
+    errs = np.zeros((K // 128, N, QUANT_CANDIDATES), dtype=np.float32)
+    self.lib.oracle_quantize(wp, K, N, int(bool(search)), codes.ctypes.data_as(ctypes.c_void_p),
+                             scales.ctypes.data_as(ctypes.c_void_p), mins.ctypes.data_as(ctypes.c_void_p),
+                             errs.ctypes.data_as(ctypes.c_void_p))
+    return codes, scales, mins, errs
+
+
+Oracle.quantize = _quantize

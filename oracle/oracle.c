@@ -35,10 +35,17 @@
  * it is written from that specification and shares no code with the device
  * packer.
  *
+ * The quantizer (oracle_quantize, below) chooses codes, scales and minimums
+ * from bf16 weights: round-to-nearest on the 16-level grid of each group,
+ * optionally with a range search that clips outliers (its own header below).
+ *
  * Mutants for negative-control tests (compile with -DORACLE_MUTANT=n):
  *   1 = nibbles read in reversed order within a word,
  *   2 = group index off by one (k = 128g is assigned to group g-1),
- *   3 = the minimum term dropped.
+ *   3 = the minimum term dropped,
+ *   4 = quantizer rounds toward zero instead of to nearest,
+ *   5 = quantizer spreads the range over 16 steps instead of 15,
+ *   6 = quantizer keeps the candidate with the largest error.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -289,4 +296,126 @@ void oracle_unpack_tiled(const uint8_t* packed, int K, int N, uint32_t* codes,
                 mins[hi] = get_u16(e + 6);
             }
         }
+}
+
+/* ---- quantizer ------------------------------------------------------------
+ *
+ * From bf16 weights w[K][N] (row-major) to the canonical format: codes
+ * [K/8][N], scales and minimums [K/128][N].  Token Rush README, section
+ * "Quantization": group-wise asymmetric int4, 128 weights per bf16 scale and
+ * minimum; the round-to-nearest row of the quality table; and "an MSE range
+ * search per group that clips a few outliers to buy precision for the rest".
+ * The pages give no formulas.  Reading taken (the plainest one):
+ *
+ *   For one group (column n, rows 128g .. 128g+127), lo = min w, hi = max w.
+ *   A candidate p in (0, 1] spans [a, b] = [p*lo, p*hi] with 15 equal steps:
+ *       s = (b - a) / 15,  sb = bf16(s),  mb = bf16(a),
+ *       q_k = clamp(round_half_even((w_k - mb) / sb), 0, 15)   (q = 0 if sb == 0),
+ *       e = sum over k ascending of (w_k - (mb + q_k * sb))^2.
+ *   Round-to-nearest is the single candidate p = 1.  The range search tries
+ *   p = (100 - i) / 100 for i = 0 .. 20 and keeps the candidate with the
+ *   smallest e (the first one, i.e. the widest range, on ties).
+ *
+ * Every step is one IEEE fp32 operation rounded to nearest (no fused
+ * multiply-add): where the result is an integer decision (a code, the chosen
+ * candidate) both this oracle and the device kernel must take it in the same
+ * precision, and fp32 is the plainest precision for bf16 data.  bf16(.) is
+ * round-to-nearest-even of an fp32 value.
+ */
+#define QUANT_CANDIDATES 21
+
+static float f32_of_bf16(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+static float bf16_round_f32(float v) { return f32_of_bf16(oracle_bf16_rn((double)v)); }
+
+static int code_of(float w, float mb, float sb) {
+    if (sb == 0.0f) return 0;
+    volatile float d = w - mb;
+    volatile float t = d / sb;
+#if ORACLE_MUTANT == 4
+    float r = truncf(t);
+#else
+    float r = nearbyintf(t);       /* default rounding mode: ties to even */
+#endif
+    if (!(r > 0.0f)) return 0;     /* also maps -0 and NaN to 0 */
+    if (r > 15.0f) return 15;
+    return (int)r;
+}
+
+/* Quantise one group of 128 fp32 values with candidate p; returns the error
+ * and writes the codes and the bf16 scale / minimum. */
+static float quant_candidate(const float* w, float lo, float hi, float p, uint8_t* q,
+                             float* sb_out, float* mb_out) {
+    volatile float a = p * lo;
+    volatile float b = p * hi;
+    volatile float span = b - a;
+#if ORACLE_MUTANT == 5
+    volatile float s = span / 16.0f;
+#else
+    volatile float s = span / 15.0f;
+#endif
+    float sb = bf16_round_f32(s);
+    float mb = bf16_round_f32(a);
+    float e = 0.0f;
+    for (int k = 0; k < 128; k++) {
+        q[k] = (uint8_t)code_of(w[k], mb, sb);
+        volatile float prod = (float)q[k] * sb;
+        volatile float dq = mb + prod;
+        volatile float r = w[k] - dq;
+        volatile float r2 = r * r;
+        e = e + r2;
+    }
+    *sb_out = sb;
+    *mb_out = mb;
+    return e;
+}
+
+/* errs (optional): per group and candidate, the error e, [G][N][21]. */
+void oracle_quantize(const uint16_t* w, int K, int N, int search, uint32_t* codes,
+                     uint16_t* scales, uint16_t* mins, float* errs) {
+    int G = K / 128;
+    memset(codes, 0, sizeof(uint32_t) * (size_t)(K / 8) * N);
+    #pragma omp parallel for schedule(static)
+    for (long gn = 0; gn < (long)G * N; gn++) {
+        int g = (int)(gn / N), n = (int)(gn % N);
+        float v[128];
+        float lo = 0.0f, hi = 0.0f;
+        for (int k = 0; k < 128; k++) {
+            v[k] = f32_of_bf16(w[(size_t)(128 * g + k) * N + n]);
+            if (k == 0 || v[k] < lo) lo = v[k];
+            if (k == 0 || v[k] > hi) hi = v[k];
+        }
+        int ncand = search ? QUANT_CANDIDATES : 1;
+        uint8_t q[128], best_q[128];
+        float best_e = 0.0f, best_s = 0.0f, best_m = 0.0f;
+        for (int i = 0; i < ncand; i++) {
+            volatile float num = (float)(100 - i);
+            float p = num / 100.0f;
+            float sb, mb;
+            float e = quant_candidate(v, lo, hi, p, q, &sb, &mb);
+            if (errs) errs[(size_t)gn * QUANT_CANDIDATES + i] = e;
+#if ORACLE_MUTANT == 6
+            int better = (i == 0) || (e >= best_e);
+#else
+            int better = (i == 0) || (e < best_e);
+#endif
+            if (better) {
+                best_e = e;
+                best_s = sb;
+                best_m = mb;
+                memcpy(best_q, q, 128);
+            }
+        }
+        for (int k = 0; k < 128; k++) {
+            int kk = 128 * g + k;
+            codes[(size_t)(kk / 8) * N + n] |= (uint32_t)best_q[k] << (4 * (kk % 8));
+        }
+        scales[(size_t)g * N + n] = oracle_bf16_rn((double)best_s);
+        mins[(size_t)g * N + n] = oracle_bf16_rn((double)best_m);
+    }
 }
