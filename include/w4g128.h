@@ -125,6 +125,23 @@ W4G128_API int w4g128_pack(const uint32_t* codes, const w4g128_bf16* scales, con
 W4G128_API int w4g128_unpack(const void* packed, int K, int N, uint32_t* codes, w4g128_bf16* scales,
                              w4g128_bf16* mins, void* stream);
 
+/* bf16 weights w[K][N] (row-major, device) -> the canonical format that
+ * w4g128_pack takes: codes [K/8][N], scales and mins [K/128][N] (device,
+ * caller-owned).  Token Rush README, "Quantization": 128 weights per bf16
+ * scale and minimum; round-to-nearest (search = 0), or round-to-nearest with
+ * the per-group range search that clips outliers (search = 1).  Per group of
+ * 128 rows of one column, with lo / hi its smallest / largest weight, a
+ * candidate p spans [p lo, p hi] in 15 steps: scale = bf16((p hi - p lo) /
+ * 15), min = bf16(p lo), q = clamp(round_half_even((w - min) / scale), 0, 15)
+ * (0 when scale = 0); search = 1 tries p = 1.00, 0.99, ..., 0.80 and keeps
+ * the smallest sum of (w - (min + q scale))^2 over the group (the widest on
+ * ties).  Every step is one fp32 operation rounded to nearest (no fused
+ * multiply-add), so the result is bit-exact and deterministic.  Weights must
+ * be finite with |w| < 2^126.  A one-time preprocessing call, not part of the
+ * weight stream. */
+W4G128_API int w4g128_quantize(const w4g128_bf16* w, int K, int N, int search, uint32_t* codes,
+                               w4g128_bf16* scales, w4g128_bf16* mins, void* stream);
+
 /* Workspace bytes needed by w4g128_gemm_verify(M, K, N) on the current
  * device (and by w4g128_gemv, M = 1).  Returns 0 for invalid arguments. */
 W4G128_API size_t w4g128_workspace_bytes(int M, int K, int N);

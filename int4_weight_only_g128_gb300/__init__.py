@@ -12,7 +12,7 @@ import os
 
 __all__ = [
     "W4G128Error", "lib", "exported_symbols",
-    "w4g128_status_string", "w4g128_packed_bytes", "w4g128_pack", "w4g128_unpack",
+    "w4g128_status_string", "w4g128_packed_bytes", "w4g128_pack", "w4g128_unpack", "w4g128_quantize",
     "w4g128_workspace_bytes", "w4g128_gemv", "w4g128_gemm_verify",
     "w4g128_decode_step_workspace_bytes", "w4g128_decode_step", "w4g128_verify_step", "w4g128_workspace_status",
     "w4g128_probe_read", "w4g128_probe_copy", "w4g128_probe_sink_bytes", "w4g128_gemv_noalloc",
@@ -71,6 +71,8 @@ def lib():
     L.w4g128_pack.argtypes = [p, p, p, i, i, p, p]
     L.w4g128_unpack.restype = i
     L.w4g128_unpack.argtypes = [p, i, i, p, p, p, p]
+    L.w4g128_quantize.restype = i
+    L.w4g128_quantize.argtypes = [p, i, i, i, p, p, p, p]
     L.w4g128_workspace_bytes.restype = sz
     L.w4g128_workspace_bytes.argtypes = [i, i, i]
     L.w4g128_gemv.restype = i
@@ -139,6 +141,12 @@ def w4g128_pack(codes, scales, mins, K, N, packed, stream=None):
 def w4g128_unpack(packed, K, N, codes, scales, mins, stream=None):
     _check("w4g128_unpack", lib().w4g128_unpack(_ptr(packed), K, N, _ptr(codes), _ptr(scales), _ptr(mins),
                                                 _stream(stream)))
+
+
+def w4g128_quantize(w, K, N, search, codes, scales, mins, stream=None):
+    """bf16 weights [K][N] -> canonical codes, scales, mins (search: 0 RTN, 1 range search)."""
+    _check("w4g128_quantize", lib().w4g128_quantize(_ptr(w), K, N, int(search), _ptr(codes), _ptr(scales),
+                                                    _ptr(mins), _stream(stream)))
 
 
 def w4g128_workspace_bytes(M, K, N):

@@ -105,6 +105,16 @@ int w4g128_unpack(const void* packed, int K, int N, uint32_t* codes, w4g128_bf16
   return w4g128::launch_unpack(packed, K, N, codes, scales, mins, as_stream(stream));
 }
 
+int w4g128_quantize(const w4g128_bf16* w, int K, int N, int search, uint32_t* codes, w4g128_bf16* scales,
+                    w4g128_bf16* mins, void* stream) {
+  if (w == nullptr || codes == nullptr || scales == nullptr || mins == nullptr) return W4G128_ERR_INVALID_ARG;
+  if (search != 0 && search != 1) return W4G128_ERR_INVALID_ARG;
+  if (!shape_ok(K, N)) return W4G128_ERR_SHAPE;
+  if (!aligned(w, 4) || !aligned(codes, 4) || !aligned(scales, 4) || !aligned(mins, 4)) return W4G128_ERR_ALIGN;
+  if (!w4g128::device_is_sm103()) return W4G128_ERR_DEVICE;
+  return w4g128::launch_quantize(w, K, N, search, codes, scales, mins, as_stream(stream));
+}
+
 size_t w4g128_workspace_bytes(int M, int K, int N) {
   const w4g128_matrix m{nullptr, nullptr, nullptr, K, N};
   return stream_bytes(&m, 1, M);

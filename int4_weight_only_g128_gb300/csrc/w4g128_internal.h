@@ -31,6 +31,9 @@ int launch_pack(const uint32_t* codes, const uint16_t* scales, const uint16_t* m
 int launch_unpack(const void* packed, int K, int N, uint32_t* codes, uint16_t* scales, uint16_t* mins,
                   cudaStream_t stream);
 
+int launch_quantize(const uint16_t* w, int K, int N, int search, uint32_t* codes, uint16_t* scales,
+                    uint16_t* mins, cudaStream_t stream);
+
 // One matrix of a streaming call, as the host hands it over.
 struct HostMatrix {
   const void* packed;

@@ -17,7 +17,7 @@ def L():
 
 def test_every_header_symbol_is_exported(L):
     names = w.exported_symbols()
-    assert len(names) == 15
+    assert len(names) == 16
     for n in names:
         assert hasattr(L, n), n
 
