@@ -726,53 +726,93 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Strea
 // ----------------------------------------------------------------- reduce kernel
 
 // M >= 2: folds the segment partials of every quad the schedule split between
-// warps.  One thread per 4 adjacent outputs of one row (16-byte loads), its S
-// partials loaded kRedBatch segments at a time and summed per output in
-// segment order exactly as a single warp would have.  Quads owned by one warp
-// were written by the streaming kernel and are skipped.
-constexpr int kRedBatch = 8;
-constexpr int kRedBlocksPerSM = 4;
+// warps.  One CTA per quad: the quad's S partial slots are one contiguous run
+// of S x M x 64 fp32, pulled into shared memory by 1-D bulk copies of up to
+// kRedChunk segments (two stages), and each thread folds one (row, 4
+// adjacent columns) unit over the segments in order -- the left fold a single
+// warp would have made.  Quads owned by one warp were written by the streaming
+// kernel; their CTAs exit before waiting for it.
+constexpr int kMaxRows = W4G128_MAX_M;
+constexpr int kRedChunk = 16;                              // segments per bulk copy
+constexpr int kRedThreads = kMaxRows * 16;                 // one per (row, 4 columns)
+constexpr int kRedStageBytes = kRedChunk * kMaxRows * 64 * 4;  // 32 KB at M = 8
+constexpr int kRedSmem = 2 * kRedStageBytes + 16;          // two stages + two mbarriers
+
 template <int MAXMAT>
-__global__ void __launch_bounds__(256, kRedBlocksPerSM) reduce_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
-  grid_dependency_wait();  // every partial of the streaming kernel is written and visible
-  const int units_per_quad = p.M * 16;  // (row, 4-column group) units
-  const int per_quad = p.M * 64;        // floats per partial slot
+__global__ void __launch_bounds__(kRedThreads) reduce_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
+  extern __shared__ __align__(128) uint8_t rsm[];
+  __shared__ int ok;
+  const int gq = blockIdx.x;
+  int lo = 0, hi = p.count - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.mats[mid].quad_begin <= gq) lo = mid; else hi = mid - 1;
+  }
+  const MatParams& m = p.mats[lo];
+  const int q = gq - m.quad_begin;
+  const int G = m.K / kGroup, S = div_up(G, seg_groups<kMMA>()), T = m.N / kTileN;
   const long long I = p.total_items;
-  const int total = p.total_quads * units_per_quad;
-  for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < total; u += gridDim.x * blockDim.x) {
-    const int gq = u / units_per_quad;
-    const int rem = u - gq * units_per_quad;
-    const int row = rem >> 4, col = 4 * (rem & 15);
-    int lo = 0, hi = p.count - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.mats[mid].quad_begin <= gq) lo = mid; else hi = mid - 1;
+  const long long q_first = m.item_begin + static_cast<long long>(q) * S;
+  if (owner_of(q_first, I, p.W) == owner_of(q_first + S - 1, I, p.W)) return;  // owned: y is written
+
+  grid_dependency_wait();  // every partial of the streaming kernel is written and visible
+  const int per_quad = p.M * 64;  // floats per partial slot
+  const uint32_t slot_bytes = static_cast<uint32_t>(per_quad) * 4u;
+  const int stage_floats = kRedChunk * per_quad;
+  const float* buf = reinterpret_cast<const float*>(rsm);
+  const uint32_t buf0 = smem_addr(rsm), bar0 = smem_addr(rsm + 2 * kRedStageBytes);
+  const float* src = p.partials + q_first * per_quad;
+  const int nchunks = div_up(S, kRedChunk);
+  uint64_t pol = 0;
+  auto issue = [&](int ch) {
+    const int ns = min(kRedChunk, S - ch * kRedChunk);
+    const uint32_t bar = bar0 + 8 * (ch & 1);
+    mbar_arrive_expect_tx(bar, ns * slot_bytes);
+    bulk_g2s(buf0 + (ch & 1) * stage_floats * 4, src + static_cast<long long>(ch) * stage_floats, ns * slot_bytes,
+             bar, pol);
+  };
+  if (threadIdx.x == 0) {
+    mbar_init(bar0, 1);
+    mbar_init(bar0 + 8, 1);
+    fence_mbar_init();
+    pol = l2_policy_evict_first();  // partials are read once
+    issue(0);
+    if (nchunks > 1) issue(1);
+  }
+  const int u = threadIdx.x, row = u >> 4, col = 4 * (u & 15);
+  const bool active = row < p.M && col < kTileN * min(kQuadTiles, T - kQuadTiles * q);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int ch = 0; ch < nchunks; ++ch) {
+    if (threadIdx.x == 0) {
+      const bool got = mbar_wait_bounded(bar0 + 8 * (ch & 1), (ch >> 1) & 1);
+      if (!got) {
+        // record the timeout and wait (bounded) for the other stage's copy
+        atomicCAS(p.status, 0u, static_cast<unsigned>(W4G128_ERR_TIMEOUT));
+        if (ch + 1 < nchunks) (void)mbar_wait_bounded(bar0 + 8 * ((ch + 1) & 1), ((ch + 1) >> 1) & 1);
+      }
+      ok = got;
     }
-    const MatParams& m = p.mats[lo];
-    const int q = gq - m.quad_begin;
-    const int G = m.K / kGroup, S = div_up(G, seg_groups<kMMA>()), T = m.N / kTileN;
-    if (col >= kTileN * min(kQuadTiles, T - kQuadTiles * q)) continue;  // ragged last quad
-    const long long q_first = m.item_begin + static_cast<long long>(q) * S;
-    if (owner_of(q_first, I, p.W) == owner_of(q_first + S - 1, I, p.W)) continue;  // owned quad
-    const float4* part = reinterpret_cast<const float4*>(p.partials + q_first * per_quad + row * 64 + col);
-    const int stride = per_quad / 4;  // float4s between consecutive segments
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < S; s0 += kRedBatch) {  // a batch of segments in flight, then fold in order
-      float4 v[kRedBatch];
-#pragma unroll
-      for (int k = 0; k < kRedBatch; ++k)
-        v[k] = (s0 + k < S) ? __ldcg(part + static_cast<long long>(s0 + k) * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int k = 0; k < kRedBatch; ++k) {
-        if (s0 + k < S) {
-          if (s0 + k == 0) {
-            acc = v[k];
-          } else {
-            acc.x += v[k].x; acc.y += v[k].y; acc.z += v[k].z; acc.w += v[k].w;
-          }
+    __syncthreads();
+    if (!ok) return;
+    if (active) {
+      const float* b = buf + (ch & 1) * stage_floats + row * 64 + col;
+      const int ns = min(kRedChunk, S - ch * kRedChunk);
+      for (int s = 0; s < ns; ++s) {
+        const float4 v = *reinterpret_cast<const float4*>(b + s * per_quad);
+        if (ch == 0 && s == 0) {
+          acc = v;
+        } else {
+          acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
         }
       }
     }
+    __syncthreads();  // the stage is consumed before it is refilled
+    if (threadIdx.x == 0 && ch + 2 < nchunks) {
+      fence_proxy_async_smem();
+      issue(ch + 2);
+    }
+  }
+  if (active) {
     uint32_t* yo = reinterpret_cast<uint32_t*>(m.y + static_cast<long long>(row) * m.N + kQuadTiles * kTileN * q + col);
     yo[0] = static_cast<uint32_t>(to_bf16(acc.x)) | (static_cast<uint32_t>(to_bf16(acc.y)) << 16);
     yo[1] = static_cast<uint32_t>(to_bf16(acc.z)) | (static_cast<uint32_t>(to_bf16(acc.w)) << 16);
@@ -797,6 +837,8 @@ void setup_mode(DeviceInfo& d) {
   cudaFuncSetAttribute(stream_kernel<MODE, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   cudaFuncSetAttribute(stream_kernel<MODE, W4G128_MAX_MATRICES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        smem);
+  cudaFuncSetAttribute(reduce_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRedSmem);
+  cudaFuncSetAttribute(reduce_kernel<W4G128_MAX_MATRICES>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRedSmem);
   int occ1 = 0, occ2 = 0;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ1, stream_kernel<MODE, 1>, kNW * 32, smem);
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, stream_kernel<MODE, W4G128_MAX_MATRICES>, kNW * 32, smem);
@@ -927,12 +969,9 @@ int launch_mode(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, cudaStr
   }
 
   if (MODE != kMMA) return W4G128_OK;  // M = 1 folds split quads inside the streaming kernel
-  // one thread per (quad, row, 4 columns), at most one resident wave
-  const long long units = static_cast<long long>(sp.total_quads) * sp.M * 16;
-  const long long wave = static_cast<long long>(device_info()->sms) * kRedBlocksPerSM;
-  cfg.gridDim = dim3(static_cast<unsigned>(std::max(1LL, std::min((units + 255) / 256, wave))));
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
+  cfg.gridDim = dim3(static_cast<unsigned>(sp.total_quads));  // one CTA per quad
+  cfg.blockDim = dim3(kRedThreads);
+  cfg.dynamicSmemBytes = kRedSmem;
   if (cudaLaunchKernelEx(&cfg, reduce_kernel<MAXMAT>, sp) != cudaSuccess) {
     cudaGetLastError();
     return W4G128_ERR_CUDA;
