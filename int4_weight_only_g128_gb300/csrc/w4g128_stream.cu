@@ -521,6 +521,10 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
       const long long q_first = m.item_begin + static_cast<long long>(cc.q) * S;
       const long long q_last = q_first + S - 1;
       const bool owned = (q_first >= it_a) && (q_last < it_b);
+      // A run holding the quad's first segments but not all of them (the
+      // quad continues in later warps) keeps their left fold too and stores it
+      // as one partial: the fold over segments then starts from it.
+      const bool prefix = (q_first >= it_a) && !owned;
       if constexpr (MODE == kM1) {
         // reduce the 4 lane classes c of each column (same tree on every lane)
 #pragma unroll
@@ -534,30 +538,33 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
           }
       }
       const int rows = (MODE == kM1) ? 1 : p.M;
-      if (owned) {
+      if (owned || prefix) {
 #pragma unroll
         for (int t = 0; t < kQuadTiles; ++t)
 #pragma unroll
           for (int e = 0; e < NA; ++e) tot[t][e] = (cc.s == 0) ? seg[t][e] : tot[t][e] + seg[t][e];
-      } else {
-        float* part = p.partials + cc.item * rows * 64;  // one slot per (matrix, quad, segment)
+      }
+      if (!owned && (!prefix || cc.item + 1 == it_b)) {
+        // one slot per (matrix, quad, segment): the segment sum, or at the last
+        // segment of a prefix run the fold of segments 0 .. s
+        float* part = p.partials + cc.item * rows * 64;
         if constexpr (MODE == kM1) {
           // lane (r, c) stores tile c's columns r and r + 8
           if (c < ntiles) {
-            part[16 * c + r] = pick(seg, c, 0);
-            part[16 * c + r + 8] = pick(seg, c, 1);
+            part[16 * c + r] = prefix ? pick(tot, c, 0) : pick(seg, c, 0);
+            part[16 * c + r + 8] = prefix ? pick(tot, c, 1) : pick(seg, c, 1);
           }
         } else {
 #pragma unroll
           for (int t = 0; t < kQuadTiles; ++t) {
             if (t < ntiles) {
               if (2 * c < rows) {
-                part[(2 * c) * 64 + 16 * t + r] = seg[t][0];
-                part[(2 * c) * 64 + 16 * t + r + 8] = seg[t][2];
+                part[(2 * c) * 64 + 16 * t + r] = prefix ? tot[t][0] : seg[t][0];
+                part[(2 * c) * 64 + 16 * t + r + 8] = prefix ? tot[t][2] : seg[t][2];
               }
               if (2 * c + 1 < rows) {
-                part[(2 * c + 1) * 64 + 16 * t + r] = seg[t][1];
-                part[(2 * c + 1) * 64 + 16 * t + r + 8] = seg[t][3];
+                part[(2 * c + 1) * 64 + 16 * t + r] = prefix ? tot[t][1] : seg[t][1];
+                part[(2 * c + 1) * 64 + 16 * t + r + 8] = prefix ? tot[t][3] : seg[t][3];
               }
             }
           }
@@ -607,21 +614,24 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
           prev = __shfl_sync(0xffffffffu, prev, 0);
           if (prev + 1 == expected) {
             __threadfence();
-            const float* part = p.partials + q_first * 64;
+            // slots from the prefix run's last segment (its fold) to the quad's end
+            const long long first = I * (wf + 1) / p.W - 1;
+            const int nslot = static_cast<int>(q_last - first + 1);
+            const float* part = p.partials + first * 64;
             const int ncols = ntiles * kTileN;
             const bool c0 = lane < ncols, c1 = lane + 32 < ncols;
             float a0 = 0.f, a1 = 0.f;
-            for (int s0 = 0; s0 < S; s0 += 8) {  // both columns' loads of 8 segments in flight
+            for (int s0 = 0; s0 < nslot; s0 += 8) {  // both columns' loads of 8 slots in flight
               float v0[8], v1[8];
 #pragma unroll
               for (int u = 0; u < 8; ++u) {
-                const bool ok = s0 + u < S;
+                const bool ok = s0 + u < nslot;
                 v0[u] = (ok && c0) ? __ldcg(part + static_cast<long long>(s0 + u) * 64 + lane) : 0.f;
                 v1[u] = (ok && c1) ? __ldcg(part + static_cast<long long>(s0 + u) * 64 + lane + 32) : 0.f;
               }
 #pragma unroll
               for (int u = 0; u < 8; ++u) {
-                if (s0 + u < S) {
+                if (s0 + u < nslot) {
                   a0 = (s0 + u == 0) ? v0[u] : a0 + v0[u];
                   a1 = (s0 + u == 0) ? v1[u] : a1 + v1[u];
                 }
@@ -726,16 +736,17 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Strea
 // ----------------------------------------------------------------- reduce kernel
 
 // M >= 2: folds the segment partials of every quad the schedule split between
-// warps.  One CTA per quad: the quad's S partial slots are one contiguous run
-// of S x M x 64 fp32, pulled into shared memory by 1-D bulk copies of up to
-// kRedChunk segments (two stages), and each thread folds one (row, 4
-// adjacent columns) unit over the segments in order -- the left fold a single
+// warps.  One CTA per quad: the quad's partial slots -- the fold of the
+// segments its first warp held, then one slot per later segment -- are one
+// contiguous run of M x 64 fp32 slots, pulled into shared memory by 1-D bulk
+// copies of up to kRedChunk slots (two stages), and each thread folds one
+// (row, 4 adjacent columns) unit over them in order -- the left fold a single
 // warp would have made.  Quads owned by one warp were written by the streaming
 // kernel; their CTAs exit before waiting for it.
 constexpr int kMaxRows = W4G128_MAX_M;
-constexpr int kRedChunk = 16;                              // segments per bulk copy
+constexpr int kRedChunk = 8;                               // segments per bulk copy
 constexpr int kRedThreads = kMaxRows * 16;                 // one per (row, 4 columns)
-constexpr int kRedStageBytes = kRedChunk * kMaxRows * 64 * 4;  // 32 KB at M = 8
+constexpr int kRedStageBytes = kRedChunk * kMaxRows * 64 * 4;  // 16 KB at M = 8
 constexpr int kRedSmem = 2 * kRedStageBytes + 16;          // two stages + two mbarriers
 
 template <int MAXMAT>
@@ -753,7 +764,12 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(const __grid_consta
   const int G = m.K / kGroup, S = div_up(G, seg_groups<kMMA>()), T = m.N / kTileN;
   const long long I = p.total_items;
   const long long q_first = m.item_begin + static_cast<long long>(q) * S;
-  if (owner_of(q_first, I, p.W) == owner_of(q_first + S - 1, I, p.W)) return;  // owned: y is written
+  const int wf = owner_of(q_first, I, p.W);
+  if (wf == owner_of(q_first + S - 1, I, p.W)) return;  // owned: y is written
+  // Slots from the prefix run's last segment (which holds the fold of the
+  // segments before it) to the quad's last segment.
+  const long long first = I * (wf + 1) / p.W - 1;
+  const int nslot = static_cast<int>(q_first + S - first);
 
   grid_dependency_wait();  // every partial of the streaming kernel is written and visible
   const int per_quad = p.M * 64;  // floats per partial slot
@@ -761,11 +777,11 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(const __grid_consta
   const int stage_floats = kRedChunk * per_quad;
   const float* buf = reinterpret_cast<const float*>(rsm);
   const uint32_t buf0 = smem_addr(rsm), bar0 = smem_addr(rsm + 2 * kRedStageBytes);
-  const float* src = p.partials + q_first * per_quad;
-  const int nchunks = div_up(S, kRedChunk);
+  const float* src = p.partials + first * per_quad;
+  const int nchunks = div_up(nslot, kRedChunk);
   uint64_t pol = 0;
   auto issue = [&](int ch) {
-    const int ns = min(kRedChunk, S - ch * kRedChunk);
+    const int ns = min(kRedChunk, nslot - ch * kRedChunk);
     const uint32_t bar = bar0 + 8 * (ch & 1);
     mbar_arrive_expect_tx(bar, ns * slot_bytes);
     bulk_g2s(buf0 + (ch & 1) * stage_floats * 4, src + static_cast<long long>(ch) * stage_floats, ns * slot_bytes,
@@ -796,7 +812,7 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(const __grid_consta
     if (!ok) return;
     if (active) {
       const float* b = buf + (ch & 1) * stage_floats + row * 64 + col;
-      const int ns = min(kRedChunk, S - ch * kRedChunk);
+      const int ns = min(kRedChunk, nslot - ch * kRedChunk);
       for (int s = 0; s < ns; ++s) {
         const float4 v = *reinterpret_cast<const float4*>(b + s * per_quad);
         if (ch == 0 && s == 0) {
