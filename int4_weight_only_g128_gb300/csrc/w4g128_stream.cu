@@ -103,13 +103,22 @@ __host__ __device__ constexpr int seg_groups() { return MODE == kM1 ? W4G128_SEG
 
 template <int MODE>
 __host__ __device__ constexpr int slot_bytes() { return kQuadTiles * kBlockBytes + Pkg<MODE>::kBytes; }
-constexpr int kBarBytes = ((kNW * kDepth * 8 + 127) / 128) * 128;  // kNW * kDepth mbarriers
+#ifndef W4G128_M1_RING_DEPTH
+#define W4G128_M1_RING_DEPTH 2
+#endif
+// Ring slots per warp: kDepth, or for the small-package M = 1 modes
+// W4G128_M1_RING_DEPTH (three 4688-byte slots per warp still fit 16 warps).
 template <int MODE>
-__host__ __device__ constexpr int smem_bytes() { return kBarBytes + kNW * kDepth * slot_bytes<MODE>(); }
+__host__ __device__ constexpr int ring_depth() { return MODE == kMMA ? kDepth : W4G128_M1_RING_DEPTH; }
+constexpr int kMaxDepth = kDepth > W4G128_M1_RING_DEPTH ? kDepth : W4G128_M1_RING_DEPTH;
+constexpr int kBarBytes = ((kNW * kMaxDepth * 8 + 127) / 128) * 128;  // per warp, its ring's mbarriers
+template <int MODE>
+__host__ __device__ constexpr int smem_bytes() { return kBarBytes + kNW * ring_depth<MODE>() * slot_bytes<MODE>(); }
 
 static_assert(slot_bytes<kM1>() % 16 == 0 && slot_bytes<kMMA>() % 16 == 0, "bulk copies need 16-byte slots");
 static_assert(Pkg<kM1>::kBytes % 16 == 0 && Pkg<kMMA>::kBytes % 16 == 0, "bulk copies need 16-byte packages");
-static_assert((kDepth & (kDepth - 1)) == 0, "ring depth must be a power of two");
+static_assert(smem_bytes<kM1>() <= 232448 && smem_bytes<kMMA>() <= 232448 && smem_bytes<kMMA1>() <= 232448,
+              "a CTA's rings must fit the 227 KB of shared memory");
 
 // ----------------------------------------------------------------- parameters
 
@@ -420,6 +429,7 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int NA = Acc<MODE>::kN;
   constexpr int kSlot = slot_bytes<MODE>();
+  constexpr int kDepth = ring_depth<MODE>();  // shadows the default depth
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane >> 2, c = lane & 3;
   const int wg = blockIdx.x * (blockDim.x >> 5) + warp;  // CTAs hold up to kNW warps
