@@ -86,6 +86,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(dist, value, device):
+    """The largest value over all ranks (the slowest rank's time); dist None
+    means a single process."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbps(world, steps, bytes_per_step, seconds):
+    """Whole-job throughput: each of `world` ranks streamed `steps` steps of its
+    own copy of the workload in at most `seconds`."""
+    return world * steps * bytes_per_step / seconds / 1e9
+
+
 def dist_init(backend):
     import torch.distributed as dist
     ws, _, _ = dist_env()
@@ -333,13 +350,6 @@ def run_ours(args):
         if dist is not None:
             dist.barrier()
 
-    def max_over_ranks(v):
-        if dist is None:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     def capture(calls):
         """CUDA graph of the given launch callables (each takes the capture stream)."""
         g = torch.cuda.CUDAGraph()
@@ -368,7 +378,7 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        return max_over_ranks(e0.elapsed_time(e1) * 1e-3)
+        return max_over_ranks(dist, e0.elapsed_time(e1) * 1e-3, "cuda")
 
     # ---- clocks sampled over a soak of identical steps that ends with the timed region
     clocks = ClockSampler(local)
@@ -389,8 +399,8 @@ def run_ours(args):
     launch1, launch8 = total1 / args.steps, total8 / args.steps
 
     bytes1, bytes8 = algorithmic_bytes(1), algorithmic_bytes(8)
-    value = world * args.steps * bytes1 / total1 / 1e9
-    value8 = world * args.steps * bytes8 / total8 / 1e9
+    value = aggregate_gbps(world, args.steps, bytes1, total1)
+    value8 = aggregate_gbps(world, args.steps, bytes8, total8)
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
     by_m = {}
@@ -541,8 +551,8 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    e2e_s = max_over_ranks(e0.elapsed_time(e1) * 1e-3)
-    e2e_value = world * args.steps * bytes1 / e2e_s / 1e9
+    e2e_s = max_over_ranks(dist, e0.elapsed_time(e1) * 1e-3, "cuda")
+    e2e_value = aggregate_gbps(world, args.steps, bytes1, e2e_s)
 
     if rank != 0:
         return 0
