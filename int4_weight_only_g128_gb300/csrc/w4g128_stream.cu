@@ -12,16 +12,19 @@
 //    blocks of 1088 bytes, plus that group's activation package) through a
 //    private ring of shared-memory slots filled by 1-D TMA bulk copies
 //    (cp.async.bulk) and completed on per-slot mbarriers.  Within a matrix a
-//    warp's range is one sequential byte stream.  No block-wide barrier exists
-//    after launch, so warps never wait on each other.
+//    warp's range is one sequential byte stream.  Warps never wait on each
+//    other while streaming (at M = 1 a CTA's warps meet once, at its end).
 //  * A quad owned wholly by one warp is written straight to y.  For a quad
-//    split between warps every segment sum goes to its own fp32 partial
-//    slot, and the partials are folded in segment order:
-//      - M = 1: by whichever warp of the quad arrives last (an atomic ticket;
-//        nobody waits) -- 64 outputs, cheap enough to overlap the stream;
-//      - M >= 2: by a small reduce kernel launched right behind the streaming
-//        kernel (programmatic dependent launch), one thread per output with
-//        its loads in flight, since 64*M outputs would stall one warp.
+//    split between warps every segment sum goes to its own fp32 partial slot
+//    (the warp holding the quad's first segments stores their left fold as
+//    one slot), and the slots are folded in segment order:
+//      - M = 1: each warp takes the tickets of its (at most two) split quads
+//        after its stream; the CTA holding a quad's last ticket folds it with
+//        all its threads once its warps are done -- no warp stalls mid-stream;
+//      - M >= 2: by a reduce kernel launched right behind the streaming
+//        kernel (programmatic dependent launch), one CTA per split quad
+//        pulling its slots into shared memory with bulk copies, since 64*M
+//        outputs per quad would tie up the SMs that finish last.
 //  * A small prep kernel (launched first; the streaming kernel overlaps it by
 //    programmatic dependent launch) turns x into per-group packages in the
 //    order the lanes consume them, with the group sums the factorised
@@ -433,10 +436,25 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane >> 2, c = lane & 3;
   const int wg = blockIdx.x * (blockDim.x >> 5) + warp;  // CTAs hold up to kNW warps
-  if (wg >= p.W) return;  // whole warp; there are no block-wide barriers
+  // M = 1: split quads whose last ticket a warp of this CTA took; folded by
+  // the whole CTA after its stream (the only block-wide barriers are here and
+  // before that fold).
+  __shared__ int fold_n;
+  __shared__ int fold_q[2 * kNW];
+  if constexpr (MODE != kMMA) {
+    if (threadIdx.x == 0) fold_n = 0;
+    __syncthreads();
+  }
 
   const long long I = p.total_items;
   const long long it_a = I * wg / p.W, it_b = I * (wg + 1) / p.W;
+  // A warp's contiguous range holds at most two split quads (its first and its
+  // last); their tickets are taken after the stream, so no ticket stalls it.
+  int pend_q0 = 0, pend_q1 = 0;  // global quad indices
+  unsigned pend_e0 = 0u, pend_e1 = 0u;  // warps contributing to each
+  int n_pend = 0;
+  bool failed = false;
+  if (wg < p.W) {
 
   const uint32_t bar0 = smem_addr(smem) + warp * kDepth * 8;
   const uint32_t ring0 = smem_addr(smem) + kBarBytes + warp * kDepth * kSlot;
@@ -512,7 +530,8 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
           (void)mbar_wait_bounded(bar0 + 8 * static_cast<int>(k % kDepth), (k / kDepth) & 1u);
       }
       __syncwarp();
-      return;
+      failed = true;
+      break;
     }
     const int ntiles = cc.ntiles;
     // M = 1: a straight-line body for full quads lets the compiler interleave
@@ -622,51 +641,79 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
               }
             }
           }
-        } else if constexpr (MODE != kMMA) {
-          // Split quad at M = 1 (both M = 1 modes leave the quad's 64 columns
-          // in order in a partial slot): publish, take a ticket; the last arriver folds
-          // the segment partials in segment order and writes y.
-          __threadfence();
-          __syncwarp();
-          const int wf = owner_of(q_first, I, p.W), wl = owner_of(q_last, I, p.W);
-          const unsigned expected = static_cast<unsigned>(wl - wf + 1);
-          unsigned* ticket = p.tickets + m.quad_begin + cc.q;
-          unsigned prev = 0;
-          if (lane == 0) prev = atomicAdd(ticket, 1u);
-          prev = __shfl_sync(0xffffffffu, prev, 0);
-          if (prev + 1 == expected) {
-            __threadfence();
-            // slots from the prefix run's last segment (its fold) to the quad's end
-            const long long first = I * (wf + 1) / p.W - 1;
-            const int nslot = static_cast<int>(q_last - first + 1);
-            const float* part = p.partials + first * 64;
-            const int ncols = ntiles * kTileN;
-            const bool c0 = lane < ncols, c1 = lane + 32 < ncols;
-            float a0 = 0.f, a1 = 0.f;
-            for (int s0 = 0; s0 < nslot; s0 += 8) {  // both columns' loads of 8 slots in flight
-              float v0[8], v1[8];
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                const bool ok = s0 + u < nslot;
-                v0[u] = (ok && c0) ? __ldcg(part + static_cast<long long>(s0 + u) * 64 + lane) : 0.f;
-                v1[u] = (ok && c1) ? __ldcg(part + static_cast<long long>(s0 + u) * 64 + lane + 32) : 0.f;
-              }
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                if (s0 + u < nslot) {
-                  a0 = (s0 + u == 0) ? v0[u] : a0 + v0[u];
-                  a1 = (s0 + u == 0) ? v1[u] : a1 + v1[u];
-                }
-              }
-            }
-            if (c0) m.y[n0 + lane] = to_bf16(a0);
-            if (c1) m.y[n0 + lane + 32] = to_bf16(a1);
-            if (lane == 0) *ticket = 0u;  // ready for the next call
+        } else if (MODE != kMMA && n_pend < 2) {
+          // Split quad at M = 1: its partials are written; the ticket comes after
+          // the stream.  (M >= 2: the reduce kernel folds every split quad.)
+          const int gq = m.quad_begin + cc.q;
+          const unsigned e = static_cast<unsigned>(owner_of(q_last, I, p.W) - owner_of(q_first, I, p.W) + 1);
+          if (n_pend == 0) {
+            pend_q0 = gq;
+            pend_e0 = e;
+          } else {
+            pend_q1 = gq;
+            pend_e1 = e;
           }
+          ++n_pend;
         }
       }
     }
     cursor_next<MODE>(cc, p);
+  }
+  if (!failed && n_pend > 0) {
+    __threadfence();  // this warp's partials are visible before its tickets
+    __syncwarp();
+    if (lane == 0) {
+      // the warp holding a quad's last ticket hands the quad to its CTA's fold
+      if (atomicAdd(p.tickets + pend_q0, 1u) + 1 == pend_e0) fold_q[atomicAdd(&fold_n, 1)] = pend_q0;
+      if (n_pend > 1 && atomicAdd(p.tickets + pend_q1, 1u) + 1 == pend_e1) fold_q[atomicAdd(&fold_n, 1)] = pend_q1;
+    }
+    __syncwarp();
+  }
+  }  // warp in range
+  if constexpr (MODE == kMMA) return;  // M >= 2: the reduce kernel folds
+  __syncthreads();
+  __threadfence();  // the other contributors' partials, published before their tickets
+
+  // ---- fold the completed split quads: one thread per (quad, 4 columns), the
+  // quad's slots from its first warp's prefix fold on, in segment order.
+  const int rows = 1;
+  const int upq = rows * 16, per_quad = rows * 64, nunit = fold_n * upq;
+  for (int idx = threadIdx.x; idx < nunit; idx += blockDim.x) {
+    const int gq = fold_q[idx / upq], u = idx % upq, row = u >> 4, col = 4 * (u & 15);
+    int lo = 0, hi = p.count - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.mats[mid].quad_begin <= gq) lo = mid; else hi = mid - 1;
+    }
+    const MatParams& m = p.mats[lo];
+    const int q = gq - m.quad_begin;
+    const int G = m.K / kGroup, S = div_up(G, seg_groups<MODE>()), T = m.N / kTileN;
+    if (col >= kTileN * min(kQuadTiles, T - kQuadTiles * q)) continue;  // ragged last quad
+    const long long q_first = m.item_begin + static_cast<long long>(q) * S;
+    const long long first = I * (owner_of(q_first, I, p.W) + 1) / p.W - 1;
+    const int nslot = static_cast<int>(q_first + S - first);
+    const float4* part = reinterpret_cast<const float4*>(p.partials + first * per_quad + row * 64 + col);
+    const int stride = per_quad / 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < nslot; s0 += 8) {  // 8 slots in flight, then fold in order
+      float4 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        v[k] = (s0 + k < nslot) ? __ldcg(part + static_cast<long long>(s0 + k) * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (s0 + k < nslot) {
+          if (s0 + k == 0) {
+            acc = v[k];
+          } else {
+            acc.x += v[k].x; acc.y += v[k].y; acc.z += v[k].z; acc.w += v[k].w;
+          }
+        }
+      }
+    }
+    uint32_t* yo = reinterpret_cast<uint32_t*>(m.y + static_cast<long long>(row) * m.N + kQuadTiles * kTileN * q + col);
+    yo[0] = static_cast<uint32_t>(to_bf16(acc.x)) | (static_cast<uint32_t>(to_bf16(acc.y)) << 16);
+    yo[1] = static_cast<uint32_t>(to_bf16(acc.z)) | (static_cast<uint32_t>(to_bf16(acc.w)) << 16);
   }
 }
 
@@ -941,7 +988,7 @@ bool make_plan(const HostMatrix* mats, int count, int M, bool verify, const Devi
     quads += NQ;
     groups += G;
     xbytes += static_cast<long long>(G) * pl.pkg;
-    if (quads > (1 << 24) || groups > 0x7FFFFFFF) return false;  // reduce_kernel indexes quads * 128 in int
+    if (quads > (1 << 24) || groups > 0x7FFFFFFF) return false;  // quad indices stay well inside int
   }
   pl.items = items;
   pl.total_quads = static_cast<int>(quads);
@@ -1005,8 +1052,7 @@ int launch_mode(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, cudaStr
     cudaGetLastError();
     return W4G128_ERR_CUDA;
   }
-
-  if (MODE != kMMA) return W4G128_OK;  // M = 1 folds split quads inside the streaming kernel
+  if (MODE != kMMA) return W4G128_OK;  // M = 1: split quads are folded inside the streaming kernel
   cfg.gridDim = dim3(static_cast<unsigned>(sp.total_quads));  // one CTA per quad
   cfg.blockDim = dim3(kRedThreads);
   cfg.dynamicSmemBytes = kRedSmem;
