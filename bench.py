@@ -213,15 +213,35 @@ def profiled_traffic():
 
 # --------------------------------------------------------------------------- CPU oracle
 
-def time_oracle(budget_s, cols_hint=None):
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def time_oracle(budget_s, cols_hint=None, nthreads=0):
     """Times the fp64 oracle on the first `cols` columns of every layer
-    matrix; returns (GB/s-equivalent of packed weight bytes, cores, sample, s)."""
+    matrix (nthreads 0: every core); returns (GB/s-equivalent of packed
+    weight bytes, threads, sample, s)."""
     import numpy as np
 
     import oracle
     import synth
     O = oracle.Oracle()
-    cores = O.max_threads()
+    cores = nthreads or O.max_threads()
 
     def timed(cols):
         tot = 0.0
@@ -231,7 +251,7 @@ def time_oracle(budget_s, cols_hint=None):
             c, s, m = synth.columns(SEED, i, K, N, sel)
             x = synth.x(SEED, 100 + i, 1, K)
             t0 = time.perf_counter()
-            O.gemm(x, c, s, m)
+            O.gemm(x, c, s, m, nthreads=nthreads)
             tot += time.perf_counter() - t0
             nbytes += weight_bytes(K, cols) + 2 * K + 2 * cols
         return nbytes, tot
@@ -395,6 +415,21 @@ def run_ours(args):
     for M in MS:
         totals[M] = timed_graph(M, args.steps, args.warmup)
     clk = clocks.stop()
+
+    # informative only: the same step with one weight copy (209 MB, so the
+    # 126 MB L2 holds part of it between steps)
+    l2_warm = {}
+    for M in (1, 8):
+        _, _, _, descs_w, ws_w = io[M]
+        g = capture([lambda cs: w.w4g128_decode_step(descs_w[0], M, ws_w, stream=cs) for _ in range(50)])
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        l2_warm[f"M{M}_us_per_step"] = round(e0.elapsed_time(e1) * 1e3 / 50, 3)
     total1, total8 = totals[1], totals[8]
     launch1, launch8 = total1 / args.steps, total8 / args.steps
 
@@ -562,7 +597,10 @@ def run_ours(args):
     cpu = None
     if not args.no_cpu_baseline:
         v, cores, sample, _ = time_oracle(args.cpu_budget)
-        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+        v1, _, sample1, _ = time_oracle(args.cpu_budget / 5, nthreads=1)
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
+               "cpu_model": cpu_model(), "nproc": os.cpu_count(),
+               "single_thread": {"value": round(v1, 4), "sample": sample1}}
 
     out = {
         "metric": METRIC,
@@ -588,6 +626,7 @@ def run_ours(args):
                "achieved": round(achieved8, 1), "frac": round(achieved8 / peak, 4),
                "verify_cost_ratio_t8_over_t1": round(total8 / total1, 4)},
         "layer_step_by_M": by_m,
+        "layer_step_one_copy_l2_warm_informative": l2_warm,
         "us_per_call": per_call,
         "full_decode_step": full,
         "bandwidth_probes": probe,
