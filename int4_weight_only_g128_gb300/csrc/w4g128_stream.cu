@@ -1,5 +1,7 @@
 // The weight-streaming kernels: y_i = x_i . dequant(W_i) for a list of
-// int4-g128 matrices, M = 1 on CUDA cores and M <= 8 on the warp-level MMA.
+// int4-g128 matrices -- M = 1 decode on CUDA cores, the M <= 8 verify (M = 1
+// included, so that its rows match bit for bit whatever M) on the warp-level
+// MMA.
 //
 // Design (sm_103a, one GPU):
 //  * The work is a flat list of items (matrix, 64-column quad, segment of 4
@@ -65,7 +67,7 @@ namespace {
 // ----------------------------------------------------------------- modes
 
 enum Mode : int {
-  kM1 = 0,   // M = 1, CUDA cores: bf16 x bf16 -> fp32 FMA on the dequantised pairs
+  kM1 = 0,   // M = 1, CUDA cores: fp16 x fp16 -> fp32 FMA on the dequantised pairs
   kMMA = 1,  // M <= 8, warp MMA m16n8k16 f16 -> f32 with the weights as the 16-row operand
   kMMA1 = 2, // M = 1 with the verify arithmetic: the warp MMA, every B column carrying the one x row
 };
@@ -97,10 +99,10 @@ template <> struct Pkg<kMMA> { static constexpr int kRows = 8, kRowBytes = 320, 
 template <> struct Pkg<kMMA1> { static constexpr int kRows = 1, kRowBytes = 320, kBytes = 336; };
 
 // Groups per split-K segment (an item's K extent): fixed per mode, never by
-// the grid, so every summation order depends on the shape and M alone.  At
-// M = 1 a segment partial is 256 bytes, so shorter segments are cheap and give
-// small matrices enough items to occupy every SM; at M >= 2 a partial is
-// 2 KB and segments stay at 512 rows.
+// the grid, so every summation order depends on the shape and M alone.  Both
+// modes use 512 rows: shorter M = 1 segments (a partial is only 256 bytes
+// there) speed up single small calls but cost more per-segment work on large
+// ones; at M >= 2 a partial is 2 KB.
 template <int MODE>
 __host__ __device__ constexpr int seg_groups() { return MODE == kM1 ? W4G128_SEG_GROUPS_M1 : kSegGroups; }
 
@@ -456,230 +458,229 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
   bool failed = false;
   if (wg < p.W) {
 
-  const uint32_t bar0 = smem_addr(smem) + warp * kDepth * 8;
-  const uint32_t ring0 = smem_addr(smem) + kBarBytes + warp * kDepth * kSlot;
-  const uint8_t* ring = smem + kBarBytes + warp * kDepth * kSlot;
+    const uint32_t bar0 = smem_addr(smem) + warp * kDepth * 8;
+    const uint32_t ring0 = smem_addr(smem) + kBarBytes + warp * kDepth * kSlot;
+    const uint8_t* ring = smem + kBarBytes + warp * kDepth * kSlot;
 
-  uint64_t pol_w = 0, pol_x = 0;
-  if (lane == 0) {
-#pragma unroll
-    for (int d = 0; d < kDepth; ++d) mbar_init(bar0 + 8 * d, 1);
-    fence_mbar_init();
-    pol_w = l2_policy_evict_first();
-    pol_x = l2_policy_evict_last();
-  }
-  __syncwarp();
-
-  Cursor cc, ic;  // compute cursor, issue cursor
-  cursor_seek<MODE>(cc, p, it_a);
-  ic = cc;
-  // Prologue: the weight bytes do not depend on the prep kernel, so start them
-  // before waiting for it; the activation packages follow after the wait.
-  // Every lane walks the cursors; lane 0 alone issues copies.  The MMA modes
-  // start one chunk early only: their larger prep finishes sooner when less
-  // prefetch is queued ahead of its completion (measured: lm_head M=8
-  // 115.1 -> 113.8 us; at M = 1 the full ring ahead is faster).
-  constexpr int kEarly = (MODE == kMMA) ? 1 : kDepth;
-  Cursor pre[kDepth];
-  int n_pre = 0;
-#pragma unroll
-  for (int d = 0; d < kEarly; ++d) {
-    if (ic.item < it_b) {
-      if (lane == 0) issue_weights<MODE>(ic, ring0 + d * kSlot, bar0 + 8 * d, pol_w);
-      pre[d] = ic;
-      ++n_pre;
-      cursor_next<MODE>(ic, p);
-    }
-  }
-  grid_dependency_wait();
-  if (lane == 0) {
-#pragma unroll
-    for (int d = 0; d < kDepth; ++d)
-      if (d < n_pre) issue_package<MODE>(pre[d], ring0 + d * kSlot, bar0 + 8 * d, pol_x);
-  }
-  unsigned issued = static_cast<unsigned>(n_pre);
-  while (issued < static_cast<unsigned>(kDepth) && ic.item < it_b) {  // the rest of the ring
+    uint64_t pol_w = 0, pol_x = 0;
     if (lane == 0) {
-      issue_weights<MODE>(ic, ring0 + issued * kSlot, bar0 + 8 * issued, pol_w);
-      issue_package<MODE>(ic, ring0 + issued * kSlot, bar0 + 8 * issued, pol_x);
-    }
-    cursor_next<MODE>(ic, p);
-    ++issued;
-  }
-  // The reduce kernel may start launching now; it waits for this grid to
-  // finish before it reads any partial.
-  grid_dependents_launch();
-
-  float seg[kQuadTiles][NA];
-  float tot[kQuadTiles][NA];
 #pragma unroll
-  for (int t = 0; t < kQuadTiles; ++t)
-#pragma unroll
-    for (int e = 0; e < NA; ++e) seg[t][e] = tot[t][e] = 0.f;
-
-  unsigned done = 0;  // chunks consumed
-  while (cc.item < it_b) {
-    const int slot = static_cast<int>(done % kDepth);
-    const uint32_t parity = (done / kDepth) & 1u;
-    if (!mbar_wait_bounded(bar0 + 8 * slot, parity)) {
-      // Give up: record the timeout, drain this warp's copies in flight
-      // (again bounded) and leave.  Quads this warp shared stay unreduced.
-      if (lane == 0) {
-        atomicCAS(p.status, 0u, static_cast<unsigned>(W4G128_ERR_TIMEOUT));
-        for (unsigned k = done + 1; k < issued; ++k)
-          (void)mbar_wait_bounded(bar0 + 8 * static_cast<int>(k % kDepth), (k / kDepth) & 1u);
-      }
-      __syncwarp();
-      failed = true;
-      break;
+      for (int d = 0; d < kDepth; ++d) mbar_init(bar0 + 8 * d, 1);
+      fence_mbar_init();
+      pol_w = l2_policy_evict_first();
+      pol_x = l2_policy_evict_last();
     }
-    const int ntiles = cc.ntiles;
-    // M = 1: a straight-line body for full quads lets the compiler interleave
-    // the four tiles; the MMA path keeps per-tile blocks (register budget).
-    if (MODE == kM1 && ntiles == kQuadTiles)
-      compute_chunk<MODE, true>(ring + slot * kSlot, ntiles, lane, seg);
-    else
-      compute_chunk<MODE, false>(ring + slot * kSlot, ntiles, lane, seg);
-
-    // Slot consumed: refill it with the chunk kDepth ahead.
     __syncwarp();
-    if (ic.item < it_b) {
+
+    Cursor cc, ic;  // compute cursor, issue cursor
+    cursor_seek<MODE>(cc, p, it_a);
+    ic = cc;
+    // Prologue: the weight bytes do not depend on the prep kernel, so start them
+    // before waiting for it; the activation packages follow after the wait.
+    // Every lane walks the cursors; lane 0 alone issues copies.  The MMA modes
+    // start one chunk early only: their larger prep finishes sooner when less
+    // prefetch is queued ahead of its completion (measured: lm_head M=8
+    // 115.1 -> 113.8 us; at M = 1 the full ring ahead is faster).
+    constexpr int kEarly = (MODE == kMMA) ? 1 : kDepth;
+    Cursor pre[kDepth];
+    int n_pre = 0;
+#pragma unroll
+    for (int d = 0; d < kEarly; ++d) {
+      if (ic.item < it_b) {
+        if (lane == 0) issue_weights<MODE>(ic, ring0 + d * kSlot, bar0 + 8 * d, pol_w);
+        pre[d] = ic;
+        ++n_pre;
+        cursor_next<MODE>(ic, p);
+      }
+    }
+    grid_dependency_wait();
+    if (lane == 0) {
+#pragma unroll
+      for (int d = 0; d < kDepth; ++d)
+        if (d < n_pre) issue_package<MODE>(pre[d], ring0 + d * kSlot, bar0 + 8 * d, pol_x);
+    }
+    unsigned issued = static_cast<unsigned>(n_pre);
+    while (issued < static_cast<unsigned>(kDepth) && ic.item < it_b) {  // the rest of the ring
       if (lane == 0) {
-        fence_proxy_async_smem();
-        const uint32_t sa = ring0 + slot * kSlot, ba = bar0 + 8 * slot;
-        issue_weights<MODE>(ic, sa, ba, pol_w);
-        issue_package<MODE>(ic, sa, ba, pol_x);
+        issue_weights<MODE>(ic, ring0 + issued * kSlot, bar0 + 8 * issued, pol_w);
+        issue_package<MODE>(ic, ring0 + issued * kSlot, bar0 + 8 * issued, pol_x);
       }
       cursor_next<MODE>(ic, p);
       ++issued;
     }
-    ++done;
+    // M >= 2: the reduce kernel may start launching now; it waits for this
+    // grid to finish before it reads any partial.
+    grid_dependents_launch();
 
-    if (cc.g + 1 == cc.g_end) {
-      // ---- end of a segment
-      const MatParams& m = p.mats[cc.mi];
-      const int S = cc.S;
-      const long long q_first = m.item_begin + static_cast<long long>(cc.q) * S;
-      const long long q_last = q_first + S - 1;
-      const bool owned = (q_first >= it_a) && (q_last < it_b);
-      // A run holding the quad's first segments but not all of them (the
-      // quad continues in later warps) keeps their left fold too and stores it
-      // as one partial: the fold over segments then starts from it.
-      const bool prefix = (q_first >= it_a) && !owned;
-      if constexpr (MODE == kM1) {
-        // reduce the 4 lane classes c of each column (same tree on every lane)
+    float seg[kQuadTiles][NA];
+    float tot[kQuadTiles][NA];
 #pragma unroll
-        for (int t = 0; t < kQuadTiles; ++t)
+    for (int t = 0; t < kQuadTiles; ++t)
 #pragma unroll
-          for (int e = 0; e < NA; ++e) {
-            float v = seg[t][e];
-            v += __shfl_xor_sync(0xffffffffu, v, 1);
-            v += __shfl_xor_sync(0xffffffffu, v, 2);
-            seg[t][e] = v;
-          }
-      }
-      const int rows = (MODE == kM1) ? 1 : p.M;
-      if (owned || prefix) {
-#pragma unroll
-        for (int t = 0; t < kQuadTiles; ++t)
-#pragma unroll
-          for (int e = 0; e < NA; ++e) tot[t][e] = (cc.s == 0) ? seg[t][e] : tot[t][e] + seg[t][e];
-      }
-      if (!owned && (!prefix || cc.item + 1 == it_b)) {
-        // one slot per (matrix, quad, segment): the segment sum, or at the last
-        // segment of a prefix run the fold of segments 0 .. s
-        float* part = p.partials + cc.item * rows * 64;
-        if constexpr (MODE == kM1) {
-          // lane (r, c) stores tile c's columns r and r + 8
-          if (c < ntiles) {
-            part[16 * c + r] = prefix ? pick(tot, c, 0) : pick(seg, c, 0);
-            part[16 * c + r + 8] = prefix ? pick(tot, c, 1) : pick(seg, c, 1);
-          }
-        } else {
-#pragma unroll
-          for (int t = 0; t < kQuadTiles; ++t) {
-            if (t < ntiles) {
-              if (2 * c < rows) {
-                part[(2 * c) * 64 + 16 * t + r] = prefix ? tot[t][0] : seg[t][0];
-                part[(2 * c) * 64 + 16 * t + r + 8] = prefix ? tot[t][2] : seg[t][2];
-              }
-              if (2 * c + 1 < rows) {
-                part[(2 * c + 1) * 64 + 16 * t + r] = prefix ? tot[t][1] : seg[t][1];
-                part[(2 * c + 1) * 64 + 16 * t + r + 8] = prefix ? tot[t][3] : seg[t][3];
-              }
-            }
-          }
+      for (int e = 0; e < NA; ++e) seg[t][e] = tot[t][e] = 0.f;
+
+    unsigned done = 0;  // chunks consumed
+    while (cc.item < it_b) {
+      const int slot = static_cast<int>(done % kDepth);
+      const uint32_t parity = (done / kDepth) & 1u;
+      if (!mbar_wait_bounded(bar0 + 8 * slot, parity)) {
+        // Give up: record the timeout, drain this warp's copies in flight
+        // (again bounded) and leave.  Quads this warp shared stay unreduced.
+        if (lane == 0) {
+          atomicCAS(p.status, 0u, static_cast<unsigned>(W4G128_ERR_TIMEOUT));
+          for (unsigned k = done + 1; k < issued; ++k)
+            (void)mbar_wait_bounded(bar0 + 8 * static_cast<int>(k % kDepth), (k / kDepth) & 1u);
         }
+        __syncwarp();
+        failed = true;
+        break;
       }
-#pragma unroll
-      for (int t = 0; t < kQuadTiles; ++t)
-#pragma unroll
-        for (int e = 0; e < NA; ++e) seg[t][e] = 0.f;
+      const int ntiles = cc.ntiles;
+      // M = 1: a straight-line body for full quads lets the compiler interleave
+      // the four tiles; the MMA path keeps per-tile blocks (register budget).
+      if (MODE == kM1 && ntiles == kQuadTiles)
+        compute_chunk<MODE, true>(ring + slot * kSlot, ntiles, lane, seg);
+      else
+        compute_chunk<MODE, false>(ring + slot * kSlot, ntiles, lane, seg);
 
-      const bool quad_end = (cc.s == S - 1) || (cc.item + 1 == it_b);
-      if (quad_end) {
-        const int n0 = kQuadTiles * kTileN * cc.q;
-        if (owned) {
+      // Slot consumed: refill it with the chunk kDepth ahead.
+      __syncwarp();
+      if (ic.item < it_b) {
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          const uint32_t sa = ring0 + slot * kSlot, ba = bar0 + 8 * slot;
+          issue_weights<MODE>(ic, sa, ba, pol_w);
+          issue_package<MODE>(ic, sa, ba, pol_x);
+        }
+        cursor_next<MODE>(ic, p);
+        ++issued;
+      }
+      ++done;
+
+      if (cc.g + 1 == cc.g_end) {
+        // ---- end of a segment
+        const MatParams& m = p.mats[cc.mi];
+        const int S = cc.S;
+        const long long q_first = m.item_begin + static_cast<long long>(cc.q) * S;
+        const long long q_last = q_first + S - 1;
+        const bool owned = (q_first >= it_a) && (q_last < it_b);
+        // A run holding the quad's first segments but not all of them (the
+        // quad continues in later warps) keeps their left fold too and stores it
+        // as one partial: the fold over segments then starts from it.
+        const bool prefix = (q_first >= it_a) && !owned;
+        if constexpr (MODE == kM1) {
+          // reduce the 4 lane classes c of each column (same tree on every lane)
+#pragma unroll
+          for (int t = 0; t < kQuadTiles; ++t)
+#pragma unroll
+            for (int e = 0; e < NA; ++e) {
+              float v = seg[t][e];
+              v += __shfl_xor_sync(0xffffffffu, v, 1);
+              v += __shfl_xor_sync(0xffffffffu, v, 2);
+              seg[t][e] = v;
+            }
+        }
+        const int rows = (MODE == kM1) ? 1 : p.M;
+        if (owned || prefix) {
+#pragma unroll
+          for (int t = 0; t < kQuadTiles; ++t)
+#pragma unroll
+            for (int e = 0; e < NA; ++e) tot[t][e] = (cc.s == 0) ? seg[t][e] : tot[t][e] + seg[t][e];
+        }
+        if (!owned && (!prefix || cc.item + 1 == it_b)) {
+          // one slot per (matrix, quad, segment): the segment sum, or at the last
+          // segment of a prefix run the fold of segments 0 .. s
+          float* part = p.partials + cc.item * rows * 64;
           if constexpr (MODE == kM1) {
+            // lane (r, c) stores tile c's columns r and r + 8
             if (c < ntiles) {
-              m.y[n0 + 16 * c + r] = to_bf16(pick(tot, c, 0));
-              m.y[n0 + 16 * c + r + 8] = to_bf16(pick(tot, c, 1));
+              part[16 * c + r] = prefix ? pick(tot, c, 0) : pick(seg, c, 0);
+              part[16 * c + r + 8] = prefix ? pick(tot, c, 1) : pick(seg, c, 1);
             }
           } else {
 #pragma unroll
             for (int t = 0; t < kQuadTiles; ++t) {
               if (t < ntiles) {
-                const int n = n0 + 16 * t + r;
                 if (2 * c < rows) {
-                  m.y[(2 * c) * m.N + n] = to_bf16(tot[t][0]);
-                  m.y[(2 * c) * m.N + n + 8] = to_bf16(tot[t][2]);
+                  part[(2 * c) * 64 + 16 * t + r] = prefix ? tot[t][0] : seg[t][0];
+                  part[(2 * c) * 64 + 16 * t + r + 8] = prefix ? tot[t][2] : seg[t][2];
                 }
                 if (2 * c + 1 < rows) {
-                  m.y[(2 * c + 1) * m.N + n] = to_bf16(tot[t][1]);
-                  m.y[(2 * c + 1) * m.N + n + 8] = to_bf16(tot[t][3]);
+                  part[(2 * c + 1) * 64 + 16 * t + r] = prefix ? tot[t][1] : seg[t][1];
+                  part[(2 * c + 1) * 64 + 16 * t + r + 8] = prefix ? tot[t][3] : seg[t][3];
                 }
               }
             }
           }
-        } else if (MODE != kMMA && n_pend < 2) {
-          // Split quad at M = 1: its partials are written; the ticket comes after
-          // the stream.  (M >= 2: the reduce kernel folds every split quad.)
-          const int gq = m.quad_begin + cc.q;
-          const unsigned e = static_cast<unsigned>(owner_of(q_last, I, p.W) - owner_of(q_first, I, p.W) + 1);
-          if (n_pend == 0) {
-            pend_q0 = gq;
-            pend_e0 = e;
-          } else {
-            pend_q1 = gq;
-            pend_e1 = e;
+        }
+#pragma unroll
+        for (int t = 0; t < kQuadTiles; ++t)
+#pragma unroll
+          for (int e = 0; e < NA; ++e) seg[t][e] = 0.f;
+
+        const bool quad_end = (cc.s == S - 1) || (cc.item + 1 == it_b);
+        if (quad_end) {
+          const int n0 = kQuadTiles * kTileN * cc.q;
+          if (owned) {
+            if constexpr (MODE == kM1) {
+              if (c < ntiles) {
+                m.y[n0 + 16 * c + r] = to_bf16(pick(tot, c, 0));
+                m.y[n0 + 16 * c + r + 8] = to_bf16(pick(tot, c, 1));
+              }
+            } else {
+#pragma unroll
+              for (int t = 0; t < kQuadTiles; ++t) {
+                if (t < ntiles) {
+                  const int n = n0 + 16 * t + r;
+                  if (2 * c < rows) {
+                    m.y[(2 * c) * m.N + n] = to_bf16(tot[t][0]);
+                    m.y[(2 * c) * m.N + n + 8] = to_bf16(tot[t][2]);
+                  }
+                  if (2 * c + 1 < rows) {
+                    m.y[(2 * c + 1) * m.N + n] = to_bf16(tot[t][1]);
+                    m.y[(2 * c + 1) * m.N + n + 8] = to_bf16(tot[t][3]);
+                  }
+                }
+              }
+            }
+          } else if (MODE != kMMA && n_pend < 2) {
+            // Split quad at M = 1: its partials are written; the ticket comes after
+            // the stream.  (M >= 2: the reduce kernel folds every split quad.)
+            const int gq = m.quad_begin + cc.q;
+            const unsigned e = static_cast<unsigned>(owner_of(q_last, I, p.W) - owner_of(q_first, I, p.W) + 1);
+            if (n_pend == 0) {
+              pend_q0 = gq;
+              pend_e0 = e;
+            } else {
+              pend_q1 = gq;
+              pend_e1 = e;
+            }
+            ++n_pend;
           }
-          ++n_pend;
         }
       }
+      cursor_next<MODE>(cc, p);
     }
-    cursor_next<MODE>(cc, p);
-  }
-  if (!failed && n_pend > 0) {
-    __threadfence();  // this warp's partials are visible before its tickets
-    __syncwarp();
-    if (lane == 0) {
-      // the warp holding a quad's last ticket hands the quad to its CTA's fold
-      if (atomicAdd(p.tickets + pend_q0, 1u) + 1 == pend_e0) fold_q[atomicAdd(&fold_n, 1)] = pend_q0;
-      if (n_pend > 1 && atomicAdd(p.tickets + pend_q1, 1u) + 1 == pend_e1) fold_q[atomicAdd(&fold_n, 1)] = pend_q1;
+    if (!failed && n_pend > 0) {
+      __threadfence();  // this warp's partials are visible before its tickets
+      __syncwarp();
+      if (lane == 0) {
+        // the warp holding a quad's last ticket hands the quad to its CTA's fold
+        if (atomicAdd(p.tickets + pend_q0, 1u) + 1 == pend_e0) fold_q[atomicAdd(&fold_n, 1)] = pend_q0;
+        if (n_pend > 1 && atomicAdd(p.tickets + pend_q1, 1u) + 1 == pend_e1) fold_q[atomicAdd(&fold_n, 1)] = pend_q1;
+      }
+      __syncwarp();
     }
-    __syncwarp();
-  }
   }  // warp in range
   if constexpr (MODE == kMMA) return;  // M >= 2: the reduce kernel folds
   __syncthreads();
   __threadfence();  // the other contributors' partials, published before their tickets
 
   // ---- fold the completed split quads: one thread per (quad, 4 columns), the
-  // quad's slots from its first warp's prefix fold on, in segment order.
-  const int rows = 1;
-  const int upq = rows * 16, per_quad = rows * 64, nunit = fold_n * upq;
+  // quad's 64-float slots from its first warp's prefix fold on, in segment order.
+  const int nunit = fold_n * 16;
   for (int idx = threadIdx.x; idx < nunit; idx += blockDim.x) {
-    const int gq = fold_q[idx / upq], u = idx % upq, row = u >> 4, col = 4 * (u & 15);
+    const int gq = fold_q[idx >> 4], col = 4 * (idx & 15);
     int lo = 0, hi = p.count - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -692,14 +693,13 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
     const long long q_first = m.item_begin + static_cast<long long>(q) * S;
     const long long first = I * (owner_of(q_first, I, p.W) + 1) / p.W - 1;
     const int nslot = static_cast<int>(q_first + S - first);
-    const float4* part = reinterpret_cast<const float4*>(p.partials + first * per_quad + row * 64 + col);
-    const int stride = per_quad / 4;
+    const float4* part = reinterpret_cast<const float4*>(p.partials + first * 64 + col);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = 0; s0 < nslot; s0 += 8) {  // 8 slots in flight, then fold in order
       float4 v[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        v[k] = (s0 + k < nslot) ? __ldcg(part + static_cast<long long>(s0 + k) * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[k] = (s0 + k < nslot) ? __ldcg(part + static_cast<long long>(s0 + k) * 16) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         if (s0 + k < nslot) {
@@ -711,7 +711,7 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
         }
       }
     }
-    uint32_t* yo = reinterpret_cast<uint32_t*>(m.y + static_cast<long long>(row) * m.N + kQuadTiles * kTileN * q + col);
+    uint32_t* yo = reinterpret_cast<uint32_t*>(m.y + kQuadTiles * kTileN * q + col);
     yo[0] = static_cast<uint32_t>(to_bf16(acc.x)) | (static_cast<uint32_t>(to_bf16(acc.y)) << 16);
     yo[1] = static_cast<uint32_t>(to_bf16(acc.z)) | (static_cast<uint32_t>(to_bf16(acc.w)) << 16);
   }

@@ -149,3 +149,31 @@ def test_lm_head_full_size_sampled(N):
         x = synth.x(SEED, 100 + M, M, K)
         y = run(mat, x)
         check_against_oracle(y, x, c, s, m, cols=cols)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M", [1, 8])
+def test_largest_k(M):
+    """K = 65536, the largest K the boundary accepts (512 groups, 128 segments
+    per quad), with a ragged last quad: every output against the oracle."""
+    K, N = 65536, 208
+    mat = DevMatrix(K, N, matrix_id=101)
+    x = synth.x(SEED, 101 + M, M, K)
+    check_against_oracle(run(mat, x, verify=(M > 1)), x, mat.codes, mat.scales, mat.mins)
+
+
+@pytest.mark.gpu
+def test_largest_n_sampled():
+    """N = 2^24, the largest N the boundary accepts (262,144 quads, 1.07 GB
+    packed at K = 128), device-generated; sampled columns, first and last
+    included, at M = 1 (gemv) and M = 8 (verify)."""
+    K, N = 128, 1 << 24
+    mat = DevMatrix(K, N, matrix_id=102, device_fill=True)
+    mat.free_canonical()
+    rng = np.random.default_rng(7)
+    cols = np.unique(np.concatenate([[0, 1, 63, 64, N // 2, N - 64, N - 1], rng.integers(0, N, 200)]))
+    c, s, m = synth.columns(SEED, 102, K, N, cols)
+    for M in (1, 8):
+        x = synth.x(SEED, 102 + M, M, K)
+        y = run(mat, x, verify=(M > 1))
+        check_against_oracle(y, x, c, s, m, cols=cols)
