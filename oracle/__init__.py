@@ -60,6 +60,7 @@ def _load(mutant=0):
     lib.oracle_pack_tiled.argtypes = [p, p, p, i, i, p]
     lib.oracle_unpack_tiled.argtypes = [p, i, i, p, p, p]
     lib.oracle_quantize.argtypes = [p, i, i, i, p, p, p, p]
+    lib.oracle_add_rmsnorm.argtypes = [i, i, p, p, p, ctypes.c_double, p, p]
     _libs[mutant] = lib
     return lib
 
@@ -191,3 +192,51 @@ def _quantize(self, w, search):
 
 
 Oracle.quantize = _quantize
+
+
+def _add_rmsnorm(self, y, residual, gamma, eps):
+    """Residual add and RMS norm of the product rows (oracle_add_rmsnorm).
+
+    y: [M][N] fp64 product (from ``gemm``), residual: [M][N] bf16 bits,
+    gamma: [N] bf16 bits.  Returns (h, out), both [M][N] fp64 and unrounded:
+    h = residual + y, out = gamma * h / sqrt(mean_n(h^2) + eps)."""
+    y, yp = _c(y, np.float64)
+    residual, rp = _c(residual, np.uint16)
+    gamma, gp = _c(gamma, np.uint16)
+    M, N = y.shape
+    assert residual.shape == (M, N) and gamma.shape == (N,)
+    h = np.empty((M, N), dtype=np.float64)
+    out = np.empty((M, N), dtype=np.float64)
+    self.lib.oracle_add_rmsnorm(M, N, yp, rp, gp, float(eps), h.ctypes.data_as(ctypes.c_void_p),
+                                out.ctypes.data_as(ctypes.c_void_p))
+    return h, out
+
+
+Oracle.add_rmsnorm = _add_rmsnorm
+
+
+def norm_bounds(h_ref, out_ref, a, gamma, eps, oracle=None):
+    """Acceptance bounds for the fused residual add + RMS norm.
+
+    h: the product's bound carried over, |h_gpu - h_ref| <= dh = 4e-3*a +
+    ulp_bf16(h_ref) (the GPU adds the residual to its fp32 product and rounds
+    once to bf16).  out: the GPU normalises its own bf16 h, so each h_j may be
+    off by dh_j; with ms = mean(h_ref^2) + eps the mean square moves by at
+    most D = mean(2|h_ref| dh + dh^2), the reciprocal root by the relative
+    rho = 1/sqrt(1 - D/ms) - 1 (plus 2^-20 for the fp32 sum, root and
+    products), and
+        |out_gpu - out_ref| <= |gamma| r (1 + rho) dh + |out_ref| rho + ulp_bf16(out_ref),
+    r = 1/sqrt(ms).  Returns (dh, dout); rows whose D reaches ms get an
+    infinite bound (no information left)."""
+    o = oracle or Oracle()
+    h_ref = np.asarray(h_ref, dtype=np.float64)
+    out_ref = np.asarray(out_ref, dtype=np.float64)
+    g = np.abs(bf16_bits_to_f64(gamma))[None, :]
+    dh = 4e-3 * np.asarray(a, dtype=np.float64) + o.bf16_ulp_array(h_ref)
+    ms = np.mean(h_ref * h_ref, axis=1, keepdims=True) + float(eps)
+    D = np.mean(2.0 * np.abs(h_ref) * dh + dh * dh, axis=1, keepdims=True)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        rho = np.where(D < ms, 1.0 / np.sqrt(np.maximum(1.0 - D / ms, 1e-300)) - 1.0, np.inf) + 2.0 ** -20
+        r = 1.0 / np.sqrt(ms)
+    dout = g * r * (1.0 + rho) * dh + np.abs(out_ref) * rho + o.bf16_ulp_array(out_ref)
+    return dh, dout

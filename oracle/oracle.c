@@ -35,6 +35,9 @@
  * it is written from that specification and shares no code with the device
  * packer.
  *
+ * oracle_add_rmsnorm (at the end) folds the product into the residual add and
+ * RMS normalisation that follow it in the model (its own header there).
+ *
  * The quantizer (oracle_quantize, below) chooses codes, scales and minimums
  * from bf16 weights: round-to-nearest on the 16-level grid of each group,
  * optionally with a range search that clips outliers (its own header below).
@@ -45,7 +48,8 @@
  *   3 = the minimum term dropped,
  *   4 = quantizer rounds toward zero instead of to nearest,
  *   5 = quantizer spreads the range over 16 steps instead of 15,
- *   6 = quantizer keeps the candidate with the largest error.
+ *   6 = quantizer keeps the candidate with the largest error,
+ *   7, 8, 9 = mistakes in the residual add and RMS norm (listed there).
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -417,5 +421,51 @@ void oracle_quantize(const uint16_t* w, int K, int N, int search, uint32_t* code
         }
         scales[(size_t)g * N + n] = oracle_bf16_rn((double)best_s);
         mins[(size_t)g * N + n] = oracle_bf16_rn((double)best_m);
+    }
+}
+
+/* ---- the product folded into the residual add and RMS norm -------------
+ *
+ * Token Rush README, progress table steps 8-9: the split-K GEMV's partial
+ * sums are added up inside the normalisation that follows the projection,
+ * not in a pass of their own.  The pages name the norm and nothing more; the
+ * reading taken here is the pre-norm transformer's residual update followed by
+ * RMS normalisation (Zhang and Sennrich, "Root Mean Square Layer
+ * Normalization", 2019), per output row m over the N columns:
+ *
+ *   h[m][n]   = residual[m][n] + y[m][n]            (the new residual stream)
+ *   out[m][n] = gamma[n] * h[m][n] / sqrt( (1/N) sum_j h[m][j]^2 + eps )
+ *
+ * y is the product computed above (fp64, not rounded); residual and gamma are
+ * bf16, eps a non-negative real.  Everything is fp64, summed in ascending j;
+ * neither h nor out is rounded to bf16 here.
+ *
+ * Mutants: 7 = mean taken over N - 1 columns, 8 = eps dropped,
+ *          9 = residual not added.
+ */
+void oracle_add_rmsnorm(int M, int N, const double* y, const uint16_t* residual, const uint16_t* gamma,
+                        double eps, double* h, double* out) {
+    for (int m = 0; m < M; m++) {
+        const size_t row = (size_t)m * (size_t)N;
+        double ss = 0.0;
+        for (int n = 0; n < N; n++) {
+            double r = bf16_val(residual[row + n]);
+#if ORACLE_MUTANT == 9
+            r = 0.0;
+#endif
+            const double v = r + y[row + n];
+            h[row + n] = v;
+            ss += v * v;
+        }
+        double cols = (double)N;
+#if ORACLE_MUTANT == 7
+        cols = (double)(N - 1);
+#endif
+        double e = eps;
+#if ORACLE_MUTANT == 8
+        e = 0.0;
+#endif
+        const double inv_rms = 1.0 / sqrt(ss / cols + e);
+        for (int n = 0; n < N; n++) out[row + n] = bf16_val(gamma[n]) * (h[row + n] * inv_rms);
     }
 }
