@@ -42,6 +42,9 @@ LAYER = [("q", 5120, 6144), ("k", 5120, 6144), ("v", 5120, 6144), ("o", 6144, 51
 # (a prefix view of the same packed buffer).
 SHAPES = [("square", 4096, 4096), ("q_k_v", 5120, 6144), ("o", 6144, 5120), ("gate_up", 5120, 34816),
           ("down", 17408, 5120), ("lm_head", 5120, 248320), ("lm_head_slice", 5120, 131072)]
+# The projections whose output feeds a residual add + RMS norm (attention
+# output and MLP down), timed fused and plain.
+NORM_SHAPES = [(6144, 5120), (17408, 5120)]
 LM_HEAD = (5120, 248320)
 N_LAYERS = 64
 L2_BYTES = 129 * 1024 * 1024
@@ -499,6 +502,37 @@ def run_ours(args):
     del lm_packed
     torch.cuda.synchronize()
 
+    # ---- the product folded into the residual add + RMS norm, on the two projections a
+    # norm follows (attention output, MLP down): fused call vs the plain call, us per call
+    norm_fused = {}
+    for si, (K, N) in enumerate(NORM_SHAPES):
+        first = pack_device(K, N, 70 + si)
+        ncopy = max(1, -(-2 * L2_BYTES // weight_bytes(K, N)))
+        mats = [first] + [first.clone() for _ in range(ncopy - 1)]
+        gam = torch.from_numpy(synth.norm_weight(SEED, 80 + si, N).view(np.int16)).cuda()
+        for M in (1, 8):
+            x = torch.from_numpy(synth.x(SEED, 310 + si, M, K).view(np.int16)).cuda()
+            res = torch.from_numpy(synth.x(SEED, 320 + si, M, N).view(np.int16)).cuda()
+            h = torch.empty(M * N, dtype=torch.int16, device="cuda")
+            o = torch.empty(M * N, dtype=torch.int16, device="cuda")
+            wsd = torch.empty(w.w4g128_workspace_bytes(M, K, N), dtype=torch.uint8, device="cuda")
+
+            def fcall(cs, r, M=M, K=K, N=N, wsd=wsd, x=x, res=res, h=h, o=o, mats=mats):
+                w.w4g128_gemm_add_rmsnorm(mats[r % len(mats)], x, res, gam, 1e-6, h, o, M, K, N, 0, wsd,
+                                          stream=cs)
+
+            def pcall(cs, r, M=M, K=K, N=N, wsd=wsd, x=x, h=h, mats=mats):
+                if M == 1:
+                    w.w4g128_gemv(mats[r % len(mats)], x, h, K, N, wsd, stream=cs)
+                else:
+                    w.w4g128_gemm_verify(mats[r % len(mats)], x, h, M, K, N, wsd, stream=cs)
+            us_f = graph_us(fcall, 64)
+            us_p = graph_us(pcall, 64)
+            norm_fused[f"{K}x{N}_M{M}"] = {"us_fused": round(us_f, 3), "us_product_only": round(us_p, 3),
+                                           "added_us": round(us_f - us_p, 3)}
+        del mats
+    torch.cuda.synchronize()
+
     # ---- the whole decode-step weight stream: 64 layer sets + the lm_head, one decode_step call
     full = {}
     fmats = [(K, N) for _ in range(N_LAYERS) for _, K, N in LAYER] + [LM_HEAD]
@@ -628,6 +662,7 @@ def run_ours(args):
         "layer_step_by_M": by_m,
         "layer_step_one_copy_l2_warm_informative": l2_warm,
         "us_per_call": per_call,
+        "residual_add_rmsnorm_us": norm_fused,
         "full_decode_step": full,
         "bandwidth_probes": probe,
         "frac_of_read_probe": {"m1": round(achieved / probe["read_GBps"], 4),

@@ -199,6 +199,33 @@ W4G128_API int w4g128_decode_step(const w4g128_matrix* mats, int count, int M, v
 W4G128_API int w4g128_verify_step(const w4g128_matrix* mats, int count, int M, void* ws, size_t ws_bytes,
                                   void* stream);
 
+/* The product folded into the residual add and RMS norm that follow it
+ * (Token Rush README, progress table steps 8-9: the split-K partial sums are
+ * added up in the norm rather than in a pass of their own).  The pages name
+ * the norm only; this is the pre-norm transformer's residual update followed
+ * by RMS normalisation (Zhang and Sennrich, 2019), per row m over the N
+ * columns:
+ *   h[m][n]   = bf16( residual[m][n] + (x . dequant(W))[m][n] )
+ *   out[m][n] = bf16( gamma[n] h[m][n] / sqrt( mean_n h[m][n]^2 + eps ) )
+ * The product is the one w4g128_decode_step (verify = 0) or
+ * w4g128_verify_step (verify = 1) computes, kept in fp32; the residual is
+ * added to it in fp32 and h rounded once, so with residual = -0.0 h is bit for
+ * bit that call's y.  The norm reads the rounded h (the value the residual
+ * stream keeps): mean_n h^2 is summed in fp32 in an order fixed by N alone,
+ * and every step after it is one correctly rounded fp32 operation, so out is
+ * deterministic.  No pass of its own: the last CTA of the call's final kernel
+ * normalises the rows.
+ *   x [M][K], residual, h, out [M][N], gamma [N]: bf16, device, row-major,
+ *   caller-owned; 1 <= M <= W4G128_MAX_M.  h may be the residual itself
+ *   (updated in place); out must not overlap x, residual or h
+ *   (W4G128_ERR_INVALID_ARG when it is one of them).  residual, gamma, h,
+ *   out: 4-byte aligned.  eps: finite and >= 0.  verify: 0 or 1.  ws as for
+ *   w4g128_gemm_verify (w4g128_workspace_bytes(M, K, N) bytes). */
+W4G128_API int w4g128_gemm_add_rmsnorm(const void* packed, const w4g128_bf16* x, const w4g128_bf16* residual,
+                                       const w4g128_bf16* gamma, float eps, w4g128_bf16* h, w4g128_bf16* out,
+                                       int M, int K, int N, int verify, void* ws, size_t ws_bytes,
+                                       void* stream);
+
 /* Size of the fixed device scratch array behind w4g128_gemv_noalloc (16 MiB). */
 #define W4G128_NOALLOC_SCRATCH_BYTES (16u << 20)
 

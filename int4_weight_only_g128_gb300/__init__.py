@@ -95,6 +95,8 @@ def lib():
     L.w4g128_verify_step.argtypes = [ctypes.POINTER(_Matrix), i, i, p, sz, p]
     L.w4g128_gemv_noalloc.restype = i
     L.w4g128_gemv_noalloc.argtypes = [p, p, p, i, i, p]
+    L.w4g128_gemm_add_rmsnorm.restype = i
+    L.w4g128_gemm_add_rmsnorm.argtypes = [p, p, p, p, ctypes.c_float, p, p, i, i, i, i, p, sz, p]
     _lib = L
     return L
 
@@ -189,6 +191,15 @@ def w4g128_verify_step(mats, M, ws, ws_bytes=None, stream=None):
     arr = _matrices(mats)
     wb = _nbytes(ws) if ws_bytes is None else ws_bytes
     _check("w4g128_verify_step", lib().w4g128_verify_step(arr, len(mats), M, _ptr(ws), wb, _stream(stream)))
+
+
+def w4g128_gemm_add_rmsnorm(packed, x, residual, gamma, eps, h, out, M, K, N, verify, ws, ws_bytes=None,
+                            stream=None):
+    """h = residual + x W (bf16, one rounding), out = gamma h / rms(h) per row."""
+    wb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    _check("w4g128_gemm_add_rmsnorm",
+           lib().w4g128_gemm_add_rmsnorm(_ptr(packed), _ptr(x), _ptr(residual), _ptr(gamma), float(eps), _ptr(h),
+                                         _ptr(out), M, K, N, int(verify), _ptr(ws), wb, _stream(stream)))
 
 
 def w4g128_workspace_status(ws, stream=None):

@@ -39,14 +39,14 @@ int check_stream_call(const w4g128_matrix* mats, int count, int M, void* ws) {
 }
 
 int run_stream(const w4g128_matrix* mats, int count, int M, bool verify, void* ws, size_t ws_bytes,
-               void* stream) {
+               void* stream, const w4g128::NormArgs* norm = nullptr) {
   int rc = check_stream_call(mats, count, M, ws);
   if (rc != W4G128_OK) return rc;
   if (!w4g128::device_is_sm103()) return W4G128_ERR_DEVICE;
   static_assert(sizeof(HostMatrix) == sizeof(w4g128_matrix), "descriptor layout");
   HostMatrix hm[W4G128_MAX_MATRICES];
   for (int i = 0; i < count; ++i) hm[i] = HostMatrix{mats[i].packed, mats[i].x, mats[i].y, mats[i].K, mats[i].N};
-  return w4g128::launch_stream(hm, count, M, verify, ws, ws_bytes, as_stream(stream));
+  return w4g128::launch_stream(hm, count, M, verify, norm, ws, ws_bytes, as_stream(stream));
 }
 
 size_t stream_bytes(const w4g128_matrix* mats, int count, int M) {
@@ -142,6 +142,20 @@ int w4g128_decode_step(const w4g128_matrix* mats, int count, int M, void* ws, si
 
 int w4g128_verify_step(const w4g128_matrix* mats, int count, int M, void* ws, size_t ws_bytes, void* stream) {
   return run_stream(mats, count, M, true, ws, ws_bytes, stream);
+}
+
+int w4g128_gemm_add_rmsnorm(const void* packed, const w4g128_bf16* x, const w4g128_bf16* residual,
+                            const w4g128_bf16* gamma, float eps, w4g128_bf16* h, w4g128_bf16* out, int M, int K,
+                            int N, int verify, void* ws, size_t ws_bytes, void* stream) {
+  if (residual == nullptr || gamma == nullptr || out == nullptr) return W4G128_ERR_INVALID_ARG;
+  if (!(eps >= 0.0f && eps <= 3.0e38f)) return W4G128_ERR_INVALID_ARG;  // finite, not negative, not NaN
+  if (verify != 0 && verify != 1) return W4G128_ERR_INVALID_ARG;
+  if (out == h || out == residual || out == x || static_cast<const void*>(h) == static_cast<const void*>(x))
+    return W4G128_ERR_INVALID_ARG;
+  if (!aligned(residual, 4) || !aligned(gamma, 4) || !aligned(out, 4)) return W4G128_ERR_ALIGN;
+  const w4g128_matrix m{packed, x, h, K, N};
+  const w4g128::NormArgs norm{residual, gamma, out, eps};
+  return run_stream(&m, 1, M, verify != 0, ws, ws_bytes, stream, &norm);
 }
 
 int w4g128_workspace_status(const void* ws, int* status_out, void* stream) {

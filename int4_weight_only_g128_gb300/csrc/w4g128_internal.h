@@ -47,11 +47,21 @@ struct HostMatrix {
 // arguments.
 size_t stream_workspace_bytes(const HostMatrix* mats, int count, int M, bool verify);
 
+// The residual add + RMS norm that a one-matrix call may end in: y becomes
+// h = residual + x W and out = gamma h / rms(h) per row (device pointers).
+struct NormArgs {
+  const uint16_t* residual;
+  const uint16_t* gamma;
+  uint16_t* out;
+  float eps;
+};
+
 // Launches the prep, streaming and (M >= 2) reduce kernels; the API layer
 // validates arguments.  M >= 2 always uses the verify arithmetic (warp MMA);
-// at M = 1 `verify` selects it over the CUDA-core decode arithmetic.
-int launch_stream(const HostMatrix* mats, int count, int M, bool verify, void* ws, size_t ws_bytes,
-                  cudaStream_t stream);
+// at M = 1 `verify` selects it over the CUDA-core decode arithmetic.  norm:
+// nullptr, or the residual add + RMS norm (count must be 1).
+int launch_stream(const HostMatrix* mats, int count, int M, bool verify, const NormArgs* norm, void* ws,
+                  size_t ws_bytes, cudaStream_t stream);
 
 int read_workspace_status(const void* ws, int* status_out, cudaStream_t stream);
 

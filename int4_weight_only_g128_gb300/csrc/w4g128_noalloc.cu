@@ -73,6 +73,6 @@ extern "C" int w4g128_gemv_noalloc(const void* packed, const w4g128_bf16* x, w4g
   void* scratch = nullptr;
   const int rc = scratch_address(&scratch);
   if (rc != W4G128_OK) return rc;
-  return w4g128::launch_stream(&m, 1, 1, false, scratch, W4G128_NOALLOC_SCRATCH_BYTES,
+  return w4g128::launch_stream(&m, 1, 1, false, nullptr, scratch, W4G128_NOALLOC_SCRATCH_BYTES,
                                static_cast<cudaStream_t>(stream));
 }

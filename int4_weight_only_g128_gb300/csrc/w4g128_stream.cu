@@ -144,6 +144,14 @@ struct StreamParams {
   float* partials;       // [total_items][rows][64]: one slot per (matrix, quad, segment)
   unsigned* tickets;     // [total_quads] arrival counters (M = 1)
   unsigned* status;
+  unsigned* done;        // CTAs finished (the residual add + RMS norm call)
+  // The residual add + RMS norm call (one matrix; residual == nullptr
+  // otherwise): its y is h = residual + x W, and the last CTA to finish
+  // writes out = gamma h / rms(h).
+  const uint16_t* residual;
+  const uint16_t* gamma;
+  uint16_t* nout;
+  float eps;
   int count, M, W, total_quads, total_groups;
   MatParams mats[MAXMAT];
 };
@@ -321,6 +329,27 @@ __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v 
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 __device__ __forceinline__ uint16_t to_bf16(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 
+// Output element i of a matrix from its fp32 sum v: bf16(v), or, in the
+// residual add + RMS norm call, h = bf16(residual + v) -- one rounding, the
+// add kept apart from any multiply.  The element's residual is read by the
+// thread that writes it, so h may overwrite the residual in place.
+template <bool NORM, int MAXMAT>
+__device__ __forceinline__ uint16_t emit(const StreamParams<MAXMAT>& p, long long i, float v) {
+  if constexpr (NORM) v = __fadd_rn(v, __uint_as_float(static_cast<uint32_t>(p.residual[i]) << 16));
+  return to_bf16(v);
+}
+
+// Elements i, i + 1 (i even) as one 32-bit word.
+template <bool NORM, int MAXMAT>
+__device__ __forceinline__ uint32_t emit2(const StreamParams<MAXMAT>& p, long long i, float a, float b) {
+  if constexpr (NORM) {
+    const uint32_t r = *reinterpret_cast<const uint32_t*>(p.residual + i);
+    a = __fadd_rn(a, bf16_lo(r));
+    b = __fadd_rn(b, bf16_hi(r));
+  }
+  return static_cast<uint32_t>(to_bf16(a)) | (static_cast<uint32_t>(to_bf16(b)) << 16);
+}
+
 // Rows of the per-lane accumulators: M = 1 keeps (column r, column r+8);
 // the MMA keeps (r, 2c), (r, 2c+1), (r+8, 2c), (r+8, 2c+1).
 template <int MODE> struct Acc { static constexpr int kN = (MODE == kM1) ? 2 : 4; };
@@ -427,9 +456,177 @@ __device__ __forceinline__ float pick(const float (&v)[kQuadTiles][NA], int t, i
   return out;
 }
 
+// ----------------------------------------------------------------- RMS norm of the finished rows
+
+// The residual add + RMS norm call ends in one CTA, the last of the final
+// grid to finish, normalising every row m of h (the matrix's y) into out:
+//   out[m][n] = bf16( fl(fl(h[m][n] r_m) gamma[n]) ),
+//   r_m = 1 / sqrt( fl(S_m / N) + eps )   (one correctly rounded fp32 op each),
+// with S_m = sum_n h[m][n]^2 summed in an order fixed by N alone, not by the
+// CTA's size: the row's N/2 bf16 pairs are dealt round robin to 256 logical
+// lanes; a lane folds lo^2 then hi^2 of each of its pairs, in order, with
+// fp32 FMAs; a xor butterfly adds each strand of 32 lanes; the 8 strand sums
+// are added as a balanced tree.
+constexpr int kNormLanes = 256;                // logical lanes per row
+constexpr int kNormStrands = kNormLanes / 32;  // 8
+constexpr int kNormBatch = 4;                  // logical lanes a thread serves side by side
+constexpr int kNormChunk = 8;                  // pairs per logical lane loaded at once (sum of squares)
+constexpr int kNormChunk2 = 4;                 // the same for the output pass
+constexpr int kNormThreads = 512;              // threads of the reduce kernel when it ends in the norm
+constexpr int kNormStageMax = 160 * 1024;      // largest h + gamma the reduce kernel stages in shared memory
+
+template <bool SMEM>
+__device__ __forceinline__ uint32_t norm_ld(const uint32_t* a) {
+  if constexpr (SMEM) return *a;
+  else return __ldcg(a);  // written by other CTAs of this grid: read through L2
+}
+
+// The two passes over h (words of bf16 pairs, row-major [M][N/2]) and gamma
+// ([N/2]): from global memory, or (SMEM) from the copies staged in shared
+// memory.  Both read the same words in the same order, so they give the
+// same bits.  From global memory the time is L2 round trips, so each thread
+// issues the loads of kNormBatch logical lanes x a chunk of pairs before it
+// consumes any (absent pairs read as 0, which adds exactly nothing).
+template <bool SMEM, int MAXMAT>
+__device__ void norm_passes(const StreamParams<MAXMAT>& p, float* ss, const uint32_t* h, const uint32_t* gam) {
+  const MatParams& m = p.mats[0];
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31;  // nt: a multiple of 32
+  const int npairs = m.N >> 1, nll = p.M * kNormLanes;
+  for (int base = 0; base < nll; base += kNormBatch * nt) {
+    float acc[kNormBatch];
+#pragma unroll
+    for (int j = 0; j < kNormBatch; ++j) acc[j] = 0.f;
+    for (int k0 = 0; k0 < npairs; k0 += kNormChunk * kNormLanes) {
+      uint32_t v[kNormBatch][kNormChunk];
+#pragma unroll
+      for (int j = 0; j < kNormBatch; ++j) {
+        const int ll = base + j * nt + tid;
+        const long long row0 = static_cast<long long>(ll / kNormLanes) * npairs;
+#pragma unroll
+        for (int c = 0; c < kNormChunk; ++c) {
+          const int pi = (ll & (kNormLanes - 1)) + k0 + c * kNormLanes;
+          v[j][c] = (ll < nll && pi < npairs) ? norm_ld<SMEM>(h + row0 + pi) : 0u;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kNormBatch; ++j)
+#pragma unroll
+        for (int c = 0; c < kNormChunk; ++c) {
+          acc[j] = fmaf(bf16_lo(v[j][c]), bf16_lo(v[j][c]), acc[j]);
+          acc[j] = fmaf(bf16_hi(v[j][c]), bf16_hi(v[j][c]), acc[j]);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < kNormBatch; ++j) {
+      float v = acc[j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      const int ll = base + j * nt + tid;
+      if (lane == 0 && ll < nll) ss[ll >> 5] = v;
+    }
+  }
+  __syncthreads();
+  uint32_t* out = reinterpret_cast<uint32_t*>(p.nout);
+  for (int base = 0; base < nll; base += kNormBatch * nt) {
+    float rs[kNormBatch];
+#pragma unroll
+    for (int j = 0; j < kNormBatch; ++j) {
+      const int ll = min(base + j * nt + tid, nll - 1);
+      const float* r = ss + (ll / kNormLanes) * kNormStrands;
+      const float S = ((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7]));
+      rs[j] = __frsqrt_rn(__fadd_rn(__fdiv_rn(S, static_cast<float>(m.N)), p.eps));
+    }
+    for (int k0 = 0; k0 < npairs; k0 += kNormChunk2 * kNormLanes) {
+      uint32_t hv[kNormBatch][kNormChunk2], gv[kNormBatch][kNormChunk2];
+#pragma unroll
+      for (int j = 0; j < kNormBatch; ++j) {
+        const int ll = base + j * nt + tid;
+        const long long row0 = static_cast<long long>(ll / kNormLanes) * npairs;
+#pragma unroll
+        for (int c = 0; c < kNormChunk2; ++c) {
+          const int pi = (ll & (kNormLanes - 1)) + k0 + c * kNormLanes;
+          const bool in = ll < nll && pi < npairs;
+          hv[j][c] = in ? norm_ld<SMEM>(h + row0 + pi) : 0u;
+          gv[j][c] = in ? norm_ld<SMEM>(gam + pi) : 0u;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kNormBatch; ++j) {
+        const int ll = base + j * nt + tid;
+        const long long row0 = static_cast<long long>(ll / kNormLanes) * npairs;
+#pragma unroll
+        for (int c = 0; c < kNormChunk2; ++c) {
+          const int pi = (ll & (kNormLanes - 1)) + k0 + c * kNormLanes;
+          if (ll < nll && pi < npairs) {
+            const float a = __fmul_rn(__fmul_rn(bf16_lo(hv[j][c]), rs[j]), bf16_lo(gv[j][c]));
+            const float b = __fmul_rn(__fmul_rn(bf16_hi(hv[j][c]), rs[j]), bf16_hi(gv[j][c]));
+            out[row0 + pi] = static_cast<uint32_t>(to_bf16(a)) | (static_cast<uint32_t>(to_bf16(b)) << 16);
+          }
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+  uint32_t v;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(v));
+  return v;
+}
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// The norm, run by the last CTA.  When h and gamma fit in the `stage` bytes
+// of shared memory the CTA holds free, they are copied there first with
+// 4-byte asynchronous copies (every word in flight at once: one L2 round
+// trip), and both passes read shared memory; otherwise both read L2.
+template <int MAXMAT>
+__device__ void norm_rows(const StreamParams<MAXMAT>& p, float* ss, uint8_t* stage, uint32_t stage_bytes) {
+  const MatParams& m = p.mats[0];
+  const int npairs = m.N >> 1;
+  const uint32_t* h = reinterpret_cast<const uint32_t*>(m.y);
+  const uint32_t* gam = reinterpret_cast<const uint32_t*>(p.gamma);
+  const long long hwords = static_cast<long long>(p.M) * npairs;
+  if ((hwords + npairs) * 4 > static_cast<long long>(stage_bytes)) {
+    norm_passes<false>(p, ss, h, gam);
+    return;
+  }
+  uint32_t* sh = reinterpret_cast<uint32_t*>(stage);
+  uint32_t* sg = sh + hwords;
+  const uint32_t sh0 = smem_addr(sh), sg0 = smem_addr(sg);
+  for (int i = threadIdx.x; i < hwords; i += blockDim.x) cp_async4(sh0 + 4u * i, h + i);
+  for (int i = threadIdx.x; i < npairs; i += blockDim.x) cp_async4(sg0 + 4u * i, gam + i);
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
+  norm_passes<true>(p, ss, sh, sg);
+}
+
+// Every thread of every CTA of the call's final grid calls this after its last
+// write of h; the CTA that arrives last runs the norm (unless the call's
+// status word reports an error: out is then left unwritten).  No CTA waits
+// here.  Publication follows the barrier-then-release pattern: the CTA's
+// writes are ordered before thread 0's release by the barrier, and the last
+// CTA's reads after thread 0's acquire by the barrier that follows it.
+template <int MAXMAT>
+__device__ __forceinline__ void norm_arrive(const StreamParams<MAXMAT>& p, uint8_t* stage, uint32_t stage_bytes) {
+  __shared__ int last;
+  __shared__ float ss[W4G128_MAX_M * kNormStrands];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    grid_dependency_wait();  // the counter was cleared by the prep kernel
+    unsigned prev;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(p.done) : "memory");
+    last = (prev + 1u == gridDim.x) && (*reinterpret_cast<volatile unsigned*>(p.status) == 0u);
+  }
+  __syncthreads();
+  if (last) norm_rows(p, ss, stage, stage_bytes);
+}
+
 // ----------------------------------------------------------------- the streaming kernel
 
-template <int MODE, int MAXMAT>
+template <int MODE, int MAXMAT, bool NORM>
 __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int NA = Acc<MODE>::kN;
@@ -624,8 +821,9 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
           if (owned) {
             if constexpr (MODE == kM1) {
               if (c < ntiles) {
-                m.y[n0 + 16 * c + r] = to_bf16(pick(tot, c, 0));
-                m.y[n0 + 16 * c + r + 8] = to_bf16(pick(tot, c, 1));
+                const int n = n0 + 16 * c + r;
+                m.y[n] = emit<NORM>(p, n, pick(tot, c, 0));
+                m.y[n + 8] = emit<NORM>(p, n + 8, pick(tot, c, 1));
               }
             } else {
 #pragma unroll
@@ -633,12 +831,14 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
                 if (t < ntiles) {
                   const int n = n0 + 16 * t + r;
                   if (2 * c < rows) {
-                    m.y[(2 * c) * m.N + n] = to_bf16(tot[t][0]);
-                    m.y[(2 * c) * m.N + n + 8] = to_bf16(tot[t][2]);
+                    const int i = (2 * c) * m.N + n;
+                    m.y[i] = emit<NORM>(p, i, tot[t][0]);
+                    m.y[i + 8] = emit<NORM>(p, i + 8, tot[t][2]);
                   }
                   if (2 * c + 1 < rows) {
-                    m.y[(2 * c + 1) * m.N + n] = to_bf16(tot[t][1]);
-                    m.y[(2 * c + 1) * m.N + n + 8] = to_bf16(tot[t][3]);
+                    const int i = (2 * c + 1) * m.N + n;
+                    m.y[i] = emit<NORM>(p, i, tot[t][1]);
+                    m.y[i + 8] = emit<NORM>(p, i + 8, tot[t][3]);
                   }
                 }
               }
@@ -711,10 +911,14 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
         }
       }
     }
-    uint32_t* yo = reinterpret_cast<uint32_t*>(m.y + kQuadTiles * kTileN * q + col);
-    yo[0] = static_cast<uint32_t>(to_bf16(acc.x)) | (static_cast<uint32_t>(to_bf16(acc.y)) << 16);
-    yo[1] = static_cast<uint32_t>(to_bf16(acc.z)) | (static_cast<uint32_t>(to_bf16(acc.w)) << 16);
+    const int i = kQuadTiles * kTileN * q + col;
+    uint32_t* yo = reinterpret_cast<uint32_t*>(m.y + i);
+    yo[0] = emit2<NORM>(p, i, acc.x, acc.y);
+    yo[1] = emit2<NORM>(p, i + 2, acc.z, acc.w);
   }
+  // The rings are drained: the dynamic shared memory after the mbarriers can
+  // stage the norm.
+  if constexpr (NORM) norm_arrive(p, smem + kBarBytes, smem_bytes<MODE>() - kBarBytes);
 }
 
 // ----------------------------------------------------------------- prep kernel
@@ -726,11 +930,19 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
 // c == 0 adds the row's (X_g, f) to the package tail.
 template <int MODE, int MAXMAT>
 __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
+  // Launched early behind the previous kernel of the stream (programmatic
+  // dependent launch): the next kernel may launch at once, but nothing here
+  // is touched before the previous one has finished -- it may still read the
+  // workspace, or write this call's x.
   grid_dependents_launch();
+  grid_dependency_wait();
   const int tid = blockIdx.x * blockDim.x + threadIdx.x, nthreads = gridDim.x * blockDim.x;
   if (MODE != kMMA)
     for (int i = tid; i < p.total_quads; i += nthreads) p.tickets[i] = 0u;
-  if (tid == 0) *p.status = 0u;
+  if (tid == 0) {
+    *p.status = 0u;
+    *p.done = 0u;
+  }
 
   constexpr int kRows = Pkg<MODE>::kRows;
   const int lane = threadIdx.x & 31;
@@ -818,8 +1030,8 @@ constexpr int kRedThreads = kMaxRows * 16;                 // one per (row, 4 co
 constexpr int kRedStageBytes = kRedChunk * kMaxRows * 64 * 4;  // 16 KB at M = 8
 constexpr int kRedSmem = 2 * kRedStageBytes + 16;          // two stages + two mbarriers
 
-template <int MAXMAT>
-__global__ void __launch_bounds__(kRedThreads) reduce_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
+template <int MAXMAT, bool NORM>
+__global__ void __launch_bounds__(kNormThreads) reduce_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
   extern __shared__ __align__(128) uint8_t rsm[];
   __shared__ int ok;
   const int gq = blockIdx.x;
@@ -834,7 +1046,15 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(const __grid_consta
   const long long I = p.total_items;
   const long long q_first = m.item_begin + static_cast<long long>(q) * S;
   const int wf = owner_of(q_first, I, p.W);
-  if (wf == owner_of(q_first + S - 1, I, p.W)) return;  // owned: y is written
+  // The next call's prep kernel may launch now; it waits for this grid to
+  // finish, and this grid does not finish before the streaming kernel: every
+  // CTA waits for it (below, or here for owned quads).
+  grid_dependents_launch();
+  if (wf == owner_of(q_first + S - 1, I, p.W)) {  // owned: y is written
+    grid_dependency_wait();
+    if constexpr (NORM) norm_arrive(p, rsm + kRedSmem, dynamic_smem_bytes() - kRedSmem);
+    return;
+  }
   // Slots from the prefix run's last segment (which holds the fold of the
   // segments before it) to the quad's last segment.
   const long long first = I * (wf + 1) / p.W - 1;
@@ -898,10 +1118,12 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(const __grid_consta
     }
   }
   if (active) {
-    uint32_t* yo = reinterpret_cast<uint32_t*>(m.y + static_cast<long long>(row) * m.N + kQuadTiles * kTileN * q + col);
-    yo[0] = static_cast<uint32_t>(to_bf16(acc.x)) | (static_cast<uint32_t>(to_bf16(acc.y)) << 16);
-    yo[1] = static_cast<uint32_t>(to_bf16(acc.z)) | (static_cast<uint32_t>(to_bf16(acc.w)) << 16);
+    const long long i = static_cast<long long>(row) * m.N + kQuadTiles * kTileN * q + col;
+    uint32_t* yo = reinterpret_cast<uint32_t*>(m.y + i);
+    yo[0] = emit2<NORM>(p, i, acc.x, acc.y);
+    yo[1] = emit2<NORM>(p, i + 2, acc.z, acc.w);
   }
+  if constexpr (NORM) norm_arrive(p, rsm + kRedSmem, dynamic_smem_bytes() - kRedSmem);
 }
 
 // ----------------------------------------------------------------- host planning
@@ -919,14 +1141,21 @@ bool g_dev_init[64] = {false};
 template <int MODE>
 void setup_mode(DeviceInfo& d) {
   const int smem = smem_bytes<MODE>();
-  cudaFuncSetAttribute(stream_kernel<MODE, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  cudaFuncSetAttribute(stream_kernel<MODE, W4G128_MAX_MATRICES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaFuncSetAttribute(stream_kernel<MODE, 1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaFuncSetAttribute(stream_kernel<MODE, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaFuncSetAttribute(stream_kernel<MODE, W4G128_MAX_MATRICES, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        smem);
-  cudaFuncSetAttribute(reduce_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRedSmem);
-  cudaFuncSetAttribute(reduce_kernel<W4G128_MAX_MATRICES>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRedSmem);
-  int occ1 = 0, occ2 = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ1, stream_kernel<MODE, 1>, kNW * 32, smem);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, stream_kernel<MODE, W4G128_MAX_MATRICES>, kNW * 32, smem);
+  cudaFuncSetAttribute(reduce_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRedSmem);
+  cudaFuncSetAttribute(reduce_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       kRedSmem + kNormStageMax);
+  cudaFuncSetAttribute(reduce_kernel<W4G128_MAX_MATRICES, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       kRedSmem);
+  int occ1 = 0, occ2 = 0, occ3 = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ1, stream_kernel<MODE, 1, false>, kNW * 32, smem);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, stream_kernel<MODE, W4G128_MAX_MATRICES, false>, kNW * 32,
+                                                smem);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ3, stream_kernel<MODE, 1, true>, kNW * 32, smem);
+  occ2 = std::min(occ2, occ3);
   const int occ = std::min(occ1, occ2);
   d.occ[MODE] = occ > 0 ? occ : 1;
 }
@@ -1007,12 +1236,18 @@ bool make_plan(const HostMatrix* mats, int count, int M, bool verify, const Devi
 }
 
 template <int MAXMAT>
-void fill_params(StreamParams<MAXMAT>& sp, const HostMatrix* mats, int count, int M, const Plan& pl, void* ws) {
+void fill_params(StreamParams<MAXMAT>& sp, const HostMatrix* mats, int count, int M, const Plan& pl,
+                 const NormArgs* norm, void* ws) {
   auto* base = static_cast<uint8_t*>(ws);
   sp.total_items = pl.items;
   sp.partials = reinterpret_cast<float*>(base + pl.off_partials);
   sp.tickets = reinterpret_cast<unsigned*>(base + pl.off_tickets);
   sp.status = reinterpret_cast<unsigned*>(base);
+  sp.done = reinterpret_cast<unsigned*>(base + 128);  // inside the status word's 256 bytes
+  sp.residual = norm ? norm->residual : nullptr;
+  sp.gamma = norm ? norm->gamma : nullptr;
+  sp.nout = norm ? norm->out : nullptr;
+  sp.eps = norm ? norm->eps : 0.f;
   sp.count = count;
   sp.M = M;
   sp.W = pl.W;
@@ -1032,31 +1267,43 @@ void fill_params(StreamParams<MAXMAT>& sp, const HostMatrix* mats, int count, in
   }
 }
 
-template <int MODE, int MAXMAT>
+template <int MODE, int MAXMAT, bool NORM>
 int launch_mode(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, cudaStream_t stream) {
-  const int prep_blocks = std::max(1, std::min(div_up(sp.total_groups * 32, 256), 1024));
-  prep_kernel<MODE, MAXMAT><<<prep_blocks, 256, 0, stream>>>(sp);
-  if (cudaGetLastError() != cudaSuccess) return W4G128_ERR_CUDA;
-
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(cta_warps * 32);
-  cfg.dynamicSmemBytes = smem_bytes<MODE>();
-  cfg.stream = stream;
+  // Every kernel of the call is a programmatic dependent launch: the prep
+  // kernel behind whatever precedes it in the stream (it waits for that to
+  // finish before touching anything), the streaming kernel behind the prep
+  // kernel (its weight copies start before it waits), the reduce kernel
+  // behind the streaming kernel.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, stream_kernel<MODE, MAXMAT>, sp) != cudaSuccess) {
+  cfg.gridDim = dim3(std::max(1, std::min(div_up(sp.total_groups * 32, 256), 1024)));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  if (cudaLaunchKernelEx(&cfg, prep_kernel<MODE, MAXMAT>, sp) != cudaSuccess) {
+    cudaGetLastError();
+    return W4G128_ERR_CUDA;
+  }
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(cta_warps * 32);
+  cfg.dynamicSmemBytes = smem_bytes<MODE>();
+  if (cudaLaunchKernelEx(&cfg, stream_kernel<MODE, MAXMAT, NORM>, sp) != cudaSuccess) {
     cudaGetLastError();
     return W4G128_ERR_CUDA;
   }
   if (MODE != kMMA) return W4G128_OK;  // M = 1: split quads are folded inside the streaming kernel
   cfg.gridDim = dim3(static_cast<unsigned>(sp.total_quads));  // one CTA per quad
-  cfg.blockDim = dim3(kRedThreads);
+  cfg.blockDim = dim3(NORM ? kNormThreads : kRedThreads);
   cfg.dynamicSmemBytes = kRedSmem;
-  if (cudaLaunchKernelEx(&cfg, reduce_kernel<MAXMAT>, sp) != cudaSuccess) {
+  if (NORM) {  // room to stage h and gamma for the norm, when they fit
+    const long long stage = 2LL * sp.mats[0].N * (sp.M + 1);
+    if (stage <= kNormStageMax) cfg.dynamicSmemBytes = kRedSmem + static_cast<int>(stage);
+  }
+  if (cudaLaunchKernelEx(&cfg, reduce_kernel<MAXMAT, NORM>, sp) != cudaSuccess) {
     cudaGetLastError();
     return W4G128_ERR_CUDA;
   }
@@ -1064,12 +1311,20 @@ int launch_mode(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, cudaStr
 }
 
 template <int MAXMAT>
-int launch_with(const HostMatrix* mats, int count, int M, const Plan& pl, void* ws, cudaStream_t stream) {
+int launch_with(const HostMatrix* mats, int count, int M, const Plan& pl, const NormArgs* norm, void* ws,
+                cudaStream_t stream) {
   static thread_local StreamParams<MAXMAT> sp;  // large for MAXMAT = 512: keep it off the stack
-  fill_params(sp, mats, count, M, pl, ws);
-  if (pl.mode == kMMA) return launch_mode<kMMA>(sp, pl.grid, pl.cta_warps, stream);
-  if (pl.mode == kMMA1) return launch_mode<kMMA1>(sp, pl.grid, pl.cta_warps, stream);
-  return launch_mode<kM1>(sp, pl.grid, pl.cta_warps, stream);
+  fill_params(sp, mats, count, M, pl, norm, ws);
+  if constexpr (MAXMAT == 1) {
+    if (norm != nullptr) {
+      if (pl.mode == kMMA) return launch_mode<kMMA, 1, true>(sp, pl.grid, pl.cta_warps, stream);
+      if (pl.mode == kMMA1) return launch_mode<kMMA1, 1, true>(sp, pl.grid, pl.cta_warps, stream);
+      return launch_mode<kM1, 1, true>(sp, pl.grid, pl.cta_warps, stream);
+    }
+  }
+  if (pl.mode == kMMA) return launch_mode<kMMA, MAXMAT, false>(sp, pl.grid, pl.cta_warps, stream);
+  if (pl.mode == kMMA1) return launch_mode<kMMA1, MAXMAT, false>(sp, pl.grid, pl.cta_warps, stream);
+  return launch_mode<kM1, MAXMAT, false>(sp, pl.grid, pl.cta_warps, stream);
 }
 
 }  // namespace
@@ -1087,15 +1342,16 @@ size_t stream_workspace_bytes(const HostMatrix* mats, int count, int M, bool ver
   return pl.bytes;
 }
 
-int launch_stream(const HostMatrix* mats, int count, int M, bool verify, void* ws, size_t ws_bytes,
-                  cudaStream_t stream) {
+int launch_stream(const HostMatrix* mats, int count, int M, bool verify, const NormArgs* norm, void* ws,
+                  size_t ws_bytes, cudaStream_t stream) {
   const DeviceInfo* d = device_info();
   if (d == nullptr || !d->ok) return W4G128_ERR_DEVICE;
   Plan pl;
   if (!make_plan(mats, count, M, verify, *d, pl)) return W4G128_ERR_SHAPE;
   if (ws_bytes < pl.bytes) return W4G128_ERR_WORKSPACE;
-  if (count == 1) return launch_with<1>(mats, count, M, pl, ws, stream);
-  return launch_with<W4G128_MAX_MATRICES>(mats, count, M, pl, ws, stream);
+  if (norm != nullptr && count != 1) return W4G128_ERR_INVALID_ARG;
+  if (count == 1) return launch_with<1>(mats, count, M, pl, norm, ws, stream);
+  return launch_with<W4G128_MAX_MATRICES>(mats, count, M, pl, norm, ws, stream);
 }
 
 int read_workspace_status(const void* ws, int* status_out, cudaStream_t stream) {

@@ -12,6 +12,10 @@ Workload recipe (one matrix of shape K x N, M activation rows):
   mins   bf16   [K/128][N]  -8 * scale * (1 + U(-0.1, 0.1)) rounded to bf16
   x      bf16   [M][K]      N(0, 1) rounded to bf16
 Each (seed, matrix_id) pair names independent streams for the four arrays.
+
+For the residual add + RMS norm call: the residual [M][N] is drawn like x
+(N(0, 1), its own stream id) and the norm weight gamma [N] is
+1 + 0.25 N(0, 1), cut to bf16 (norm_weight).
 """
 import ctypes
 import os
@@ -140,3 +144,10 @@ def fill_device(seed, matrix_id, K, N, codes_ptr, scales_ptr, mins_ptr, stream=0
     rc = lib.synth_dev_meta(seed, matrix_id, (K // 128) * N, scales_ptr, mins_ptr, stream)
     if rc != 0:
         raise RuntimeError(f"synth_dev_meta failed with CUDA error {rc}")
+
+
+def norm_weight(seed, stream_id, N):
+    """RMS-norm weight gamma [N] as bf16 bits: 1 + 0.25 N(0, 1), truncated to bf16."""
+    z = x(seed, stream_id, 1, N)[0].astype(np.uint32) << 16
+    g = (1.0 + 0.25 * z.view(np.float32).astype(np.float64)).astype(np.float32)
+    return (g.view(np.uint32) >> 16).astype(np.uint16)

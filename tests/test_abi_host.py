@@ -17,7 +17,7 @@ def L():
 
 def test_every_header_symbol_is_exported(L):
     names = w.exported_symbols()
-    assert len(names) == 16
+    assert len(names) == 17
     for n in names:
         assert hasattr(L, n), n
 
@@ -55,6 +55,31 @@ def test_gemv_argument_errors(L):
 def test_verify_argument_errors(L):
     for M in (0, 9, -1):
         assert L.w4g128_gemm_verify(FAKE, FAKE, FAKE, M, 128, 16, FAKE, 1 << 20, None) == E_INVALID
+
+
+def test_add_rmsnorm_argument_errors(L):
+    F, G, H, O, R = FAKE, FAKE + 0x1000, FAKE + 0x2000, FAKE + 0x3000, FAKE + 0x4000
+
+    def call(packed=F, x=F + 0x800, res=R, gam=G, eps=1e-6, h=H, out=O, M=1, K=128, N=16, verify=0, ws=F):
+        return L.w4g128_gemm_add_rmsnorm(packed, x, res, gam, eps, h, out, M, K, N, verify, ws, 1 << 20, None)
+
+    assert call(res=None) == E_INVALID
+    assert call(gam=None) == E_INVALID
+    assert call(out=None) == E_INVALID
+    assert call(h=None) == E_INVALID
+    assert call(eps=-1.0) == E_INVALID
+    assert call(eps=float("nan")) == E_INVALID
+    assert call(eps=float("inf")) == E_INVALID
+    assert call(verify=2) == E_INVALID
+    assert call(out=H) == E_INVALID          # out is h
+    assert call(out=R) == E_INVALID          # out is the residual
+    assert call(x=H) == E_INVALID            # h is x
+    assert call(M=9) == E_INVALID
+    assert call(N=24) == E_SHAPE
+    assert call(gam=G + 2) == E_ALIGN
+    assert call(res=R + 2) == E_ALIGN
+    assert call(out=O + 2) == E_ALIGN
+    assert call(h=H + 2) == E_ALIGN
 
 
 def test_decode_step_argument_errors(L):
@@ -96,6 +121,8 @@ def test_no_device_is_reported_not_faked():
     L = w.lib()
     assert L.w4g128_gemv(FAKE, FAKE, FAKE, 128, 16, FAKE, 1 << 20, None) == E_DEVICE
     assert L.w4g128_pack(FAKE, FAKE, FAKE, 128, 16, FAKE, None) == E_DEVICE
+    assert L.w4g128_gemm_add_rmsnorm(FAKE, FAKE + 0x800, FAKE + 0x1000, FAKE + 0x2000, 1e-6, FAKE + 0x1000,
+                                     FAKE + 0x3000, 1, 128, 16, 0, FAKE, 1 << 20, None) == E_DEVICE
     assert w.w4g128_workspace_bytes(1, 128, 16) == 0
 
 
