@@ -339,11 +339,18 @@ __device__ __forceinline__ uint16_t emit(const StreamParams<MAXMAT>& p, long lon
   return to_bf16(v);
 }
 
-// Elements i, i + 1 (i even) as one 32-bit word.
+// The residual's elements i, i + 1 (i even) as one 32-bit word (0 without
+// the norm); loaded ahead of the sums it is added to.
 template <bool NORM, int MAXMAT>
-__device__ __forceinline__ uint32_t emit2(const StreamParams<MAXMAT>& p, long long i, float a, float b) {
+__device__ __forceinline__ uint32_t residual2(const StreamParams<MAXMAT>& p, long long i) {
+  if constexpr (NORM) return *reinterpret_cast<const uint32_t*>(p.residual + i);
+  else return 0u;
+}
+
+// Elements i, i + 1 as one 32-bit word, given residual2 of them.
+template <bool NORM>
+__device__ __forceinline__ uint32_t emit2(float a, float b, uint32_t r) {
   if constexpr (NORM) {
-    const uint32_t r = *reinterpret_cast<const uint32_t*>(p.residual + i);
     a = __fadd_rn(a, bf16_lo(r));
     b = __fadd_rn(b, bf16_hi(r));
   }
@@ -463,107 +470,87 @@ __device__ __forceinline__ float pick(const float (&v)[kQuadTiles][NA], int t, i
 //   out[m][n] = bf16( fl(fl(h[m][n] r_m) gamma[n]) ),
 //   r_m = 1 / sqrt( fl(S_m / N) + eps )   (one correctly rounded fp32 op each),
 // with S_m = sum_n h[m][n]^2 summed in an order fixed by N alone, not by the
-// CTA's size: the row's N/2 bf16 pairs are dealt round robin to 256 logical
-// lanes; a lane folds lo^2 then hi^2 of each of its pairs, in order, with
-// fp32 FMAs; a xor butterfly adds each strand of 32 lanes; the 8 strand sums
-// are added as a balanced tree.
+// CTA's size: the row is cut into 8-column chunks, dealt round robin to 256
+// logical lanes (chunk j to lane j mod 256); a lane folds the squares of its
+// chunks' columns in column order with fp32 FMAs; a xor butterfly adds each
+// strand of 32 lanes; the 8 strand sums are added as a balanced tree.
 constexpr int kNormLanes = 256;                // logical lanes per row
 constexpr int kNormStrands = kNormLanes / 32;  // 8
-constexpr int kNormBatch = 4;                  // logical lanes a thread serves side by side
-constexpr int kNormChunk = 8;                  // pairs per logical lane loaded at once (sum of squares)
-constexpr int kNormChunk2 = 4;                 // the same for the output pass
 constexpr int kNormThreads = 512;              // threads of the reduce kernel when it ends in the norm
 constexpr int kNormStageMax = 160 * 1024;      // largest h + gamma the reduce kernel stages in shared memory
 
+// One 8-column chunk (4 words of bf16 pairs): a 16-byte load from the staged
+// copy in shared memory, or four 4-byte loads through L2 (h was written by
+// other CTAs of this grid; global rows need only 4-byte alignment).
 template <bool SMEM>
-__device__ __forceinline__ uint32_t norm_ld(const uint32_t* a) {
-  if constexpr (SMEM) return *a;
-  else return __ldcg(a);  // written by other CTAs of this grid: read through L2
+__device__ __forceinline__ uint4 norm_chunk(const uint32_t* a) {
+  if constexpr (SMEM) return *reinterpret_cast<const uint4*>(a);
+  else return make_uint4(__ldcg(a), __ldcg(a + 1), __ldcg(a + 2), __ldcg(a + 3));
+}
+
+__device__ __forceinline__ float sq_word(uint32_t v, float acc) {
+  acc = fmaf(bf16_lo(v), bf16_lo(v), acc);
+  return fmaf(bf16_hi(v), bf16_hi(v), acc);
+}
+
+// out word = bf16 pair of (h * r) * g, element by element
+__device__ __forceinline__ uint32_t norm_word(uint32_t h, uint32_t g, float r) {
+  const float2 v = fmul2(fmul2(make_float2(bf16_lo(h), bf16_hi(h)), make_float2(r, r)),
+                         make_float2(bf16_lo(g), bf16_hi(g)));
+  uint32_t o;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o) : "f"(v.y), "f"(v.x));  // (hi, lo)
+  return o;
 }
 
 // The two passes over h (words of bf16 pairs, row-major [M][N/2]) and gamma
-// ([N/2]): from global memory, or (SMEM) from the copies staged in shared
-// memory.  Both read the same words in the same order, so they give the
-// same bits.  From global memory the time is L2 round trips, so each thread
-// issues the loads of kNormBatch logical lanes x a chunk of pairs before it
-// consumes any (absent pairs read as 0, which adds exactly nothing).
+// ([N/2]): from the copies staged in shared memory (SMEM), or from global
+// memory; both fold the same values in the same order, so they give the
+// same bits.  Thread t serves logical lanes t, t + nt, ...; nt and M * 256
+// are multiples of 32, so the 32 logical lanes of a strand sit in one warp.
+// The output pass is elementwise: thread t writes chunks t, t + nt, ....
 template <bool SMEM, int MAXMAT>
 __device__ void norm_passes(const StreamParams<MAXMAT>& p, float* ss, const uint32_t* h, const uint32_t* gam) {
   const MatParams& m = p.mats[0];
-  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31;  // nt: a multiple of 32
-  const int npairs = m.N >> 1, nll = p.M * kNormLanes;
-  for (int base = 0; base < nll; base += kNormBatch * nt) {
-    float acc[kNormBatch];
-#pragma unroll
-    for (int j = 0; j < kNormBatch; ++j) acc[j] = 0.f;
-    for (int k0 = 0; k0 < npairs; k0 += kNormChunk * kNormLanes) {
-      uint32_t v[kNormBatch][kNormChunk];
-#pragma unroll
-      for (int j = 0; j < kNormBatch; ++j) {
-        const int ll = base + j * nt + tid;
-        const long long row0 = static_cast<long long>(ll / kNormLanes) * npairs;
-#pragma unroll
-        for (int c = 0; c < kNormChunk; ++c) {
-          const int pi = (ll & (kNormLanes - 1)) + k0 + c * kNormLanes;
-          v[j][c] = (ll < nll && pi < npairs) ? norm_ld<SMEM>(h + row0 + pi) : 0u;
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < kNormBatch; ++j)
-#pragma unroll
-        for (int c = 0; c < kNormChunk; ++c) {
-          acc[j] = fmaf(bf16_lo(v[j][c]), bf16_lo(v[j][c]), acc[j]);
-          acc[j] = fmaf(bf16_hi(v[j][c]), bf16_hi(v[j][c]), acc[j]);
-        }
+  const int nt = blockDim.x, lane = threadIdx.x & 31;
+  const int npairs = m.N >> 1, nchunk = npairs >> 2, nll = p.M * kNormLanes;
+  for (int ll = threadIdx.x; ll < nll; ll += nt) {
+    const uint32_t* hr = h + static_cast<long long>(ll / kNormLanes) * npairs;
+    float acc = 0.f;
+#pragma unroll 4
+    for (int j = ll & (kNormLanes - 1); j < nchunk; j += kNormLanes) {
+      const uint4 v = norm_chunk<SMEM>(hr + 4 * j);
+      acc = sq_word(v.w, sq_word(v.z, sq_word(v.y, sq_word(v.x, acc))));
     }
 #pragma unroll
-    for (int j = 0; j < kNormBatch; ++j) {
-      float v = acc[j];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      const int ll = base + j * nt + tid;
-      if (lane == 0 && ll < nll) ss[ll >> 5] = v;
-    }
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) ss[ll >> 5] = acc;
   }
   __syncthreads();
+  if (threadIdx.x < p.M) {  // r_m, kept in the first strand slot of its row
+    const float* r = ss + threadIdx.x * kNormStrands;
+    const float S = ((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7]));
+    ss[W4G128_MAX_M * kNormStrands + threadIdx.x] = __frsqrt_rn(__fadd_rn(__fdiv_rn(S, static_cast<float>(m.N)), p.eps));
+  }
+  __syncthreads();
+  const float* rs = ss + W4G128_MAX_M * kNormStrands;
   uint32_t* out = reinterpret_cast<uint32_t*>(p.nout);
-  for (int base = 0; base < nll; base += kNormBatch * nt) {
-    float rs[kNormBatch];
-#pragma unroll
-    for (int j = 0; j < kNormBatch; ++j) {
-      const int ll = min(base + j * nt + tid, nll - 1);
-      const float* r = ss + (ll / kNormLanes) * kNormStrands;
-      const float S = ((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7]));
-      rs[j] = __frsqrt_rn(__fadd_rn(__fdiv_rn(S, static_cast<float>(m.N)), p.eps));
-    }
-    for (int k0 = 0; k0 < npairs; k0 += kNormChunk2 * kNormLanes) {
-      uint32_t hv[kNormBatch][kNormChunk2], gv[kNormBatch][kNormChunk2];
-#pragma unroll
-      for (int j = 0; j < kNormBatch; ++j) {
-        const int ll = base + j * nt + tid;
-        const long long row0 = static_cast<long long>(ll / kNormLanes) * npairs;
-#pragma unroll
-        for (int c = 0; c < kNormChunk2; ++c) {
-          const int pi = (ll & (kNormLanes - 1)) + k0 + c * kNormLanes;
-          const bool in = ll < nll && pi < npairs;
-          hv[j][c] = in ? norm_ld<SMEM>(h + row0 + pi) : 0u;
-          gv[j][c] = in ? norm_ld<SMEM>(gam + pi) : 0u;
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < kNormBatch; ++j) {
-        const int ll = base + j * nt + tid;
-        const long long row0 = static_cast<long long>(ll / kNormLanes) * npairs;
-#pragma unroll
-        for (int c = 0; c < kNormChunk2; ++c) {
-          const int pi = (ll & (kNormLanes - 1)) + k0 + c * kNormLanes;
-          if (ll < nll && pi < npairs) {
-            const float a = __fmul_rn(__fmul_rn(bf16_lo(hv[j][c]), rs[j]), bf16_lo(gv[j][c]));
-            const float b = __fmul_rn(__fmul_rn(bf16_hi(hv[j][c]), rs[j]), bf16_hi(gv[j][c]));
-            out[row0 + pi] = static_cast<uint32_t>(to_bf16(a)) | (static_cast<uint32_t>(to_bf16(b)) << 16);
-          }
-        }
-      }
+  const bool vec = (reinterpret_cast<uintptr_t>(out) & 15u) == 0u;
+  const long long total = static_cast<long long>(p.M) * nchunk;
+#pragma unroll 2
+  for (long long c = threadIdx.x; c < total; c += nt) {
+    const int row = static_cast<int>(c / nchunk), j = static_cast<int>(c - static_cast<long long>(row) * nchunk);
+    const uint4 v = norm_chunk<SMEM>(h + 4 * c);
+    const uint4 g = norm_chunk<SMEM>(gam + 4 * j);
+    const float r = rs[row];
+    const uint4 o = make_uint4(norm_word(v.x, g.x, r), norm_word(v.y, g.y, r), norm_word(v.z, g.z, r),
+                               norm_word(v.w, g.w, r));
+    if (vec) {
+      *reinterpret_cast<uint4*>(out + 4 * c) = o;
+    } else {
+      out[4 * c] = o.x;
+      out[4 * c + 1] = o.y;
+      out[4 * c + 2] = o.z;
+      out[4 * c + 3] = o.w;
     }
   }
 }
@@ -574,14 +561,25 @@ __device__ __forceinline__ uint32_t dynamic_smem_bytes() {
   return v;
 }
 
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+template <int BYTES>
+__device__ __forceinline__ void cp_async(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(dst), "l"(src), "n"(BYTES) : "memory");
+}
+
+// Copies `words` 32-bit words from global to shared memory with asynchronous
+// copies, 16 bytes at a time when both ends allow it.
+__device__ __forceinline__ void stage_words(uint32_t dst, const uint32_t* src, long long words) {
+  if (((dst | static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src))) & 15u) == 0u && (words & 3) == 0) {
+    for (long long i = threadIdx.x; 4 * i < words; i += blockDim.x) cp_async<16>(dst + 16u * i, src + 4 * i);
+  } else {
+    for (long long i = threadIdx.x; i < words; i += blockDim.x) cp_async<4>(dst + 4u * i, src + i);
+  }
 }
 
 // The norm, run by the last CTA.  When h and gamma fit in the `stage` bytes
-// of shared memory the CTA holds free, they are copied there first with
-// 4-byte asynchronous copies (every word in flight at once: one L2 round
-// trip), and both passes read shared memory; otherwise both read L2.
+// of shared memory the CTA holds free, they are staged there first (every
+// copy in flight at once: one L2 round trip) and both passes read shared
+// memory; otherwise both read L2.
 template <int MAXMAT>
 __device__ void norm_rows(const StreamParams<MAXMAT>& p, float* ss, uint8_t* stage, uint32_t stage_bytes) {
   const MatParams& m = p.mats[0];
@@ -594,10 +592,9 @@ __device__ void norm_rows(const StreamParams<MAXMAT>& p, float* ss, uint8_t* sta
     return;
   }
   uint32_t* sh = reinterpret_cast<uint32_t*>(stage);
-  uint32_t* sg = sh + hwords;
-  const uint32_t sh0 = smem_addr(sh), sg0 = smem_addr(sg);
-  for (int i = threadIdx.x; i < hwords; i += blockDim.x) cp_async4(sh0 + 4u * i, h + i);
-  for (int i = threadIdx.x; i < npairs; i += blockDim.x) cp_async4(sg0 + 4u * i, gam + i);
+  uint32_t* sg = sh + hwords;  // hwords is a multiple of 8: 16-byte aligned when stage is
+  stage_words(smem_addr(sh), h, hwords);
+  stage_words(smem_addr(sg), gam, npairs);
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
   __syncthreads();
   norm_passes<true>(p, ss, sh, sg);
@@ -612,7 +609,7 @@ __device__ void norm_rows(const StreamParams<MAXMAT>& p, float* ss, uint8_t* sta
 template <int MAXMAT>
 __device__ __forceinline__ void norm_arrive(const StreamParams<MAXMAT>& p, uint8_t* stage, uint32_t stage_bytes) {
   __shared__ int last;
-  __shared__ float ss[W4G128_MAX_M * kNormStrands];
+  __shared__ float ss[W4G128_MAX_M * (kNormStrands + 1)];  // strand sums, then r_m
   __syncthreads();
   if (threadIdx.x == 0) {
     grid_dependency_wait();  // the counter was cleared by the prep kernel
@@ -894,6 +891,8 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
     const long long first = I * (owner_of(q_first, I, p.W) + 1) / p.W - 1;
     const int nslot = static_cast<int>(q_first + S - first);
     const float4* part = reinterpret_cast<const float4*>(p.partials + first * 64 + col);
+    const int i = kQuadTiles * kTileN * q + col;
+    const uint32_t r0 = residual2<NORM>(p, i), r1 = residual2<NORM>(p, i + 2);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = 0; s0 < nslot; s0 += 8) {  // 8 slots in flight, then fold in order
       float4 v[8];
@@ -911,10 +910,9 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
         }
       }
     }
-    const int i = kQuadTiles * kTileN * q + col;
     uint32_t* yo = reinterpret_cast<uint32_t*>(m.y + i);
-    yo[0] = emit2<NORM>(p, i, acc.x, acc.y);
-    yo[1] = emit2<NORM>(p, i + 2, acc.z, acc.w);
+    yo[0] = emit2<NORM>(acc.x, acc.y, r0);
+    yo[1] = emit2<NORM>(acc.z, acc.w, r1);
   }
   // The rings are drained: the dynamic shared memory after the mbarriers can
   // stage the norm.
@@ -1086,6 +1084,12 @@ __global__ void __launch_bounds__(kNormThreads) reduce_kernel(const __grid_const
   }
   const int u = threadIdx.x, row = u >> 4, col = 4 * (u & 15);
   const bool active = row < p.M && col < kTileN * min(kQuadTiles, T - kQuadTiles * q);
+  const long long i = static_cast<long long>(row) * m.N + kQuadTiles * kTileN * q + col;
+  uint32_t r0 = 0u, r1 = 0u;  // the residual, loaded while the partials are in flight
+  if (active) {
+    r0 = residual2<NORM>(p, i);
+    r1 = residual2<NORM>(p, i + 2);
+  }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int ch = 0; ch < nchunks; ++ch) {
     if (threadIdx.x == 0) {
@@ -1118,10 +1122,9 @@ __global__ void __launch_bounds__(kNormThreads) reduce_kernel(const __grid_const
     }
   }
   if (active) {
-    const long long i = static_cast<long long>(row) * m.N + kQuadTiles * kTileN * q + col;
     uint32_t* yo = reinterpret_cast<uint32_t*>(m.y + i);
-    yo[0] = emit2<NORM>(p, i, acc.x, acc.y);
-    yo[1] = emit2<NORM>(p, i + 2, acc.z, acc.w);
+    yo[0] = emit2<NORM>(acc.x, acc.y, r0);
+    yo[1] = emit2<NORM>(acc.z, acc.w, r1);
   }
   if constexpr (NORM) norm_arrive(p, rsm + kRedSmem, dynamic_smem_bytes() - kRedSmem);
 }
