@@ -213,8 +213,10 @@ W4G128_API int w4g128_verify_step(const w4g128_matrix* mats, int count, int M, v
  * bit that call's y.  The norm reads the rounded h (the value the residual
  * stream keeps): mean_n h^2 is summed in fp32 in an order fixed by N alone,
  * and every step after it is one correctly rounded fp32 operation, so out is
- * deterministic.  No pass of its own: the last CTA of the call's final kernel
- * normalises the rows.
+ * deterministic.  The residual add happens where the split-K sums are
+ * folded; one small kernel, launched behind the product's kernels, then
+ * normalises the rows.  If the call's status word reports an error, out is
+ * left unwritten.
  *   x [M][K], residual, h, out [M][N], gamma [N]: bf16, device, row-major,
  *   caller-owned; 1 <= M <= W4G128_MAX_M.  h may be the residual itself
  *   (updated in place); out must not overlap x, residual or h

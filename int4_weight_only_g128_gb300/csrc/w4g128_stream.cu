@@ -144,10 +144,9 @@ struct StreamParams {
   float* partials;       // [total_items][rows][64]: one slot per (matrix, quad, segment)
   unsigned* tickets;     // [total_quads] arrival counters (M = 1)
   unsigned* status;
-  unsigned* done;        // CTAs finished (the residual add + RMS norm call)
   // The residual add + RMS norm call (one matrix; residual == nullptr
-  // otherwise): its y is h = residual + x W, and the last CTA to finish
-  // writes out = gamma h / rms(h).
+  // otherwise): its y is h = residual + x W, and the norm kernel writes
+  // out = gamma h / rms(h).
   const uint16_t* residual;
   const uint16_t* gamma;
   uint16_t* nout;
@@ -463,164 +462,6 @@ __device__ __forceinline__ float pick(const float (&v)[kQuadTiles][NA], int t, i
   return out;
 }
 
-// ----------------------------------------------------------------- RMS norm of the finished rows
-
-// The residual add + RMS norm call ends in one CTA, the last of the final
-// grid to finish, normalising every row m of h (the matrix's y) into out:
-//   out[m][n] = bf16( fl(fl(h[m][n] r_m) gamma[n]) ),
-//   r_m = 1 / sqrt( fl(S_m / N) + eps )   (one correctly rounded fp32 op each),
-// with S_m = sum_n h[m][n]^2 summed in an order fixed by N alone, not by the
-// CTA's size: the row is cut into 8-column chunks, dealt round robin to 256
-// logical lanes (chunk j to lane j mod 256); a lane folds the squares of its
-// chunks' columns in column order with fp32 FMAs; a xor butterfly adds each
-// strand of 32 lanes; the 8 strand sums are added as a balanced tree.
-constexpr int kNormLanes = 256;                // logical lanes per row
-constexpr int kNormStrands = kNormLanes / 32;  // 8
-constexpr int kNormThreads = 512;              // threads of the reduce kernel when it ends in the norm
-constexpr int kNormStageMax = 160 * 1024;      // largest h + gamma the reduce kernel stages in shared memory
-
-// One 8-column chunk (4 words of bf16 pairs): a 16-byte load from the staged
-// copy in shared memory, or four 4-byte loads through L2 (h was written by
-// other CTAs of this grid; global rows need only 4-byte alignment).
-template <bool SMEM>
-__device__ __forceinline__ uint4 norm_chunk(const uint32_t* a) {
-  if constexpr (SMEM) return *reinterpret_cast<const uint4*>(a);
-  else return make_uint4(__ldcg(a), __ldcg(a + 1), __ldcg(a + 2), __ldcg(a + 3));
-}
-
-__device__ __forceinline__ float sq_word(uint32_t v, float acc) {
-  acc = fmaf(bf16_lo(v), bf16_lo(v), acc);
-  return fmaf(bf16_hi(v), bf16_hi(v), acc);
-}
-
-// out word = bf16 pair of (h * r) * g, element by element
-__device__ __forceinline__ uint32_t norm_word(uint32_t h, uint32_t g, float r) {
-  const float2 v = fmul2(fmul2(make_float2(bf16_lo(h), bf16_hi(h)), make_float2(r, r)),
-                         make_float2(bf16_lo(g), bf16_hi(g)));
-  uint32_t o;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o) : "f"(v.y), "f"(v.x));  // (hi, lo)
-  return o;
-}
-
-// The two passes over h (words of bf16 pairs, row-major [M][N/2]) and gamma
-// ([N/2]): from the copies staged in shared memory (SMEM), or from global
-// memory; both fold the same values in the same order, so they give the
-// same bits.  Thread t serves logical lanes t, t + nt, ...; nt and M * 256
-// are multiples of 32, so the 32 logical lanes of a strand sit in one warp.
-// The output pass is elementwise: thread t writes chunks t, t + nt, ....
-template <bool SMEM, int MAXMAT>
-__device__ void norm_passes(const StreamParams<MAXMAT>& p, float* ss, const uint32_t* h, const uint32_t* gam) {
-  const MatParams& m = p.mats[0];
-  const int nt = blockDim.x, lane = threadIdx.x & 31;
-  const int npairs = m.N >> 1, nchunk = npairs >> 2, nll = p.M * kNormLanes;
-  for (int ll = threadIdx.x; ll < nll; ll += nt) {
-    const uint32_t* hr = h + static_cast<long long>(ll / kNormLanes) * npairs;
-    float acc = 0.f;
-#pragma unroll 4
-    for (int j = ll & (kNormLanes - 1); j < nchunk; j += kNormLanes) {
-      const uint4 v = norm_chunk<SMEM>(hr + 4 * j);
-      acc = sq_word(v.w, sq_word(v.z, sq_word(v.y, sq_word(v.x, acc))));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) ss[ll >> 5] = acc;
-  }
-  __syncthreads();
-  if (threadIdx.x < p.M) {  // r_m, kept in the first strand slot of its row
-    const float* r = ss + threadIdx.x * kNormStrands;
-    const float S = ((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7]));
-    ss[W4G128_MAX_M * kNormStrands + threadIdx.x] = __frsqrt_rn(__fadd_rn(__fdiv_rn(S, static_cast<float>(m.N)), p.eps));
-  }
-  __syncthreads();
-  const float* rs = ss + W4G128_MAX_M * kNormStrands;
-  uint32_t* out = reinterpret_cast<uint32_t*>(p.nout);
-  const bool vec = (reinterpret_cast<uintptr_t>(out) & 15u) == 0u;
-  const long long total = static_cast<long long>(p.M) * nchunk;
-#pragma unroll 2
-  for (long long c = threadIdx.x; c < total; c += nt) {
-    const int row = static_cast<int>(c / nchunk), j = static_cast<int>(c - static_cast<long long>(row) * nchunk);
-    const uint4 v = norm_chunk<SMEM>(h + 4 * c);
-    const uint4 g = norm_chunk<SMEM>(gam + 4 * j);
-    const float r = rs[row];
-    const uint4 o = make_uint4(norm_word(v.x, g.x, r), norm_word(v.y, g.y, r), norm_word(v.z, g.z, r),
-                               norm_word(v.w, g.w, r));
-    if (vec) {
-      *reinterpret_cast<uint4*>(out + 4 * c) = o;
-    } else {
-      out[4 * c] = o.x;
-      out[4 * c + 1] = o.y;
-      out[4 * c + 2] = o.z;
-      out[4 * c + 3] = o.w;
-    }
-  }
-}
-
-__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
-  uint32_t v;
-  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(v));
-  return v;
-}
-
-template <int BYTES>
-__device__ __forceinline__ void cp_async(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(dst), "l"(src), "n"(BYTES) : "memory");
-}
-
-// Copies `words` 32-bit words from global to shared memory with asynchronous
-// copies, 16 bytes at a time when both ends allow it.
-__device__ __forceinline__ void stage_words(uint32_t dst, const uint32_t* src, long long words) {
-  if (((dst | static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src))) & 15u) == 0u && (words & 3) == 0) {
-    for (long long i = threadIdx.x; 4 * i < words; i += blockDim.x) cp_async<16>(dst + 16u * i, src + 4 * i);
-  } else {
-    for (long long i = threadIdx.x; i < words; i += blockDim.x) cp_async<4>(dst + 4u * i, src + i);
-  }
-}
-
-// The norm, run by the last CTA.  When h and gamma fit in the `stage` bytes
-// of shared memory the CTA holds free, they are staged there first (every
-// copy in flight at once: one L2 round trip) and both passes read shared
-// memory; otherwise both read L2.
-template <int MAXMAT>
-__device__ void norm_rows(const StreamParams<MAXMAT>& p, float* ss, uint8_t* stage, uint32_t stage_bytes) {
-  const MatParams& m = p.mats[0];
-  const int npairs = m.N >> 1;
-  const uint32_t* h = reinterpret_cast<const uint32_t*>(m.y);
-  const uint32_t* gam = reinterpret_cast<const uint32_t*>(p.gamma);
-  const long long hwords = static_cast<long long>(p.M) * npairs;
-  if ((hwords + npairs) * 4 > static_cast<long long>(stage_bytes)) {
-    norm_passes<false>(p, ss, h, gam);
-    return;
-  }
-  uint32_t* sh = reinterpret_cast<uint32_t*>(stage);
-  uint32_t* sg = sh + hwords;  // hwords is a multiple of 8: 16-byte aligned when stage is
-  stage_words(smem_addr(sh), h, hwords);
-  stage_words(smem_addr(sg), gam, npairs);
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-  __syncthreads();
-  norm_passes<true>(p, ss, sh, sg);
-}
-
-// Every thread of every CTA of the call's final grid calls this after its last
-// write of h; the CTA that arrives last runs the norm (unless the call's
-// status word reports an error: out is then left unwritten).  No CTA waits
-// here.  Publication follows the barrier-then-release pattern: the CTA's
-// writes are ordered before thread 0's release by the barrier, and the last
-// CTA's reads after thread 0's acquire by the barrier that follows it.
-template <int MAXMAT>
-__device__ __forceinline__ void norm_arrive(const StreamParams<MAXMAT>& p, uint8_t* stage, uint32_t stage_bytes) {
-  __shared__ int last;
-  __shared__ float ss[W4G128_MAX_M * (kNormStrands + 1)];  // strand sums, then r_m
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    grid_dependency_wait();  // the counter was cleared by the prep kernel
-    unsigned prev;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(p.done) : "memory");
-    last = (prev + 1u == gridDim.x) && (*reinterpret_cast<volatile unsigned*>(p.status) == 0u);
-  }
-  __syncthreads();
-  if (last) norm_rows(p, ss, stage, stage_bytes);
-}
-
 // ----------------------------------------------------------------- the streaming kernel
 
 template <int MODE, int MAXMAT, bool NORM>
@@ -914,9 +755,6 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
     yo[0] = emit2<NORM>(acc.x, acc.y, r0);
     yo[1] = emit2<NORM>(acc.z, acc.w, r1);
   }
-  // The rings are drained: the dynamic shared memory after the mbarriers can
-  // stage the norm.
-  if constexpr (NORM) norm_arrive(p, smem + kBarBytes, smem_bytes<MODE>() - kBarBytes);
 }
 
 // ----------------------------------------------------------------- prep kernel
@@ -937,10 +775,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Strea
   const int tid = blockIdx.x * blockDim.x + threadIdx.x, nthreads = gridDim.x * blockDim.x;
   if (MODE != kMMA)
     for (int i = tid; i < p.total_quads; i += nthreads) p.tickets[i] = 0u;
-  if (tid == 0) {
-    *p.status = 0u;
-    *p.done = 0u;
-  }
+  if (tid == 0) *p.status = 0u;
 
   constexpr int kRows = Pkg<MODE>::kRows;
   const int lane = threadIdx.x & 31;
@@ -1029,7 +864,7 @@ constexpr int kRedStageBytes = kRedChunk * kMaxRows * 64 * 4;  // 16 KB at M = 8
 constexpr int kRedSmem = 2 * kRedStageBytes + 16;          // two stages + two mbarriers
 
 template <int MAXMAT, bool NORM>
-__global__ void __launch_bounds__(kNormThreads) reduce_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
+__global__ void __launch_bounds__(kRedThreads) reduce_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
   extern __shared__ __align__(128) uint8_t rsm[];
   __shared__ int ok;
   const int gq = blockIdx.x;
@@ -1050,7 +885,6 @@ __global__ void __launch_bounds__(kNormThreads) reduce_kernel(const __grid_const
   grid_dependents_launch();
   if (wf == owner_of(q_first + S - 1, I, p.W)) {  // owned: y is written
     grid_dependency_wait();
-    if constexpr (NORM) norm_arrive(p, rsm + kRedSmem, dynamic_smem_bytes() - kRedSmem);
     return;
   }
   // Slots from the prefix run's last segment (which holds the fold of the
@@ -1126,7 +960,96 @@ __global__ void __launch_bounds__(kNormThreads) reduce_kernel(const __grid_const
     yo[0] = emit2<NORM>(acc.x, acc.y, r0);
     yo[1] = emit2<NORM>(acc.z, acc.w, r1);
   }
-  if constexpr (NORM) norm_arrive(p, rsm + kRedSmem, dynamic_smem_bytes() - kRedSmem);
+}
+
+// ----------------------------------------------------------------- RMS norm kernel
+
+// The residual add + RMS norm call ends in this kernel, launched behind the
+// call's last kernel (programmatic dependent launch): every h is written and
+// visible once it has waited.  One CTA per (row m, slice of kNormSlice 8-column
+// chunks) normalises its slice of row m:
+//   out[m][n] = bf16( fl(fl(h[m][n] r_m) gamma[n]) ),
+//   r_m = 1 / sqrt( fl(S_m / N) + eps )   (one correctly rounded fp32 op each),
+// with S_m = sum_n h[m][n]^2 summed in an order fixed by N alone: the row is
+// cut into 8-column chunks dealt round robin to the 256 threads (chunk j to
+// thread j mod 256); a thread folds the squares of its chunks' columns in
+// column order with fp32 FMAs; a xor butterfly adds each warp's 32 sums; the
+// 8 warp sums are added as a balanced tree.  Every CTA of a row computes the
+// same S_m from the whole row (a few KB from L2) and keeps the chunks of its
+// own slice in shared memory for the output pass.
+constexpr int kNormThreads = 256;
+constexpr int kNormSlice = 128;  // chunks (1024 columns) per CTA
+
+__device__ __forceinline__ float sq_word(uint32_t v, float acc) {
+  acc = fmaf(bf16_lo(v), bf16_lo(v), acc);
+  return fmaf(bf16_hi(v), bf16_hi(v), acc);
+}
+
+// out word = bf16 pair of (h * r) * g, element by element
+__device__ __forceinline__ uint32_t norm_word(uint32_t h, uint32_t g, float r) {
+  const float2 v = fmul2(fmul2(make_float2(bf16_lo(h), bf16_hi(h)), make_float2(r, r)),
+                         make_float2(bf16_lo(g), bf16_hi(g)));
+  uint32_t o;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o) : "f"(v.y), "f"(v.x));  // (hi, lo)
+  return o;
+}
+
+// 8 columns (4 words) at a: one 16-byte access when `vec`, else four 4-byte
+// ones (rows need only 4-byte alignment)
+__device__ __forceinline__ uint4 load_chunk(const uint32_t* a, bool vec) {
+  if (vec) return __ldcg(reinterpret_cast<const uint4*>(a));
+  return make_uint4(__ldcg(a), __ldcg(a + 1), __ldcg(a + 2), __ldcg(a + 3));
+}
+
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __grid_constant__ StreamParams<1> p) {
+  __shared__ uint4 mine[kNormSlice];
+  __shared__ float wsum[kNormThreads / 32];
+  __shared__ float r_row;
+  // The next call's prep kernel may launch now; it waits for this grid.
+  grid_dependents_launch();
+  grid_dependency_wait();
+  if (*reinterpret_cast<volatile unsigned*>(p.status) != 0u) return;  // the product failed: out left unwritten
+  const MatParams& m = p.mats[0];
+  const int row = blockIdx.y, j0 = blockIdx.x * kNormSlice, t = threadIdx.x;
+  const int npairs = m.N >> 1, nchunk = npairs >> 2;
+  const uint32_t* h = reinterpret_cast<const uint32_t*>(m.y) + static_cast<long long>(row) * npairs;
+  const uint32_t* gam = reinterpret_cast<const uint32_t*>(p.gamma);
+  uint32_t* out = reinterpret_cast<uint32_t*>(p.nout) + static_cast<long long>(row) * npairs;
+  // rows start 32-byte aligned relative to the base (N % 16 == 0): one test per array
+  const bool hvec = (reinterpret_cast<uintptr_t>(m.y) & 15u) == 0u;
+  const bool gvec = (reinterpret_cast<uintptr_t>(p.gamma) & 15u) == 0u;
+  const bool ovec = (reinterpret_cast<uintptr_t>(p.nout) & 15u) == 0u;
+  float acc = 0.f;
+#pragma unroll 4
+  for (int j = t; j < nchunk; j += kNormThreads) {
+    const uint4 v = load_chunk(h + 4 * j, hvec);
+    acc = sq_word(v.w, sq_word(v.z, sq_word(v.y, sq_word(v.x, acc))));
+    if (j >= j0 && j < j0 + kNormSlice) mine[j - j0] = v;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((t & 31) == 0) wsum[t >> 5] = acc;
+  __syncthreads();
+  if (t == 0) {
+    const float S = ((wsum[0] + wsum[1]) + (wsum[2] + wsum[3])) + ((wsum[4] + wsum[5]) + (wsum[6] + wsum[7]));
+    r_row = __frsqrt_rn(__fadd_rn(__fdiv_rn(S, static_cast<float>(m.N)), p.eps));
+  }
+  __syncthreads();
+  const int j = j0 + t;
+  if (t < kNormSlice && j < nchunk) {
+    const uint4 v = mine[t], g = load_chunk(gam + 4 * j, gvec);
+    const float r = r_row;
+    const uint4 o = make_uint4(norm_word(v.x, g.x, r), norm_word(v.y, g.y, r), norm_word(v.z, g.z, r),
+                               norm_word(v.w, g.w, r));
+    if (ovec) {
+      *reinterpret_cast<uint4*>(out + 4 * j) = o;
+    } else {
+      out[4 * j] = o.x;
+      out[4 * j + 1] = o.y;
+      out[4 * j + 2] = o.z;
+      out[4 * j + 3] = o.w;
+    }
+  }
 }
 
 // ----------------------------------------------------------------- host planning
@@ -1149,8 +1072,7 @@ void setup_mode(DeviceInfo& d) {
   cudaFuncSetAttribute(stream_kernel<MODE, W4G128_MAX_MATRICES, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        smem);
   cudaFuncSetAttribute(reduce_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRedSmem);
-  cudaFuncSetAttribute(reduce_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       kRedSmem + kNormStageMax);
+  cudaFuncSetAttribute(reduce_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRedSmem);
   cudaFuncSetAttribute(reduce_kernel<W4G128_MAX_MATRICES, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        kRedSmem);
   int occ1 = 0, occ2 = 0, occ3 = 0;
@@ -1246,7 +1168,6 @@ void fill_params(StreamParams<MAXMAT>& sp, const HostMatrix* mats, int count, in
   sp.partials = reinterpret_cast<float*>(base + pl.off_partials);
   sp.tickets = reinterpret_cast<unsigned*>(base + pl.off_tickets);
   sp.status = reinterpret_cast<unsigned*>(base);
-  sp.done = reinterpret_cast<unsigned*>(base + 128);  // inside the status word's 256 bytes
   sp.residual = norm ? norm->residual : nullptr;
   sp.gamma = norm ? norm->gamma : nullptr;
   sp.nout = norm ? norm->out : nullptr;
@@ -1298,17 +1219,25 @@ int launch_mode(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, cudaStr
     cudaGetLastError();
     return W4G128_ERR_CUDA;
   }
-  if (MODE != kMMA) return W4G128_OK;  // M = 1: split quads are folded inside the streaming kernel
-  cfg.gridDim = dim3(static_cast<unsigned>(sp.total_quads));  // one CTA per quad
-  cfg.blockDim = dim3(NORM ? kNormThreads : kRedThreads);
-  cfg.dynamicSmemBytes = kRedSmem;
-  if (NORM) {  // room to stage h and gamma for the norm, when they fit
-    const long long stage = 2LL * sp.mats[0].N * (sp.M + 1);
-    if (stage <= kNormStageMax) cfg.dynamicSmemBytes = kRedSmem + static_cast<int>(stage);
+  if (MODE == kMMA) {  // M >= 2: the split quads are folded by the reduce kernel
+    cfg.gridDim = dim3(static_cast<unsigned>(sp.total_quads));  // one CTA per quad
+    cfg.blockDim = dim3(kRedThreads);
+    cfg.dynamicSmemBytes = kRedSmem;
+    if (cudaLaunchKernelEx(&cfg, reduce_kernel<MAXMAT, NORM>, sp) != cudaSuccess) {
+      cudaGetLastError();
+      return W4G128_ERR_CUDA;
+    }
   }
-  if (cudaLaunchKernelEx(&cfg, reduce_kernel<MAXMAT, NORM>, sp) != cudaSuccess) {
-    cudaGetLastError();
-    return W4G128_ERR_CUDA;
+  if constexpr (NORM) {
+    static_assert(MAXMAT == 1, "the residual add + RMS norm call streams one matrix");
+    const int nchunk = sp.mats[0].N / 8;
+    cfg.gridDim = dim3(static_cast<unsigned>(div_up(nchunk, kNormSlice)), static_cast<unsigned>(sp.M));
+    cfg.blockDim = dim3(kNormThreads);
+    cfg.dynamicSmemBytes = 0;
+    if (cudaLaunchKernelEx(&cfg, rmsnorm_kernel, sp) != cudaSuccess) {
+      cudaGetLastError();
+      return W4G128_ERR_CUDA;
+    }
   }
   return W4G128_OK;
 }

@@ -149,9 +149,9 @@ def test_verify_rows_independent_of_m(K, N):
 @pytest.mark.gpu
 @pytest.mark.parametrize("K,N,M,verify", [(128, 40960, 1, 0), (256, 40960, 1, 1), (128, 10240, 8, 0),
                                           (384, 9216, 2, 1)])
-def test_add_rmsnorm_rows_too_wide_to_stage(K, N, M, verify):
-    """Rows whose h and gamma do not fit in the last CTA's shared memory are
-    normalised from L2 instead (same order, same bound)."""
+def test_add_rmsnorm_wide_rows(K, N, M, verify):
+    """Wide rows: many 1024-column slices per row, each computing the row's
+    mean square itself."""
     mat = DevMatrix(K, N, matrix_id=37 + M)
     x, res, gam = inputs(mat, M, 37 + M)
     h, out = fused(mat, x, res, gam, verify=verify)
