@@ -230,6 +230,13 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const StreamParams<MAXMAT
   c.g_end = min(seg_groups<MODE>(), c.G);
 }
 
+// Arrival at a split quad: returns the count before this arrival.
+__device__ __forceinline__ unsigned ticket_acq_rel(unsigned* t) {
+  unsigned prev;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(t) : "memory");
+  return prev;
+}
+
 // Owner warp of an item under the balanced split [floor(wI/W), floor((w+1)I/W)).
 __device__ __forceinline__ int owner_of(long long item, long long I, int W) {
   return static_cast<int>(((item + 1) * W + I - 1) / I) - 1;
@@ -700,19 +707,22 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
       cursor_next<MODE>(cc, p);
     }
     if (!failed && n_pend > 0) {
-      __threadfence();  // this warp's partials are visible before its tickets
+      // The tickets are acq_rel atomics: the release publishes this warp's
+      // partials (the other lanes' stores are ordered before it by the warp
+      // barrier), and the acquire of the quad's last ticket makes every other
+      // contributor's partials visible to this CTA (its threads are ordered
+      // after it by the barrier before the fold).  No full fence is needed.
       __syncwarp();
       if (lane == 0) {
         // the warp holding a quad's last ticket hands the quad to its CTA's fold
-        if (atomicAdd(p.tickets + pend_q0, 1u) + 1 == pend_e0) fold_q[atomicAdd(&fold_n, 1)] = pend_q0;
-        if (n_pend > 1 && atomicAdd(p.tickets + pend_q1, 1u) + 1 == pend_e1) fold_q[atomicAdd(&fold_n, 1)] = pend_q1;
+        if (ticket_acq_rel(p.tickets + pend_q0) + 1 == pend_e0) fold_q[atomicAdd(&fold_n, 1)] = pend_q0;
+        if (n_pend > 1 && ticket_acq_rel(p.tickets + pend_q1) + 1 == pend_e1) fold_q[atomicAdd(&fold_n, 1)] = pend_q1;
       }
       __syncwarp();
     }
   }  // warp in range
   if constexpr (MODE == kMMA) return;  // M >= 2: the reduce kernel folds
-  __syncthreads();
-  __threadfence();  // the other contributors' partials, published before their tickets
+  __syncthreads();  // orders the fold after the acquiring tickets of this CTA's warps
 
   // ---- fold the completed split quads: one thread per (quad, 4 columns), the
   // quad's 64-float slots from its first warp's prefix fold on, in segment order.
