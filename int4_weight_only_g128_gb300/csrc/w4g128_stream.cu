@@ -230,6 +230,17 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const StreamParams<MAXMAT
   c.g_end = min(seg_groups<MODE>(), c.G);
 }
 
+// What the M = 1 fold of one split quad needs, recorded by the warp that
+// reaches it (32 bytes).
+struct PendFold {
+  long long first;  // first partial slot of the fold (the first warp's prefix fold)
+  uint16_t* y;      // the quad's first output column
+  int nslot;        // slots from `first` to the quad's last segment
+  int cols;         // columns of the quad (64, fewer in a ragged last quad)
+  int n0;           // index of the quad's first column in y
+  int pad;
+};
+
 // Arrival at a split quad: returns the count before this arrival.
 __device__ __forceinline__ unsigned ticket_acq_rel(unsigned* t) {
   unsigned prev;
@@ -472,7 +483,10 @@ __device__ __forceinline__ float pick(const float (&v)[kQuadTiles][NA], int t, i
 // ----------------------------------------------------------------- the streaming kernel
 
 template <int MODE, int MAXMAT, bool NORM>
-__global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
+// M = 1 (CUDA cores) is held to 120 registers (no spills): 4096 of the SM's
+// 65536 registers stay free for the next call's one-warp prep CTAs.
+__global__ void __launch_bounds__(kNW * 32, 16 / kNW) __maxnreg__(MODE == kM1 ? 120 : 128)
+    stream_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int NA = Acc<MODE>::kN;
   constexpr int kSlot = slot_bytes<MODE>();
@@ -482,9 +496,12 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
   const int wg = blockIdx.x * (blockDim.x >> 5) + warp;  // CTAs hold up to kNW warps
   // M = 1: split quads whose last ticket a warp of this CTA took; folded by
   // the whole CTA after its stream (the only block-wide barriers are here and
-  // before that fold).
+  // before that fold).  Each warp records what the fold of its (at most two)
+  // split quads needs when it reaches them, so the fold after the barrier
+  // reads only shared memory (no lookups in the matrix table, no divisions).
   __shared__ int fold_n;
-  __shared__ int fold_q[2 * kNW];
+  __shared__ int fold_ref[2 * kNW];     // entries of pend_info to fold
+  __shared__ PendFold pend_info[2 * kNW];
   if constexpr (MODE != kMMA) {
     if (threadIdx.x == 0) fold_n = 0;
     __syncthreads();
@@ -519,11 +536,12 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
     ic = cc;
     // Prologue: the weight bytes do not depend on the prep kernel, so start them
     // before waiting for it; the activation packages follow after the wait.
-    // Every lane walks the cursors; lane 0 alone issues copies.  The MMA modes
-    // start one chunk early only: their larger prep finishes sooner when less
-    // prefetch is queued ahead of its completion (measured: lm_head M=8
-    // 115.1 -> 113.8 us; at M = 1 the full ring ahead is faster).
-    constexpr int kEarly = (MODE == kMMA) ? 1 : kDepth;
+    // Every lane walks the cursors; lane 0 alone issues copies.  One chunk
+    // starts early: the streaming CTAs become resident while the previous
+    // call's kernels finish, and a deeper early prefetch competes with that
+    // call's tail and with the prep kernel (measured on back-to-back layer
+    // steps at M = 1: 40.4 -> 40.1 us; lm_head M = 8 115.1 -> 113.8 us).
+    constexpr int kEarly = 1;
     Cursor pre[kDepth];
     int n_pre = 0;
 #pragma unroll
@@ -692,7 +710,18 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
             // Split quad at M = 1: its partials are written; the ticket comes after
             // the stream.  (M >= 2: the reduce kernel folds every split quad.)
             const int gq = m.quad_begin + cc.q;
-            const unsigned e = static_cast<unsigned>(owner_of(q_last, I, p.W) - owner_of(q_first, I, p.W) + 1);
+            const int w_first = owner_of(q_first, I, p.W);
+            const unsigned e = static_cast<unsigned>(owner_of(q_last, I, p.W) - w_first + 1);
+            if (lane == 0) {
+              // the fold reads the quad's slots from its first warp's prefix fold on
+              const long long first = I * (w_first + 1) / p.W - 1;
+              PendFold& f = pend_info[2 * warp + n_pend];
+              f.first = first;
+              f.y = m.y + n0;
+              f.nslot = static_cast<int>(q_last + 1 - first);
+              f.cols = kTileN * ntiles;
+              f.n0 = n0;
+            }
             if (n_pend == 0) {
               pend_q0 = gq;
               pend_e0 = e;
@@ -715,8 +744,9 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
       __syncwarp();
       if (lane == 0) {
         // the warp holding a quad's last ticket hands the quad to its CTA's fold
-        if (ticket_acq_rel(p.tickets + pend_q0) + 1 == pend_e0) fold_q[atomicAdd(&fold_n, 1)] = pend_q0;
-        if (n_pend > 1 && ticket_acq_rel(p.tickets + pend_q1) + 1 == pend_e1) fold_q[atomicAdd(&fold_n, 1)] = pend_q1;
+        if (ticket_acq_rel(p.tickets + pend_q0) + 1 == pend_e0) fold_ref[atomicAdd(&fold_n, 1)] = 2 * warp;
+        if (n_pend > 1 && ticket_acq_rel(p.tickets + pend_q1) + 1 == pend_e1)
+          fold_ref[atomicAdd(&fold_n, 1)] = 2 * warp + 1;
       }
       __syncwarp();
     }
@@ -728,22 +758,12 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
   // quad's 64-float slots from its first warp's prefix fold on, in segment order.
   const int nunit = fold_n * 16;
   for (int idx = threadIdx.x; idx < nunit; idx += blockDim.x) {
-    const int gq = fold_q[idx >> 4], col = 4 * (idx & 15);
-    int lo = 0, hi = p.count - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.mats[mid].quad_begin <= gq) lo = mid; else hi = mid - 1;
-    }
-    const MatParams& m = p.mats[lo];
-    const int q = gq - m.quad_begin;
-    const int G = m.K / kGroup, S = div_up(G, seg_groups<MODE>()), T = m.N / kTileN;
-    if (col >= kTileN * min(kQuadTiles, T - kQuadTiles * q)) continue;  // ragged last quad
-    const long long q_first = m.item_begin + static_cast<long long>(q) * S;
-    const long long first = I * (owner_of(q_first, I, p.W) + 1) / p.W - 1;
-    const int nslot = static_cast<int>(q_first + S - first);
-    const float4* part = reinterpret_cast<const float4*>(p.partials + first * 64 + col);
-    const int i = kQuadTiles * kTileN * q + col;
-    const uint32_t r0 = residual2<NORM>(p, i), r1 = residual2<NORM>(p, i + 2);
+    const PendFold& f = pend_info[fold_ref[idx >> 4]];
+    const int col = 4 * (idx & 15);
+    if (col >= f.cols) continue;  // ragged last quad
+    const int nslot = f.nslot;
+    const float4* part = reinterpret_cast<const float4*>(p.partials + f.first * 64 + col);
+    const uint32_t r0 = residual2<NORM>(p, f.n0 + col), r1 = residual2<NORM>(p, f.n0 + col + 2);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = 0; s0 < nslot; s0 += 8) {  // 8 slots in flight, then fold in order
       float4 v[8];
@@ -761,7 +781,7 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
         }
       }
     }
-    uint32_t* yo = reinterpret_cast<uint32_t*>(m.y + i);
+    uint32_t* yo = reinterpret_cast<uint32_t*>(f.y + col);
     yo[0] = emit2<NORM>(acc.x, acc.y, r0);
     yo[1] = emit2<NORM>(acc.z, acc.w, r1);
   }
@@ -769,12 +789,77 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) stream_kernel(const __grid
 
 // ----------------------------------------------------------------- prep kernel
 
-// One warp per (matrix, group): lane (row, c) builds row `row` / lane class c
-// of the group's activation package.  The four lanes of a row agree on the
-// row's scale 2^s (from the largest magnitude among their 128 values), store
-// x' = x 2^s as fp16 pairs with their class sum X_c and f = 2^-s, and lane
-// c == 0 adds the row's (X_g, f) to the package tail.
-template <int MODE, int MAXMAT>
+// Lane class c of one (group, x row) package row, built by four consecutive
+// lanes (lane & ~3 .. + 3, one per class), which agree on the row's scale 2^s
+// from the largest magnitude among their 128 values: x' = x 2^s as fp16 pairs
+// in operand order, the class sum X_c and f = 2^-s go to dst + 80 c, and lane
+// c == 0 writes the row's (X_g, f) to tail[0..1].  xg: the row's 128 values of
+// the group, or nullptr for a zero row (then the row is written as zeros);
+// dst == nullptr writes nothing.  Every lane of the warp must call it (it
+// shuffles).
+__device__ __forceinline__ void build_row_class(const uint16_t* xg, int c, int lane, uint8_t* dst, float* tail) {
+  uint32_t w[16];  // bf16 pairs in operand order
+  float X = 0.f;   // sum of this lane's 32 values
+  uint32_t amax = 0u;  // largest |x| among them, as bf16 magnitude bits
+  if (xg != nullptr) {
+    // x rows start 4-byte aligned (K even, x 4-byte aligned): one 32-bit
+    // load per operand pair
+    const uint32_t* xr = reinterpret_cast<const uint32_t*>(xg);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      w[2 * i] = xr[8 * i + c];
+      w[2 * i + 1] = xr[8 * i + c + 4];
+    }
+    uint32_t mag2 = 0u;  // per-half maxima of |x| bits
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      X = (((X + bf16_lo(w[2 * i])) + bf16_hi(w[2 * i])) + bf16_lo(w[2 * i + 1])) + bf16_hi(w[2 * i + 1]);
+      mag2 = __vmaxu2(mag2, __vmaxu2(w[2 * i] & 0x7FFF7FFFu, w[2 * i + 1] & 0x7FFF7FFFu));
+    }
+    amax = max(mag2 & 0xFFFFu, mag2 >> 16);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = 0u;
+  }
+  amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  // biased exponent e of the row's largest |x|: x 2^(141 - e) lies in
+  // [2^14, 2^15); the cap keeps 2^s a normal fp32 for zero or tiny rows.
+  const int sft = min(141 - static_cast<int>(amax >> 7), 126);
+  const float up = __int_as_float((127 + sft) << 23);
+  const float f = __int_as_float((127 - sft) << 23);
+  if (dst != nullptr) {
+    uint32_t h[20];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 v = fmul2(make_float2(bf16_lo(w[i]), bf16_hi(w[i])), make_float2(up, up));
+      asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h[i]) : "f"(v.y), "f"(v.x));  // (hi, lo)
+    }
+    h[16] = __float_as_uint(X);
+    h[17] = __float_as_uint(f);
+    h[18] = h[19] = 0u;
+    uint4* o = reinterpret_cast<uint4*>(dst + c * 80);
+#pragma unroll
+    for (int i = 0; i < 5; ++i) o[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+  }
+  // group sum of the row: ((X_0 + X_1) + X_2) + X_3 over its four lane classes
+  const float X0 = __shfl_sync(0xffffffffu, X, lane & ~3);
+  const float X1 = __shfl_sync(0xffffffffu, X, (lane & ~3) + 1);
+  const float X2 = __shfl_sync(0xffffffffu, X, (lane & ~3) + 2);
+  const float X3 = __shfl_sync(0xffffffffu, X, (lane & ~3) + 3);
+  if (c == 0 && dst != nullptr) {
+    tail[0] = ((X0 + X1) + X2) + X3;
+    tail[1] = f;
+  }
+}
+
+// The prep kernels run on a 2-D grid, blockIdx.y = matrix, so no CTA
+// searches the matrix table (each lookup in the kernel parameters is an L2
+// round trip when it misses the constant cache).
+
+// M >= 2: 8 warps per CTA, one group each; lane (row, c) builds row `row` /
+// lane class c of the group's activation package (rows >= M are zeros).
+template <int MAXMAT>
 __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
   // Launched early behind the previous kernel of the stream (programmatic
   // dependent launch): the next kernel may launch at once, but nothing here
@@ -782,78 +867,43 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Strea
   // workspace, or write this call's x.
   grid_dependents_launch();
   grid_dependency_wait();
-  const int tid = blockIdx.x * blockDim.x + threadIdx.x, nthreads = gridDim.x * blockDim.x;
-  if (MODE != kMMA)
-    for (int i = tid; i < p.total_quads; i += nthreads) p.tickets[i] = 0u;
-  if (tid == 0) *p.status = 0u;
-
-  constexpr int kRows = Pkg<MODE>::kRows;
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.status = 0u;
+  constexpr int kRows = Pkg<kMMA>::kRows;
+  const MatParams& m = p.mats[blockIdx.y];
+  const int G = m.K / kGroup;
   const int lane = threadIdx.x & 31;
   const int row = lane >> 2, c = lane & 3;
-  const int warp0 = tid >> 5, nwarps = nthreads >> 5;
-  for (int wg = warp0; wg < p.total_groups; wg += nwarps) {
-    int lo = 0, hi = p.count - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.mats[mid].g_begin <= wg) lo = mid; else hi = mid - 1;
-    }
-    const MatParams& m = p.mats[lo];
-    const int g = wg - m.g_begin;
-    uint8_t* out = m.xpkg + static_cast<long long>(g) * Pkg<MODE>::kBytes;
-    uint32_t w[16];  // bf16 pairs in operand order
-    float X = 0.f;   // sum of this lane's 32 values
-    uint32_t amax = 0u;  // largest |x| among them, as bf16 magnitude bits
-    if (row < kRows && row < p.M) {
-      // x rows start 4-byte aligned (K even, x 4-byte aligned): one 32-bit
-      // load per operand pair
-      const uint32_t* xr = reinterpret_cast<const uint32_t*>(m.x + static_cast<long long>(row) * m.K + kGroup * g);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        w[2 * i] = xr[8 * i + c];
-        w[2 * i + 1] = xr[8 * i + c + 4];
-      }
-      uint32_t mag2 = 0u;  // per-half maxima of |x| bits
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        X = (((X + bf16_lo(w[2 * i])) + bf16_hi(w[2 * i])) + bf16_lo(w[2 * i + 1])) + bf16_hi(w[2 * i + 1]);
-        mag2 = __vmaxu2(mag2, __vmaxu2(w[2 * i] & 0x7FFF7FFFu, w[2 * i + 1] & 0x7FFF7FFFu));
-      }
-      amax = max(mag2 & 0xFFFFu, mag2 >> 16);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) w[i] = 0u;
-    }
-    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    // biased exponent e of the row's largest |x|: x 2^(141 - e) lies in
-    // [2^14, 2^15); the cap keeps 2^s a normal fp32 for zero or tiny rows.
-    const int sft = min(141 - static_cast<int>(amax >> 7), 126);
-    const float up = __int_as_float((127 + sft) << 23);
-    const float f = __int_as_float((127 - sft) << 23);
-    if (row < kRows) {
-      uint32_t h[20];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float2 v = fmul2(make_float2(bf16_lo(w[i]), bf16_hi(w[i])), make_float2(up, up));
-        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h[i]) : "f"(v.y), "f"(v.x));  // (hi, lo)
-      }
-      h[16] = __float_as_uint(X);
-      h[17] = __float_as_uint(f);
-      h[18] = h[19] = 0u;
-      uint4* o = reinterpret_cast<uint4*>(out + row * Pkg<MODE>::kRowBytes + c * 80);
-#pragma unroll
-      for (int i = 0; i < 5; ++i) o[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
-    }
-    // group sum of row `row`: ((X_0 + X_1) + X_2) + X_3 over its four lane classes
-    const float X0 = __shfl_sync(0xffffffffu, X, lane & ~3);
-    const float X1 = __shfl_sync(0xffffffffu, X, (lane & ~3) + 1);
-    const float X2 = __shfl_sync(0xffffffffu, X, (lane & ~3) + 2);
-    const float X3 = __shfl_sync(0xffffffffu, X, (lane & ~3) + 3);
-    if (c == 0 && row < kRows) {
-      float* tail = reinterpret_cast<float*>(out + kRows * Pkg<MODE>::kRowBytes);
-      tail[2 * row] = ((X0 + X1) + X2) + X3;
-      tail[2 * row + 1] = f;
-    }
+  for (int g = 8 * blockIdx.x + (threadIdx.x >> 5); g < G; g += 8 * gridDim.x) {
+    uint8_t* out = m.xpkg + static_cast<long long>(g) * Pkg<kMMA>::kBytes;
+    float* tail = reinterpret_cast<float*>(out + kRows * Pkg<kMMA>::kRowBytes);
+    build_row_class(row < p.M ? m.x + static_cast<long long>(row) * m.K + kGroup * g : nullptr, c, lane,
+                    out + row * Pkg<kMMA>::kRowBytes, tail + 2 * row);
+  }
+}
+
+// M = 1 (either arithmetic): the one-row package needs four lanes, so a warp
+// builds eight groups at once, lane (j, c) class c of group 8 k + j of its
+// share.  One-warp CTAs with few registers fit on an SM beside a streaming
+// CTA: the next call's prep is resident before the previous call has ended,
+// and never holds an SM the streaming kernel needs.  Also clears the
+// split-quad tickets and the status word.
+template <int MODE, int MAXMAT>
+__global__ void __launch_bounds__(32) prep1_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
+  grid_dependents_launch();
+  grid_dependency_wait();  // as in prep_kernel
+  const int lane = threadIdx.x;
+  const MatParams& m = p.mats[blockIdx.y];
+  const int G = m.K / kGroup;
+  // this matrix's split-quad tickets
+  const int nq = div_up(m.N, kQuadTiles * kTileN);
+  for (int i = blockIdx.x * 32 + lane; i < nq; i += gridDim.x * 32) p.tickets[m.quad_begin + i] = 0u;
+  if (blockIdx.x == 0 && blockIdx.y == 0 && lane == 0) *p.status = 0u;
+  const int j = lane >> 2, c = lane & 3;
+  for (int base = 8 * blockIdx.x; base < G; base += 8 * gridDim.x) {  // warp-uniform trip count
+    const int g = base + j;
+    const bool in = g < G;
+    uint8_t* out = in ? m.xpkg + static_cast<long long>(g) * Pkg<MODE>::kBytes : nullptr;
+    build_row_class(in ? m.x + kGroup * g : nullptr, c, lane, out, reinterpret_cast<float*>(out + Pkg<MODE>::kRowBytes));
   }
 }
 
@@ -1124,7 +1174,7 @@ const DeviceInfo* device_info() {
 struct Plan {
   int mode = 0, rows = 1, pkg = 0;
   long long items = 0;
-  int W = 0, grid = 0, cta_warps = kNW, total_quads = 0, total_groups = 0;
+  int W = 0, grid = 0, cta_warps = kNW, total_quads = 0, total_groups = 0, max_groups = 0;
   size_t off_tickets = 0, off_xpkg = 0, off_partials = 0, bytes = 0;
   std::vector<long long> item_begin, xpkg_off;
   std::vector<int> quad_begin, g_begin;
@@ -1151,6 +1201,7 @@ bool make_plan(const HostMatrix* mats, int count, int M, bool verify, const Devi
     items += static_cast<long long>(NQ) * S;
     quads += NQ;
     groups += G;
+    pl.max_groups = std::max(pl.max_groups, G);
     xbytes += static_cast<long long>(G) * pl.pkg;
     if (quads > (1 << 24) || groups > 0x7FFFFFFF) return false;  // quad indices stay well inside int
   }
@@ -1163,6 +1214,7 @@ bool make_plan(const HostMatrix* mats, int count, int M, bool verify, const Devi
   // holds warps gets smaller CTAs rather than fewer SMs.
   pl.cta_warps = std::min(kNW, div_up(pl.W, dev.sms));
   pl.grid = div_up(pl.W, pl.cta_warps);
+
   pl.off_tickets = 256;  // after the status word
   pl.off_xpkg = align_up(pl.off_tickets + sizeof(unsigned) * static_cast<size_t>(quads), 256);
   pl.off_partials = align_up(pl.off_xpkg + static_cast<size_t>(xbytes), 256);
@@ -1202,7 +1254,7 @@ void fill_params(StreamParams<MAXMAT>& sp, const HostMatrix* mats, int count, in
 }
 
 template <int MODE, int MAXMAT, bool NORM>
-int launch_mode(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, cudaStream_t stream) {
+int launch_mode(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, int max_groups, cudaStream_t stream) {
   // Every kernel of the call is a programmatic dependent launch: the prep
   // kernel behind whatever precedes it in the stream (it waits for that to
   // finish before touching anything), the streaming kernel behind the prep
@@ -1215,10 +1267,17 @@ int launch_mode(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, cudaStr
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cfg.gridDim = dim3(std::max(1, std::min(div_up(sp.total_groups * 32, 256), 1024)));
-  cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
-  if (cudaLaunchKernelEx(&cfg, prep_kernel<MODE, MAXMAT>, sp) != cudaSuccess) {
+  cudaError_t e;
+  cfg.gridDim = dim3(static_cast<unsigned>(std::min(div_up(max_groups, 8), 4096)), static_cast<unsigned>(sp.count));
+  if constexpr (MODE == kMMA) {
+    cfg.blockDim = dim3(256);
+    e = cudaLaunchKernelEx(&cfg, prep_kernel<MAXMAT>, sp);
+  } else {
+    cfg.blockDim = dim3(32);
+    e = cudaLaunchKernelEx(&cfg, prep1_kernel<MODE, MAXMAT>, sp);
+  }
+  if (e != cudaSuccess) {
     cudaGetLastError();
     return W4G128_ERR_CUDA;
   }
@@ -1259,14 +1318,14 @@ int launch_with(const HostMatrix* mats, int count, int M, const Plan& pl, const 
   fill_params(sp, mats, count, M, pl, norm, ws);
   if constexpr (MAXMAT == 1) {
     if (norm != nullptr) {
-      if (pl.mode == kMMA) return launch_mode<kMMA, 1, true>(sp, pl.grid, pl.cta_warps, stream);
-      if (pl.mode == kMMA1) return launch_mode<kMMA1, 1, true>(sp, pl.grid, pl.cta_warps, stream);
-      return launch_mode<kM1, 1, true>(sp, pl.grid, pl.cta_warps, stream);
+      if (pl.mode == kMMA) return launch_mode<kMMA, 1, true>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
+      if (pl.mode == kMMA1) return launch_mode<kMMA1, 1, true>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
+      return launch_mode<kM1, 1, true>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
     }
   }
-  if (pl.mode == kMMA) return launch_mode<kMMA, MAXMAT, false>(sp, pl.grid, pl.cta_warps, stream);
-  if (pl.mode == kMMA1) return launch_mode<kMMA1, MAXMAT, false>(sp, pl.grid, pl.cta_warps, stream);
-  return launch_mode<kM1, MAXMAT, false>(sp, pl.grid, pl.cta_warps, stream);
+  if (pl.mode == kMMA) return launch_mode<kMMA, MAXMAT, false>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
+  if (pl.mode == kMMA1) return launch_mode<kMMA1, MAXMAT, false>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
+  return launch_mode<kM1, MAXMAT, false>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
 }
 
 }  // namespace
