@@ -157,6 +157,16 @@ struct StreamParams {
 
 static_assert(sizeof(StreamParams<W4G128_MAX_MATRICES>) <= 32000, "kernel parameter limit");
 
+// A matrix of the call.  With one matrix the index is the constant 0, so every
+// read of its descriptor is at a fixed offset of the kernel parameters: those
+// reads are independent of one another and shared by all SMs, while a
+// computed index makes each a dependent lookup (an L2 round trip when it
+// misses the constant cache).
+template <int MAXMAT>
+__device__ __forceinline__ const MatParams& mat(const StreamParams<MAXMAT>& p, int i) {
+  return p.mats[MAXMAT == 1 ? 0 : i];
+}
+
 __host__ __device__ constexpr int div_up(int a, int b) { return (a + b - 1) / b; }
 
 // ----------------------------------------------------------------- cursor
@@ -175,7 +185,7 @@ struct Cursor {
 
 template <int MODE, int MAXMAT>
 __device__ __forceinline__ void cursor_load(Cursor& c, const StreamParams<MAXMAT>& p, int mi) {
-  const MatParams& m = p.mats[mi];
+  const MatParams& m = mat(p, mi);
   c.mi = mi;
   c.G = m.K / kGroup;
   c.S = div_up(c.G, seg_groups<MODE>());
@@ -185,22 +195,25 @@ __device__ __forceinline__ void cursor_load(Cursor& c, const StreamParams<MAXMAT
 
 template <int MODE, int MAXMAT>
 __device__ __forceinline__ void cursor_seek(Cursor& c, const StreamParams<MAXMAT>& p, long long item) {
-  int lo = 0, hi = p.count - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (p.mats[mid].item_begin <= item) lo = mid; else hi = mid - 1;
+  int lo = 0;
+  if constexpr (MAXMAT > 1) {
+    int hi = p.count - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.mats[mid].item_begin <= item) lo = mid; else hi = mid - 1;
+    }
   }
   cursor_load<MODE>(c, p, lo);
-  const long long local = item - p.mats[lo].item_begin;
+  const long long local = item - mat(p, lo).item_begin;
   c.item = item;
   c.q = static_cast<int>(local / c.S);
   c.s = static_cast<int>(local - static_cast<long long>(c.q) * c.S);
   c.g = c.s * seg_groups<MODE>();
   c.g_end = min(c.g + seg_groups<MODE>(), c.G);
   c.ntiles = min(kQuadTiles, c.T - kQuadTiles * c.q);
-  c.src = p.mats[lo].packed + static_cast<long long>(c.q) * c.G * kQuadBytes +
+  c.src = mat(p, lo).packed + static_cast<long long>(c.q) * c.G * kQuadBytes +
           static_cast<long long>(c.g) * c.ntiles * kBlockBytes;
-  c.xsrc = p.mats[lo].xpkg + static_cast<long long>(c.g) * Pkg<MODE>::kBytes;
+  c.xsrc = mat(p, lo).xpkg + static_cast<long long>(c.g) * Pkg<MODE>::kBytes;
 }
 
 template <int MODE, int MAXMAT>
@@ -217,7 +230,7 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const StreamParams<MAXMAT
   c.g = 0;
   if (++c.q < c.NQ) {  // the next quad starts where this one ended
     c.ntiles = min(kQuadTiles, c.T - kQuadTiles * c.q);
-    c.xsrc = p.mats[c.mi].xpkg;
+    c.xsrc = mat(p, c.mi).xpkg;
     c.g_end = min(seg_groups<MODE>(), c.G);
     return;
   }
@@ -225,8 +238,8 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const StreamParams<MAXMAT
   cursor_load<MODE>(c, p, c.mi + 1);
   c.q = 0;
   c.ntiles = min(kQuadTiles, c.T);
-  c.src = p.mats[c.mi].packed;
-  c.xsrc = p.mats[c.mi].xpkg;
+  c.src = mat(p, c.mi).packed;
+  c.xsrc = mat(p, c.mi).xpkg;
   c.g_end = min(seg_groups<MODE>(), c.G);
 }
 
@@ -619,7 +632,7 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) __maxnreg__(MODE == kM1 ? 
 
       if (cc.g + 1 == cc.g_end) {
         // ---- end of a segment
-        const MatParams& m = p.mats[cc.mi];
+        const MatParams& m = mat(p, cc.mi);
         const int S = cc.S;
         const long long q_first = m.item_begin + static_cast<long long>(cc.q) * S;
         const long long q_last = q_first + S - 1;
@@ -869,7 +882,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Strea
   grid_dependency_wait();
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.status = 0u;
   constexpr int kRows = Pkg<kMMA>::kRows;
-  const MatParams& m = p.mats[blockIdx.y];
+  const MatParams& m = mat(p, blockIdx.y);
   const int G = m.K / kGroup;
   const int lane = threadIdx.x & 31;
   const int row = lane >> 2, c = lane & 3;
@@ -892,7 +905,7 @@ __global__ void __launch_bounds__(32) prep1_kernel(const __grid_constant__ Strea
   grid_dependents_launch();
   grid_dependency_wait();  // as in prep_kernel
   const int lane = threadIdx.x;
-  const MatParams& m = p.mats[blockIdx.y];
+  const MatParams& m = mat(p, blockIdx.y);
   const int G = m.K / kGroup;
   // this matrix's split-quad tickets
   const int nq = div_up(m.N, kQuadTiles * kTileN);
@@ -928,12 +941,15 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(const __grid_consta
   extern __shared__ __align__(128) uint8_t rsm[];
   __shared__ int ok;
   const int gq = blockIdx.x;
-  int lo = 0, hi = p.count - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (p.mats[mid].quad_begin <= gq) lo = mid; else hi = mid - 1;
+  int lo = 0;
+  if constexpr (MAXMAT > 1) {
+    int hi = p.count - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.mats[mid].quad_begin <= gq) lo = mid; else hi = mid - 1;
+    }
   }
-  const MatParams& m = p.mats[lo];
+  const MatParams& m = mat(p, lo);
   const int q = gq - m.quad_begin;
   const int G = m.K / kGroup, S = div_up(G, seg_groups<kMMA>()), T = m.N / kTileN;
   const long long I = p.total_items;
