@@ -883,6 +883,13 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Strea
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.status = 0u;
   constexpr int kRows = Pkg<kMMA>::kRows;
   const MatParams& m = mat(p, blockIdx.y);
+  // M >= 2 takes no tickets: their array holds each quad's matrix instead, for
+  // the reduce kernel (a load from it replaces a search of the matrix table)
+  if constexpr (MAXMAT > 1) {
+    const int nq = div_up(m.N, kQuadTiles * kTileN);
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nq; i += gridDim.x * blockDim.x)
+      p.tickets[m.quad_begin + i] = blockIdx.y;
+  }
   const int G = m.K / kGroup;
   const int lane = threadIdx.x & 31;
   const int row = lane >> 2, c = lane & 3;
@@ -942,13 +949,7 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(const __grid_consta
   __shared__ int ok;
   const int gq = blockIdx.x;
   int lo = 0;
-  if constexpr (MAXMAT > 1) {
-    int hi = p.count - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.mats[mid].quad_begin <= gq) lo = mid; else hi = mid - 1;
-    }
-  }
+  if constexpr (MAXMAT > 1) lo = static_cast<int>(__ldcg(p.tickets + gq));  // written by the prep kernel
   const MatParams& m = mat(p, lo);
   const int q = gq - m.quad_begin;
   const int G = m.K / kGroup, S = div_up(G, seg_groups<kMMA>()), T = m.N / kTileN;
