@@ -342,7 +342,7 @@ def run_ours(args):
         ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
         return xs_h, xs, ys, descs, ws
 
-    MS = (1, 2, 4, 8)
+    MS = (1, 2, 4, 8, 16)
     io = {M: make_io(M) for M in MS}
 
     # ---- parity gate on sampled outputs (first and last weight copy)

@@ -10,7 +10,7 @@
  * lm_head row slice):
  *
  *     y[m][n] = bf16( sum_k x[m][k] * w[k][n] ),   w[k][n] = min[g][n] + q[k][n] * scale[g][n],
- *     g = k / 128,  q in 0..15,  1 <= M <= 8,
+ *     g = k / 128,  q in 0..15,  1 <= M <= 16,
  *
  * with bf16 x, scale, min and y, fp32 accumulation and one final
  * round-to-nearest-even to bf16.  Results are accepted when
@@ -92,7 +92,7 @@ extern "C" {
 
 typedef enum {
   W4G128_OK = 0,
-  W4G128_ERR_INVALID_ARG = 1, /* null pointer, M outside 1..8, count outside 1..W4G128_MAX_MATRICES */
+  W4G128_ERR_INVALID_ARG = 1, /* null pointer, M outside 1..W4G128_MAX_M, count outside 1..W4G128_MAX_MATRICES */
   W4G128_ERR_SHAPE = 2,       /* K % 128, N % 16, or a size outside the limits above */
   W4G128_ERR_ALIGN = 3,       /* a pointer is not aligned as required */
   W4G128_ERR_WORKSPACE = 4,   /* ws_bytes smaller than the workspace query returns */
@@ -101,7 +101,7 @@ typedef enum {
   W4G128_ERR_TIMEOUT = 7      /* (status word only) a bounded device-side wait gave up */
 } w4g128_status;
 
-#define W4G128_MAX_M 8
+#define W4G128_MAX_M 16
 #define W4G128_MAX_MATRICES 512
 
 /* Raw bf16 bit pattern. */
@@ -152,11 +152,13 @@ W4G128_API size_t w4g128_workspace_bytes(int M, int K, int N);
 W4G128_API int w4g128_gemv(const void* packed, const w4g128_bf16* x, w4g128_bf16* y, int K, int N,
                            void* ws, size_t ws_bytes, void* stream);
 
-/* y[M][N] = x[M][K] . dequant(W) for 1 <= M <= 8: the speculative M-row
- * verify step (one weight pass for M draft rows, on the tensor cores via
- * warp MMA).  Row m of the result is bitwise identical to this call on row m
- * alone (M = 1), for every M: a verify pass reproduces exactly what the same
- * arithmetic gives one token at a time.  w4g128_gemv (CUDA cores) agrees with
+/* y[M][N] = x[M][K] . dequant(W) for 1 <= M <= W4G128_MAX_M (16): the
+ * speculative M-row verify step (one weight pass for M draft rows, on the
+ * tensor cores via warp MMA; the pages draft 7 tokens, M = 9..16 serves longer
+ * drafts with two 8-row MMA tiles per weight fragment).  Row m of the result
+ * is bitwise identical to this call on row m alone (M = 1), for every M: a
+ * verify pass reproduces exactly what the same arithmetic gives one token at
+ * a time.  w4g128_gemv (CUDA cores) agrees with
  * it within the acceptance bound, not bitwise.  Token Rush README, progress
  * table steps 13-14 and 28. */
 W4G128_API int w4g128_gemm_verify(const void* packed, const w4g128_bf16* x, w4g128_bf16* y, int M, int K,

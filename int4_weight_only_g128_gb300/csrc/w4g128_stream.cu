@@ -70,7 +70,12 @@ enum Mode : int {
   kM1 = 0,   // M = 1, CUDA cores: fp16 x fp16 -> fp32 FMA on the dequantised pairs
   kMMA = 1,  // M <= 8, warp MMA m16n8k16 f16 -> f32 with the weights as the 16-row operand
   kMMA1 = 2, // M = 1 with the verify arithmetic: the warp MMA, every B column carrying the one x row
+  kMMA16 = 3, // 9 <= M <= 16: the warp MMA, two 8-row x tiles per dequantised weight fragment
 };
+
+// The modes that carry p.M x rows through the MMA (and fold in the reduce kernel).
+template <int MODE>
+__host__ __device__ constexpr bool multi_row() { return MODE == kMMA || MODE == kMMA16; }
 
 #ifndef W4G128_WARPS_PER_CTA
 #define W4G128_WARPS_PER_CTA 16
@@ -97,6 +102,7 @@ template <int MODE> struct Pkg;
 template <> struct Pkg<kM1> { static constexpr int kRows = 1, kRowBytes = 320, kBytes = 336; };
 template <> struct Pkg<kMMA> { static constexpr int kRows = 8, kRowBytes = 320, kBytes = 2624; };
 template <> struct Pkg<kMMA1> { static constexpr int kRows = 1, kRowBytes = 320, kBytes = 336; };
+template <> struct Pkg<kMMA16> { static constexpr int kRows = 16, kRowBytes = 320, kBytes = 5248; };
 
 // Groups per split-K segment (an item's K extent): fixed per mode, never by
 // the grid, so every summation order depends on the shape and M alone.  Both
@@ -114,15 +120,26 @@ __host__ __device__ constexpr int slot_bytes() { return kQuadTiles * kBlockBytes
 // Ring slots per warp: kDepth, or for the small-package M = 1 modes
 // W4G128_M1_RING_DEPTH (three 4688-byte slots per warp still fit 16 warps).
 template <int MODE>
-__host__ __device__ constexpr int ring_depth() { return MODE == kMMA ? kDepth : W4G128_M1_RING_DEPTH; }
+__host__ __device__ constexpr int ring_depth() { return multi_row<MODE>() ? kDepth : W4G128_M1_RING_DEPTH; }
 constexpr int kMaxDepth = kDepth > W4G128_M1_RING_DEPTH ? kDepth : W4G128_M1_RING_DEPTH;
 constexpr int kBarBytes = ((kNW * kMaxDepth * 8 + 127) / 128) * 128;  // per warp, its ring's mbarriers
+// Warps per CTA: 16, or 8 at M <= 16: its 9.4 KB slots (a 5.1 KB package)
+// leave room for fewer rings, and its twice as many accumulators need more
+// than 168 registers a thread, which the register file grants only with at
+// most two warps per scheduler.
 template <int MODE>
-__host__ __device__ constexpr int smem_bytes() { return kBarBytes + kNW * ring_depth<MODE>() * slot_bytes<MODE>(); }
+__host__ __device__ constexpr int cta_warps_max() { return MODE == kMMA16 ? 8 : kNW; }
+template <int MODE>
+__host__ __device__ constexpr int smem_bytes() {
+  return kBarBytes + cta_warps_max<MODE>() * ring_depth<MODE>() * slot_bytes<MODE>();
+}
 
-static_assert(slot_bytes<kM1>() % 16 == 0 && slot_bytes<kMMA>() % 16 == 0, "bulk copies need 16-byte slots");
-static_assert(Pkg<kM1>::kBytes % 16 == 0 && Pkg<kMMA>::kBytes % 16 == 0, "bulk copies need 16-byte packages");
-static_assert(smem_bytes<kM1>() <= 232448 && smem_bytes<kMMA>() <= 232448 && smem_bytes<kMMA1>() <= 232448,
+static_assert(slot_bytes<kM1>() % 16 == 0 && slot_bytes<kMMA>() % 16 == 0 && slot_bytes<kMMA16>() % 16 == 0,
+              "bulk copies need 16-byte slots");
+static_assert(Pkg<kM1>::kBytes % 16 == 0 && Pkg<kMMA>::kBytes % 16 == 0 && Pkg<kMMA16>::kBytes % 16 == 0,
+              "bulk copies need 16-byte packages");
+static_assert(smem_bytes<kM1>() <= 232448 && smem_bytes<kMMA>() <= 232448 && smem_bytes<kMMA1>() <= 232448 &&
+                  smem_bytes<kMMA16>() <= 232448,
               "a CTA's rings must fit the 227 KB of shared memory");
 
 // ----------------------------------------------------------------- parameters
@@ -328,6 +345,25 @@ __device__ __forceinline__ void mma_word(uint32_t w, uint32_t xa, uint32_t xb, f
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(xa), "r"(xb));
 }
 
+// The same A fragment against two 8-row x tiles (rows 0-7 into d, 8-15 into e):
+// each is exactly the MMA mma_word issues for its rows.
+__device__ __forceinline__ void mma_word2(uint32_t w, uint32_t xa, uint32_t xb, uint32_t ya, uint32_t yb,
+                                          float (&d)[4], float (&e)[4]) {
+  const uint32_t v = w >> 8;
+  const uint32_t a0 = lop3_and_or(w, 0x000F000Fu, kMagic);
+  const uint32_t a1 = lop3_and_or(w, 0x00F000F0u, kMagic);
+  const uint32_t a2 = lop3_and_or(v, 0x000F000Fu, kMagic);
+  const uint32_t a3 = lop3_and_or(v, 0x00F000F0u, kMagic);
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(xa), "r"(xb));
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(e[0]), "+f"(e[1]), "+f"(e[2]), "+f"(e[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(ya), "r"(yb));
+}
+
 // Two IEEE fp32 FMAs in one instruction (Blackwell packed f32x2); each lane of
 // the pair rounds exactly like fmaf.
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
@@ -389,7 +425,7 @@ __device__ __forceinline__ uint32_t emit2(float a, float b, uint32_t r) {
 
 // Rows of the per-lane accumulators: M = 1 keeps (column r, column r+8);
 // the MMA keeps (r, 2c), (r, 2c+1), (r+8, 2c), (r+8, 2c+1).
-template <int MODE> struct Acc { static constexpr int kN = (MODE == kM1) ? 2 : 4; };
+template <int MODE> struct Acc { static constexpr int kN = (MODE == kM1) ? 2 : (MODE == kMMA16 ? 8 : 4); };
 
 // One chunk: every tile of the quad for one group, added into seg[t][*].
 // FULL: the quad has all 4 tiles, so the tiles form one straight-line block
@@ -399,7 +435,7 @@ __device__ __forceinline__ void compute_chunk(const uint8_t* sl, int ntiles, int
                                               float (&seg)[kQuadTiles][Acc<MODE>::kN]) {
   const int r = lane >> 2, c = lane & 3;
   const uint8_t* pk = sl + kQuadTiles * kBlockBytes;
-  const int row = (MODE == kMMA) ? r : 0;
+  const int row = multi_row<MODE>() ? r : 0;
   const uint32_t* xr = reinterpret_cast<const uint32_t*>(pk + row * Pkg<MODE>::kRowBytes + c * 80);
   uint32_t xw[16];
 #pragma unroll
@@ -435,6 +471,58 @@ __device__ __forceinline__ void compute_chunk(const uint8_t* sl, int ntiles, int
         a2 = ffma2(fmul2(s2, ff), make_float2(lo, hi), a2);
         seg[t][0] = a2.x;
         seg[t][1] = a2.y;
+      }
+    }
+  } else if constexpr (MODE == kMMA16) {
+    // rows r (tile 0) and 8 + r (tile 1) of the B operand; (X_g, f) of rows
+    // 2c, 2c + 1 and 8 + 2c, 9 + 2c.  Each tile goes through exactly the
+    // arithmetic of the 8-row mode, so every row's bits match it.
+    const uint32_t* yr = reinterpret_cast<const uint32_t*>(pk + (8 + r) * Pkg<MODE>::kRowBytes + c * 80);
+    uint32_t yw[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = reinterpret_cast<const uint4*>(yr)[i];
+      yw[4 * i] = v.x; yw[4 * i + 1] = v.y; yw[4 * i + 2] = v.z; yw[4 * i + 3] = v.w;
+    }
+    const float* tl = reinterpret_cast<const float*>(pk + Pkg<MODE>::kRows * Pkg<MODE>::kRowBytes);
+    const float4 xq0 = *reinterpret_cast<const float4*>(tl + 4 * c);
+    const float4 xq1 = *reinterpret_cast<const float4*>(tl + 16 + 4 * c);
+#pragma unroll
+    for (int t = 0; t < kQuadTiles; ++t) {
+      if (FULL || t < ntiles) {
+        const uint8_t* blk = sl + t * kBlockBytes;
+        const uint4 u0 = *reinterpret_cast<const uint4*>(blk + 16 * lane);
+        const uint4 u1 = *reinterpret_cast<const uint4*>(blk + 512 + 16 * lane);
+        const uint2 me = *reinterpret_cast<const uint2*>(blk + kCodeBytes + 8 * r);
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+        float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_word2(u0.x, xw[0], xw[1], yw[0], yw[1], d0, e0);
+        mma_word2(u0.y, xw[2], xw[3], yw[2], yw[3], d1, e1);
+        mma_word2(u0.z, xw[4], xw[5], yw[4], yw[5], d0, e0);
+        mma_word2(u0.w, xw[6], xw[7], yw[6], yw[7], d1, e1);
+        mma_word2(u1.x, xw[8], xw[9], yw[8], yw[9], d0, e0);
+        mma_word2(u1.y, xw[10], xw[11], yw[10], yw[11], d1, e1);
+        mma_word2(u1.z, xw[12], xw[13], yw[12], yw[13], d0, e0);
+        mma_word2(u1.w, xw[14], xw[15], yw[14], yw[15], d1, e1);
+        const float sl0 = bf16_lo(me.x), sh0 = bf16_lo(me.y);
+        const float ml0 = fmaf(-1024.f, sl0, bf16_hi(me.x));
+        const float mh0 = fmaf(-64.f, sh0, bf16_hi(me.y));
+        auto epilogue = [&](const float (&a)[4], const float (&b)[4], const float4 xq, float& s0, float& s1,
+                            float& s2, float& s3) {
+          const float2 Xab = make_float2(xq.x, xq.z);
+          const float2 fab = make_float2(xq.y, xq.w);
+          const float2 fab16 = make_float2(xq.y * 0.0625f, xq.w * 0.0625f);
+          float2 lo2 = ffma2(make_float2(ml0, ml0), Xab, make_float2(s0, s1));
+          lo2 = ffma2(fmul2(make_float2(sl0, sl0), fab), make_float2(a[0] + b[0], a[1] + b[1]), lo2);
+          float2 hi2 = ffma2(make_float2(mh0, mh0), Xab, make_float2(s2, s3));
+          hi2 = ffma2(fmul2(make_float2(sh0, sh0), fab16), make_float2(a[2] + b[2], a[3] + b[3]), hi2);
+          s0 = lo2.x;
+          s1 = lo2.y;
+          s2 = hi2.x;
+          s3 = hi2.y;
+        };
+        epilogue(d0, d1, xq0, seg[t][0], seg[t][1], seg[t][2], seg[t][3]);
+        epilogue(e0, e1, xq1, seg[t][4], seg[t][5], seg[t][6], seg[t][7]);
       }
     }
   } else {
@@ -498,7 +586,9 @@ __device__ __forceinline__ float pick(const float (&v)[kQuadTiles][NA], int t, i
 template <int MODE, int MAXMAT, bool NORM>
 // M = 1 (CUDA cores) is held to 120 registers (no spills): 4096 of the SM's
 // 65536 registers stay free for the next call's one-warp prep CTAs.
-__global__ void __launch_bounds__(kNW * 32, 16 / kNW) __maxnreg__(MODE == kM1 ? 120 : 128)
+// M <= 16 (8 warps) may use up to 255.
+__global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
+    __maxnreg__(MODE == kM1 ? 120 : (MODE == kMMA16 ? 255 : 128))
     stream_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int NA = Acc<MODE>::kN;
@@ -515,7 +605,7 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) __maxnreg__(MODE == kM1 ? 
   __shared__ int fold_n;
   __shared__ int fold_ref[2 * kNW];     // entries of pend_info to fold
   __shared__ PendFold pend_info[2 * kNW];
-  if constexpr (MODE != kMMA) {
+  if constexpr (!multi_row<MODE>()) {
     if (threadIdx.x == 0) fold_n = 0;
     __syncthreads();
   }
@@ -671,16 +761,21 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) __maxnreg__(MODE == kM1 ? 
               part[16 * c + r + 8] = prefix ? pick(tot, c, 1) : pick(seg, c, 1);
             }
           } else {
+            // accumulator 4h + {0, 1, 2, 3}: rows 8h + 2c, 8h + 2c + 1 of columns r, r + 8
 #pragma unroll
             for (int t = 0; t < kQuadTiles; ++t) {
               if (t < ntiles) {
-                if (2 * c < rows) {
-                  part[(2 * c) * 64 + 16 * t + r] = prefix ? tot[t][0] : seg[t][0];
-                  part[(2 * c) * 64 + 16 * t + r + 8] = prefix ? tot[t][2] : seg[t][2];
-                }
-                if (2 * c + 1 < rows) {
-                  part[(2 * c + 1) * 64 + 16 * t + r] = prefix ? tot[t][1] : seg[t][1];
-                  part[(2 * c + 1) * 64 + 16 * t + r + 8] = prefix ? tot[t][3] : seg[t][3];
+#pragma unroll
+                for (int h = 0; h < NA / 4; ++h) {
+                  const int r0 = 8 * h + 2 * c;
+                  if (r0 < rows) {
+                    part[r0 * 64 + 16 * t + r] = prefix ? tot[t][4 * h] : seg[t][4 * h];
+                    part[r0 * 64 + 16 * t + r + 8] = prefix ? tot[t][4 * h + 2] : seg[t][4 * h + 2];
+                  }
+                  if (r0 + 1 < rows) {
+                    part[(r0 + 1) * 64 + 16 * t + r] = prefix ? tot[t][4 * h + 1] : seg[t][4 * h + 1];
+                    part[(r0 + 1) * 64 + 16 * t + r + 8] = prefix ? tot[t][4 * h + 3] : seg[t][4 * h + 3];
+                  }
                 }
               }
             }
@@ -706,20 +801,24 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) __maxnreg__(MODE == kM1 ? 
               for (int t = 0; t < kQuadTiles; ++t) {
                 if (t < ntiles) {
                   const int n = n0 + 16 * t + r;
-                  if (2 * c < rows) {
-                    const int i = (2 * c) * m.N + n;
-                    m.y[i] = emit<NORM>(p, i, tot[t][0]);
-                    m.y[i + 8] = emit<NORM>(p, i + 8, tot[t][2]);
-                  }
-                  if (2 * c + 1 < rows) {
-                    const int i = (2 * c + 1) * m.N + n;
-                    m.y[i] = emit<NORM>(p, i, tot[t][1]);
-                    m.y[i + 8] = emit<NORM>(p, i + 8, tot[t][3]);
+#pragma unroll
+                  for (int h = 0; h < NA / 4; ++h) {
+                    const int r0 = 8 * h + 2 * c;
+                    if (r0 < rows) {
+                      const long long i = static_cast<long long>(r0) * m.N + n;
+                      m.y[i] = emit<NORM>(p, i, tot[t][4 * h]);
+                      m.y[i + 8] = emit<NORM>(p, i + 8, tot[t][4 * h + 2]);
+                    }
+                    if (r0 + 1 < rows) {
+                      const long long i = static_cast<long long>(r0 + 1) * m.N + n;
+                      m.y[i] = emit<NORM>(p, i, tot[t][4 * h + 1]);
+                      m.y[i + 8] = emit<NORM>(p, i + 8, tot[t][4 * h + 3]);
+                    }
                   }
                 }
               }
             }
-          } else if (MODE != kMMA && n_pend < 2) {
+          } else if (!multi_row<MODE>() && n_pend < 2) {
             // Split quad at M = 1: its partials are written; the ticket comes after
             // the stream.  (M >= 2: the reduce kernel folds every split quad.)
             const int gq = m.quad_begin + cc.q;
@@ -764,7 +863,7 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW) __maxnreg__(MODE == kM1 ? 
       __syncwarp();
     }
   }  // warp in range
-  if constexpr (MODE == kMMA) return;  // M >= 2: the reduce kernel folds
+  if constexpr (multi_row<MODE>()) return;  // M >= 2: the reduce kernel folds
   __syncthreads();  // orders the fold after the acquiring tickets of this CTA's warps
 
   // ---- fold the completed split quads: one thread per (quad, 4 columns), the
@@ -870,9 +969,10 @@ __device__ __forceinline__ void build_row_class(const uint16_t* xg, int c, int l
 // searches the matrix table (each lookup in the kernel parameters is an L2
 // round trip when it misses the constant cache).
 
-// M >= 2: 8 warps per CTA, one group each; lane (row, c) builds row `row` /
-// lane class c of the group's activation package (rows >= M are zeros).
-template <int MAXMAT>
+// M >= 2: 8 warps per CTA, one group each; lane (row, c) builds rows `row`
+// (and row + 8 for the 16-row package) / lane class c of the group's
+// activation package (rows >= M are zeros).
+template <int MODE, int MAXMAT>
 __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
   // Launched early behind the previous kernel of the stream (programmatic
   // dependent launch): the next kernel may launch at once, but nothing here
@@ -881,7 +981,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Strea
   grid_dependents_launch();
   grid_dependency_wait();
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.status = 0u;
-  constexpr int kRows = Pkg<kMMA>::kRows;
+  constexpr int kRows = Pkg<MODE>::kRows;
   const MatParams& m = mat(p, blockIdx.y);
   // M >= 2 takes no tickets: their array holds each quad's matrix instead, for
   // the reduce kernel (a load from it replaces a search of the matrix table)
@@ -894,10 +994,14 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Strea
   const int lane = threadIdx.x & 31;
   const int row = lane >> 2, c = lane & 3;
   for (int g = 8 * blockIdx.x + (threadIdx.x >> 5); g < G; g += 8 * gridDim.x) {
-    uint8_t* out = m.xpkg + static_cast<long long>(g) * Pkg<kMMA>::kBytes;
-    float* tail = reinterpret_cast<float*>(out + kRows * Pkg<kMMA>::kRowBytes);
-    build_row_class(row < p.M ? m.x + static_cast<long long>(row) * m.K + kGroup * g : nullptr, c, lane,
-                    out + row * Pkg<kMMA>::kRowBytes, tail + 2 * row);
+    uint8_t* out = m.xpkg + static_cast<long long>(g) * Pkg<MODE>::kBytes;
+    float* tail = reinterpret_cast<float*>(out + kRows * Pkg<MODE>::kRowBytes);
+#pragma unroll
+    for (int row8 = 0; row8 < kRows; row8 += 8) {
+      const int rw = row8 + row;
+      build_row_class(rw < p.M ? m.x + static_cast<long long>(rw) * m.K + kGroup * g : nullptr, c, lane,
+                      out + rw * Pkg<MODE>::kRowBytes, tail + 2 * rw);
+    }
   }
 }
 
@@ -940,8 +1044,11 @@ __global__ void __launch_bounds__(32) prep1_kernel(const __grid_constant__ Strea
 constexpr int kMaxRows = W4G128_MAX_M;
 constexpr int kRedChunk = 8;                               // segments per bulk copy
 constexpr int kRedThreads = kMaxRows * 16;                 // one per (row, 4 columns)
-constexpr int kRedStageBytes = kRedChunk * kMaxRows * 64 * 4;  // 16 KB at M = 8
-constexpr int kRedSmem = 2 * kRedStageBytes + 16;          // two stages + two mbarriers
+constexpr int kRedStageBytes = kRedChunk * kMaxRows * 64 * 4;  // the largest stage (M = 16)
+constexpr int kRedSmem = 2 * kRedStageBytes + 16;          // two stages + two mbarriers, at most
+// a call's reduce CTAs: 16 M threads (one per row and 4 columns), two stages of M rows
+__host__ __device__ constexpr int red_threads(int M) { return ((16 * M + 31) / 32) * 32; }
+__host__ __device__ constexpr int red_smem(int M) { return 2 * kRedChunk * M * 64 * 4 + 16; }
 
 template <int MAXMAT, bool NORM>
 __global__ void __launch_bounds__(kRedThreads) reduce_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
@@ -952,7 +1059,7 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(const __grid_consta
   if constexpr (MAXMAT > 1) lo = static_cast<int>(__ldcg(p.tickets + gq));  // written by the prep kernel
   const MatParams& m = mat(p, lo);
   const int q = gq - m.quad_begin;
-  const int G = m.K / kGroup, S = div_up(G, seg_groups<kMMA>()), T = m.N / kTileN;
+  const int G = m.K / kGroup, S = div_up(G, kSegGroups), T = m.N / kTileN;  // the MMA modes' segments
   const long long I = p.total_items;
   const long long q_first = m.item_begin + static_cast<long long>(q) * S;
   const int wf = owner_of(q_first, I, p.W);
@@ -974,7 +1081,7 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(const __grid_consta
   const uint32_t slot_bytes = static_cast<uint32_t>(per_quad) * 4u;
   const int stage_floats = kRedChunk * per_quad;
   const float* buf = reinterpret_cast<const float*>(rsm);
-  const uint32_t buf0 = smem_addr(rsm), bar0 = smem_addr(rsm + 2 * kRedStageBytes);
+  const uint32_t buf0 = smem_addr(rsm), bar0 = smem_addr(rsm + 2 * stage_floats * 4);
   const float* src = p.partials + first * per_quad;
   const int nchunks = div_up(nslot, kRedChunk);
   uint64_t pol = 0;
@@ -1133,7 +1240,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __grid_cons
 
 struct DeviceInfo {
   int sms = 0;
-  int occ[3] = {0, 0, 0};  // CTAs per SM per mode
+  int occ[4] = {0, 0, 0, 0};  // CTAs per SM per mode
   bool ok = false;
 };
 
@@ -1153,10 +1260,11 @@ void setup_mode(DeviceInfo& d) {
   cudaFuncSetAttribute(reduce_kernel<W4G128_MAX_MATRICES, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        kRedSmem);
   int occ1 = 0, occ2 = 0, occ3 = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ1, stream_kernel<MODE, 1, false>, kNW * 32, smem);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, stream_kernel<MODE, W4G128_MAX_MATRICES, false>, kNW * 32,
+  constexpr int threads = cta_warps_max<MODE>() * 32;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ1, stream_kernel<MODE, 1, false>, threads, smem);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, stream_kernel<MODE, W4G128_MAX_MATRICES, false>, threads,
                                                 smem);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ3, stream_kernel<MODE, 1, true>, kNW * 32, smem);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ3, stream_kernel<MODE, 1, true>, threads, smem);
   occ2 = std::min(occ2, occ3);
   const int occ = std::min(occ1, occ2);
   d.occ[MODE] = occ > 0 ? occ : 1;
@@ -1180,6 +1288,7 @@ const DeviceInfo* device_info() {
       setup_mode<kM1>(d);
       setup_mode<kMMA>(d);
       setup_mode<kMMA1>(d);
+      setup_mode<kMMA16>(d);
       if (cudaGetLastError() != cudaSuccess) d.ok = false;
     }
     g_dev[dev] = d;
@@ -1200,9 +1309,9 @@ struct Plan {
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool make_plan(const HostMatrix* mats, int count, int M, bool verify, const DeviceInfo& dev, Plan& pl) {
-  pl.mode = (M > 1) ? kMMA : (verify ? kMMA1 : kM1);
+  pl.mode = (M > 8) ? kMMA16 : (M > 1) ? kMMA : (verify ? kMMA1 : kM1);
   pl.rows = M;
-  pl.pkg = (pl.mode == kMMA) ? Pkg<kMMA>::kBytes : Pkg<kM1>::kBytes;
+  pl.pkg = (pl.mode == kMMA16) ? Pkg<kMMA16>::kBytes : (pl.mode == kMMA) ? Pkg<kMMA>::kBytes : Pkg<kM1>::kBytes;
   pl.item_begin.resize(count);
   pl.quad_begin.resize(count);
   pl.g_begin.resize(count);
@@ -1225,11 +1334,12 @@ bool make_plan(const HostMatrix* mats, int count, int M, bool verify, const Devi
   pl.items = items;
   pl.total_quads = static_cast<int>(quads);
   pl.total_groups = static_cast<int>(groups);
-  const long long max_warps = static_cast<long long>(dev.sms) * dev.occ[pl.mode] * kNW;
+  const int nw = (pl.mode == kMMA16) ? cta_warps_max<kMMA16>() : kNW;
+  const long long max_warps = static_cast<long long>(dev.sms) * dev.occ[pl.mode] * nw;
   pl.W = static_cast<int>(std::min<long long>(items, max_warps));
   // Spread the warps over every SM: a call with fewer items than the grid
   // holds warps gets smaller CTAs rather than fewer SMs.
-  pl.cta_warps = std::min(kNW, div_up(pl.W, dev.sms));
+  pl.cta_warps = std::min(nw, div_up(pl.W, dev.sms));
   pl.grid = div_up(pl.W, pl.cta_warps);
 
   pl.off_tickets = 256;  // after the status word
@@ -1287,9 +1397,9 @@ int launch_mode(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, int max
   cfg.dynamicSmemBytes = 0;
   cudaError_t e;
   cfg.gridDim = dim3(static_cast<unsigned>(std::min(div_up(max_groups, 8), 4096)), static_cast<unsigned>(sp.count));
-  if constexpr (MODE == kMMA) {
+  if constexpr (multi_row<MODE>()) {
     cfg.blockDim = dim3(256);
-    e = cudaLaunchKernelEx(&cfg, prep_kernel<MAXMAT>, sp);
+    e = cudaLaunchKernelEx(&cfg, prep_kernel<MODE, MAXMAT>, sp);
   } else {
     cfg.blockDim = dim3(32);
     e = cudaLaunchKernelEx(&cfg, prep1_kernel<MODE, MAXMAT>, sp);
@@ -1305,10 +1415,10 @@ int launch_mode(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, int max
     cudaGetLastError();
     return W4G128_ERR_CUDA;
   }
-  if (MODE == kMMA) {  // M >= 2: the split quads are folded by the reduce kernel
+  if (multi_row<MODE>()) {  // M >= 2: the split quads are folded by the reduce kernel
     cfg.gridDim = dim3(static_cast<unsigned>(sp.total_quads));  // one CTA per quad
-    cfg.blockDim = dim3(kRedThreads);
-    cfg.dynamicSmemBytes = kRedSmem;
+    cfg.blockDim = dim3(red_threads(sp.M));
+    cfg.dynamicSmemBytes = red_smem(sp.M);
     if (cudaLaunchKernelEx(&cfg, reduce_kernel<MAXMAT, NORM>, sp) != cudaSuccess) {
       cudaGetLastError();
       return W4G128_ERR_CUDA;
@@ -1335,11 +1445,14 @@ int launch_with(const HostMatrix* mats, int count, int M, const Plan& pl, const 
   fill_params(sp, mats, count, M, pl, norm, ws);
   if constexpr (MAXMAT == 1) {
     if (norm != nullptr) {
+      if (pl.mode == kMMA16) return launch_mode<kMMA16, 1, true>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
       if (pl.mode == kMMA) return launch_mode<kMMA, 1, true>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
       if (pl.mode == kMMA1) return launch_mode<kMMA1, 1, true>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
       return launch_mode<kM1, 1, true>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
     }
   }
+  if (pl.mode == kMMA16)
+    return launch_mode<kMMA16, MAXMAT, false>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
   if (pl.mode == kMMA) return launch_mode<kMMA, MAXMAT, false>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
   if (pl.mode == kMMA1) return launch_mode<kMMA1, MAXMAT, false>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
   return launch_mode<kM1, MAXMAT, false>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);

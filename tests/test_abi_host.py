@@ -53,7 +53,7 @@ def test_gemv_argument_errors(L):
 
 
 def test_verify_argument_errors(L):
-    for M in (0, 9, -1):
+    for M in (0, 17, -1):
         assert L.w4g128_gemm_verify(FAKE, FAKE, FAKE, M, 128, 16, FAKE, 1 << 20, None) == E_INVALID
 
 
@@ -74,7 +74,7 @@ def test_add_rmsnorm_argument_errors(L):
     assert call(out=H) == E_INVALID          # out is h
     assert call(out=R) == E_INVALID          # out is the residual
     assert call(x=H) == E_INVALID            # h is x
-    assert call(M=9) == E_INVALID
+    assert call(M=17) == E_INVALID
     assert call(N=24) == E_SHAPE
     assert call(gam=G + 2) == E_ALIGN
     assert call(res=R + 2) == E_ALIGN

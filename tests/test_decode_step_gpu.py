@@ -26,7 +26,7 @@ def decode_step(mats, xs, M):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("M", [1, 2, 8])
+@pytest.mark.parametrize("M", [1, 2, 8, 11, 16])
 def test_decode_step_equals_separate_calls(M):
     shapes = [(128, 16), (640, 80), (4096, 4096), (1152, 208), (2048, 1024), (384, 48)]
     mats = [DevMatrix(K, N, matrix_id=200 + i) for i, (K, N) in enumerate(shapes)]

@@ -51,7 +51,7 @@ def check(mat, x, res, gam, h, out, eps=EPS):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("verify", [0, 1])
-@pytest.mark.parametrize("M", [1, 2, 5, 8])
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 16])
 @pytest.mark.parametrize("K,N", [(128, 16), (640, 80), (1152, 208), (4096, 4096)])
 def test_add_rmsnorm_matches_oracle(K, N, M, verify):
     mat = DevMatrix(K, N, matrix_id=7 * N + M)
@@ -137,11 +137,11 @@ def test_in_place_and_deterministic(M):
 @pytest.mark.parametrize("K,N", [(640, 80), (17408, 5120)])
 def test_verify_rows_independent_of_m(K, N):
     """With the verify arithmetic, row m of h and out equals the one-row call on
-    row m (the norm's order depends on N alone)."""
+    row m (the norm's order depends on N alone), for 8 and 16 rows."""
     mat = DevMatrix(K, N, matrix_id=29)
-    x, res, gam = inputs(mat, 8, 29)
+    x, res, gam = inputs(mat, 16, 29)
     h8, o8 = fused(mat, x, res, gam, verify=1)
-    for r in (0, 3, 7):
+    for r in (0, 3, 7, 8, 15):
         h1, o1 = fused(mat, x[r:r + 1], res[r:r + 1], gam, verify=1)
         assert np.array_equal(h1[0], h8[r]) and np.array_equal(o1[0], o8[r])
 

@@ -1,4 +1,4 @@
-"""M-row speculative verify (w4g128_gemm_verify, 1 <= M <= 8) against the fp64
+"""M-row speculative verify (w4g128_gemm_verify, 1 <= M <= 16) against the fp64
 oracle, plus exact cases and row consistency."""
 import numpy as np
 import pytest
@@ -11,7 +11,7 @@ from gpu_helpers import SEED, DevMatrix, check_against_oracle, run  # noqa: E402
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8, 9, 12, 16])
 @pytest.mark.parametrize("K,N", [(128, 16), (640, 80), (1152, 208), (4096, 4096)])
 def test_verify_matches_oracle(M, K, N):
     mat = DevMatrix(K, N, matrix_id=N + M)
@@ -28,10 +28,11 @@ def test_verify_projection_shapes_m8(K, N):
 
 
 @pytest.mark.gpu
-def test_verify_exact_integer_case_bit_exact():
+@pytest.mark.parametrize("M", [8, 16])
+def test_verify_exact_integer_case_bit_exact(M):
     rng = np.random.default_rng(31)
     O = oracle.Oracle()
-    K, N, M = 1024, 144, 8
+    K, N = 1024, 144
     q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
     codes = O.pack_canonical(q)
     s = np.full((K // 128, N), 0x3F80, np.uint16)
@@ -58,12 +59,13 @@ def test_verify_identical_rows_give_identical_outputs():
 @pytest.mark.parametrize("K,N", [(128, 16), (640, 80), (1152, 208), (5120, 6144), (17408, 5120)])
 def test_verify_rows_bitwise_equal_single_row_verify(K, N):
     """Row m of an M-row verify equals a verify of row m alone (M = 1), bit for
-    bit, for every M in 1..8: the exact speculative-decoding property."""
+    bit, for every M in 1..16 (both the one-tile and the two-tile MMA): the
+    exact speculative-decoding property."""
     mat = DevMatrix(K, N, matrix_id=6 + K)
-    x8 = synth.x(SEED, 6 + N, 8, K)
-    single = [run(mat, x8[m:m + 1], verify=True)[0] for m in range(8)]
-    for M in range(1, 9):
-        yM = run(mat, x8[:M], verify=True)
+    x16 = synth.x(SEED, 6 + N, 16, K)
+    single = [run(mat, x16[m:m + 1], verify=True)[0] for m in range(16)]
+    for M in range(1, 17):
+        yM = run(mat, x16[:M], verify=True)
         for m in range(M):
             assert np.array_equal(yM[m], single[m]), (M, m)
 
@@ -90,7 +92,7 @@ def _wide_range_x(rng, M, K):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("M", [1, 2, 8])
+@pytest.mark.parametrize("M", [1, 2, 8, 16])
 def test_wide_dynamic_range_x(M):
     """The kernels carry x into fp16 with one power of two per (group, row);
     values far below a group's largest, zero groups and huge values must all
@@ -101,3 +103,12 @@ def test_wide_dynamic_range_x(M):
     check_against_oracle(run(mat, x), x, mat.codes, mat.scales, mat.mins)
     if M == 1:
         check_against_oracle(run(mat, x, verify=True), x, mat.codes, mat.scales, mat.mins)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("K,N", [(5120, 6144), (17408, 5120)])
+def test_verify_projection_shapes_m16(K, N):
+    """Sixteen draft rows (two MMA x tiles) on full layer shapes."""
+    mat = DevMatrix(K, N, matrix_id=N + 16)
+    x = synth.x(SEED, 2100 + K, 16, K)
+    check_against_oracle(run(mat, x), x, mat.codes, mat.scales, mat.mins)
