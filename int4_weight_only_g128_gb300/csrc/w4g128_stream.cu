@@ -401,7 +401,7 @@ __device__ __forceinline__ uint16_t to_bf16(float v) { return __bfloat16_as_usho
 // thread that writes it, so h may overwrite the residual in place.
 template <bool NORM, int MAXMAT>
 __device__ __forceinline__ uint16_t emit(const StreamParams<MAXMAT>& p, long long i, float v) {
-  if constexpr (NORM) v = __fadd_rn(v, __uint_as_float(static_cast<uint32_t>(p.residual[i]) << 16));
+  if constexpr (NORM) v = __fadd_rn(v, __uint_as_float(static_cast<uint32_t>(__ldcg(p.residual + i)) << 16));
   return to_bf16(v);
 }
 
@@ -409,7 +409,7 @@ __device__ __forceinline__ uint16_t emit(const StreamParams<MAXMAT>& p, long lon
 // the norm); loaded ahead of the sums it is added to.
 template <bool NORM, int MAXMAT>
 __device__ __forceinline__ uint32_t residual2(const StreamParams<MAXMAT>& p, long long i) {
-  if constexpr (NORM) return *reinterpret_cast<const uint32_t*>(p.residual + i);
+  if constexpr (NORM) return __ldcg(reinterpret_cast<const uint32_t*>(p.residual + i));
   else return 0u;
 }
 
@@ -915,12 +915,13 @@ __device__ __forceinline__ void build_row_class(const uint16_t* xg, int c, int l
   uint32_t amax = 0u;  // largest |x| among them, as bf16 magnitude bits
   if (xg != nullptr) {
     // x rows start 4-byte aligned (K even, x 4-byte aligned): one 32-bit
-    // load per operand pair
+    // load per operand pair, through L2: x may be the output of the kernel
+    // this one was launched behind, written while this CTA was resident
     const uint32_t* xr = reinterpret_cast<const uint32_t*>(xg);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      w[2 * i] = xr[8 * i + c];
-      w[2 * i + 1] = xr[8 * i + c + 4];
+      w[2 * i] = __ldcg(xr + 8 * i + c);
+      w[2 * i + 1] = __ldcg(xr + 8 * i + c + 4);
     }
     uint32_t mag2 = 0u;  // per-half maxima of |x| bits
 #pragma unroll
