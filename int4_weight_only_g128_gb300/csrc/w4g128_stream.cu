@@ -970,7 +970,7 @@ __device__ __forceinline__ void build_row_class(const uint16_t* xg, int c, int l
 // searches the matrix table (each lookup in the kernel parameters is an L2
 // round trip when it misses the constant cache).
 
-// M >= 2: 8 warps per CTA, one group each; lane (row, c) builds rows `row`
+// M >= 2: one group per warp; lane (row, c) builds rows `row`
 // (and row + 8 for the 16-row package) / lane class c of the group's
 // activation package (rows >= M are zeros).
 template <int MODE, int MAXMAT>
@@ -994,7 +994,8 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Strea
   const int G = m.K / kGroup;
   const int lane = threadIdx.x & 31;
   const int row = lane >> 2, c = lane & 3;
-  for (int g = 8 * blockIdx.x + (threadIdx.x >> 5); g < G; g += 8 * gridDim.x) {
+  const int nwarp = blockDim.x >> 5;
+  for (int g = nwarp * blockIdx.x + (threadIdx.x >> 5); g < G; g += nwarp * gridDim.x) {
     uint8_t* out = m.xpkg + static_cast<long long>(g) * Pkg<MODE>::kBytes;
     float* tail = reinterpret_cast<float*>(out + kRows * Pkg<MODE>::kRowBytes);
 #pragma unroll
