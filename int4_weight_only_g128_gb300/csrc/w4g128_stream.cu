@@ -1,7 +1,7 @@
 // The weight-streaming kernels: y_i = x_i . dequant(W_i) for a list of
-// int4-g128 matrices -- M = 1 decode on CUDA cores, the M <= 8 verify (M = 1
+// int4-g128 matrices -- M = 1 decode on CUDA cores, the M <= 16 verify (M = 1
 // included, so that its rows match bit for bit whatever M) on the warp-level
-// MMA.
+// MMA -- and the optional residual add + RMS norm the product feeds.
 //
 // Design (sm_103a, one GPU):
 //  * The work is a flat list of items (matrix, 64-column quad, segment of 4
@@ -31,6 +31,13 @@
 //    programmatic dependent launch) turns x into per-group packages in the
 //    order the lanes consume them, with the group sums the factorised
 //    dequantisation needs, and clears the status word and the tickets.
+//    Every kernel of a call is a programmatic dependent launch, the prep
+//    kernel too (behind whatever precedes it; it waits for that to finish
+//    before it touches anything), so a call's launches overlap the previous
+//    call's tail.
+//  * Kernel parameters are read at fixed offsets where possible: a lookup in
+//    the matrix table with a computed index is an L2 round trip whenever it
+//    misses the constant cache, and on the critical path those add up.
 //
 // Dequantisation uses the factorised form of w = min + q*scale over a group g:
 //     sum_{k in g} x_k w_kn = scale_gn * sum_k x_k q_kn + min_gn * X_g,
