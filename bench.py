@@ -334,13 +334,22 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     def make_io(M):
+        # the six x (and the six y) are slices of one contiguous buffer, 256-byte
+        # aligned, so that the end-to-end run moves each direction in one copy
         xs_h = [synth.x(SEED, (100 if M == 1 else 200) + i, M, K) for i, (_, K, _) in enumerate(LAYER)]
-        xs = [torch.from_numpy(x.view(np.int16)).cuda() for x in xs_h]
-        ys = [torch.empty(M * N, dtype=torch.int16, device="cuda") for _, _, N in LAYER]
+        up = lambda n: -(-n // 128) * 128
+        xoff = np.cumsum([0] + [up(x.size) for x in xs_h])
+        yoff = np.cumsum([0] + [up(M * N) for _, _, N in LAYER])
+        x_all = torch.zeros(int(xoff[-1]), dtype=torch.int16, device="cuda")
+        y_all = torch.zeros(int(yoff[-1]), dtype=torch.int16, device="cuda")
+        xs = [x_all[xoff[i]:xoff[i] + x.size] for i, x in enumerate(xs_h)]
+        for xd, x in zip(xs, xs_h):
+            xd.copy_(torch.from_numpy(x.reshape(-1).view(np.int16)))
+        ys = [y_all[yoff[i]:yoff[i] + M * N] for i, (_, _, N) in enumerate(LAYER)]
         descs = [[(copies[c][i], xs[i], ys[i], K, N) for i, (_, K, N) in enumerate(LAYER)] for c in range(NCOPY)]
         nb = max(w.w4g128_decode_step_workspace_bytes(d, M) for d in descs)
         ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
-        return xs_h, xs, ys, descs, ws
+        return xs_h, xs, ys, descs, ws, x_all, y_all
 
     MS = (1, 2, 4, 8, 16)
     io = {M: make_io(M) for M in MS}
@@ -350,7 +359,7 @@ def run_ours(args):
     O = oracle.Oracle()
     worst = {}
     for M in MS:
-        xs_h, xs, ys, descs, ws = io[M]
+        xs_h, xs, ys, descs, ws = io[M][:5]
         for c in (0, NCOPY - 1):
             w.w4g128_decode_step(descs[c], M, ws, stream=st)
             torch.cuda.synchronize()
@@ -385,7 +394,7 @@ def run_ours(args):
     def timed_graph(M, steps, warmup):
         """Replays a graph of `steps` decode_step calls (rotating weight copies);
         returns the max-over-ranks seconds of the whole replay."""
-        _, _, _, descs, ws = io[M]
+        _, _, _, descs, ws = io[M][:5]
         for i in range(warmup):
             w.w4g128_decode_step(descs[i % NCOPY], M, ws, stream=st)
         torch.cuda.synchronize()
@@ -407,7 +416,7 @@ def run_ours(args):
     clocks = ClockSampler(local)
     clocks.start()
     t_soak = time.perf_counter()
-    _, _, _, descs1, ws1 = io[1]
+    _, _, _, descs1, ws1 = io[1][:5]
     k = 0
     while time.perf_counter() - t_soak < args.soak:
         for _ in range(200):
@@ -423,7 +432,7 @@ def run_ours(args):
     # 126 MB L2 holds part of it between steps)
     l2_warm = {}
     for M in (1, 8):
-        _, _, _, descs_w, ws_w = io[M]
+        _, _, _, descs_w, ws_w = io[M][:5]
         g = capture([lambda cs: w.w4g128_decode_step(descs_w[0], M, ws_w, stream=cs) for _ in range(50)])
         g.replay()
         torch.cuda.synchronize()
@@ -599,12 +608,13 @@ def run_ours(args):
     probe["copy_GBps_read_plus_write"] = round(10 * 2 * half / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
     del buf, src, dst
 
-    # ---- end to end through host buffers: pinned x in, y out, every step, eager C-ABI calls
-    xs_h, xs, ys, descs, ws = io[1]
-    x_pin = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in xs_h]
-    y_pin = [torch.empty(y.numel(), dtype=torch.int16).pin_memory() for y in ys]
-    h2d = sum(x.numel() * 2 for x in x_pin)
-    d2h = sum(y.numel() * 2 for y in y_pin)
+    # ---- end to end through host buffers: pinned x in, y out, every step, eager C-ABI calls;
+    # the layer's x and y each live in one contiguous buffer, moved in one copy per direction
+    xs_h, xs, ys, descs, ws, x_all, y_all = io[1]
+    x_pin = x_all.cpu().pin_memory()
+    y_pin = torch.empty(y_all.numel(), dtype=torch.int16).pin_memory()
+    h2d = x_pin.numel() * 2
+    d2h = y_pin.numel() * 2
     for i in range(args.warmup):
         w.w4g128_decode_step(descs[i % NCOPY], 1, ws, stream=st)
     barrier()
@@ -612,11 +622,9 @@ def run_ours(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
-        for xd, xp in zip(xs, x_pin):
-            xd.copy_(xp, non_blocking=True)
+        x_all.copy_(x_pin, non_blocking=True)
         w.w4g128_decode_step(descs[i % NCOPY], 1, ws, stream=st)
-        for yd, yp in zip(ys, y_pin):
-            yp.copy_(yd, non_blocking=True)
+        y_pin.copy_(y_all, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
