@@ -1,7 +1,7 @@
 // Inline-PTX building blocks for the sm_103a kernels: mbarriers, 1-D bulk
-// (TMA) copies global -> shared, programmatic-dependent-launch control and a
-// bounded wait.  Every wait here is bounded by the global nanosecond timer so
-// that no kernel of this library can spin forever.
+// (TMA) copies global -> shared, programmatic-dependent-launch control,
+// relaxed flag words and bounded waits.  Every wait here is bounded by the
+// global nanosecond timer so that no kernel of this library can spin forever.
 #pragma once
 #include <cstdint>
 
@@ -60,6 +60,31 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// Relaxed GPU-scope access to a 64-bit word in global memory (single-copy
+// atomic: a reader sees the old value or the new one, never a mix).
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* a) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* a, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(a), "l"(v) : "memory");
+}
+
+// Bounded wait until the word at `a` is nonzero; its last value goes to
+// `seen`.  Returns false if that did not happen within kWaitLimitNs.
+__device__ __forceinline__ bool wait_nonzero_bounded(const unsigned long long* a, unsigned long long& seen) {
+  seen = ld_relaxed_u64(a);
+  if (seen != 0ull) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    __nanosleep(64);
+    seen = ld_relaxed_u64(a);
+    if (seen != 0ull) return true;
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
 }

@@ -24,9 +24,12 @@
 //        after its stream; the CTA holding a quad's last ticket folds it with
 //        all its threads once its warps are done -- no warp stalls mid-stream;
 //      - M >= 2: by a reduce kernel launched right behind the streaming
-//        kernel (programmatic dependent launch), one CTA per split quad
-//        pulling its slots into shared memory with bulk copies, since 64*M
-//        outputs per quad would tie up the SMs that finish last.
+//        kernel (programmatic dependent launch), since 64*M outputs per quad
+//        would tie up the SMs that finish last: one CTA per quad pulling a
+//        split quad's slots into shared memory with bulk copies, or, for
+//        calls with many more quads (mostly owned) than that grid holds at
+//        once, one CTA per streaming warp folding the quad that warp's range
+//        starts in when the quad began in the warp before.
 //  * A small prep kernel (launched first; the streaming kernel overlaps it by
 //    programmatic dependent launch) turns x into per-group packages in the
 //    order the lanes consume them, with the group sums the factorised
@@ -162,11 +165,25 @@ struct MatParams {
   int g_begin;           // first (matrix, group) package index of this matrix
 };
 
+// M >= 2: warp w's split-quad record, one 64-bit word written (relaxed) at
+// the start of its stream after the prep kernel has cleared it: bit 63 set
+// once written; bit 62 set if the quad w's range starts in began in warp
+// w - 1, so every split quad is named by exactly one record, its second
+// warp's; then the quad's matrix (bits 44..52), its index in the matrix
+// (bits 20..43) and the segment w starts at (bits 0..19).
+constexpr unsigned long long kRecWritten = 1ull << 63, kRecSplit = 1ull << 62;
+__host__ __device__ constexpr unsigned long long split_rec(bool split, int mi, int q, int s) {
+  return kRecWritten | (split ? kRecSplit : 0ull) | (static_cast<unsigned long long>(mi) << 44) |
+         (static_cast<unsigned long long>(q) << 20) | static_cast<unsigned long long>(s);
+}
+static_assert(W4G128_MAX_MATRICES <= 512, "9 bits of matrix index in a split-quad record");
+
 template <int MAXMAT>
 struct StreamParams {
   long long total_items;
   float* partials;       // [total_items][rows][64]: one slot per (matrix, quad, segment)
-  unsigned* tickets;     // [total_quads] arrival counters (M = 1)
+  unsigned* tickets;     // [total_quads] arrival counters of split quads (M = 1) / matrix of each quad (M >= 2)
+  unsigned long long* recs;  // [W] split-quad records (M >= 2)
   unsigned* status;
   // The residual add + RMS norm call (one matrix; residual == nullptr
   // otherwise): its y is h = residual + x W, and the norm kernel writes
@@ -176,6 +193,7 @@ struct StreamParams {
   uint16_t* nout;
   float eps;
   int count, M, W, total_quads, total_groups;
+  int per_warp_reduce;   // M >= 2: the split quads are folded per streaming warp (else per quad)
   MatParams mats[MAXMAT];
 };
 
@@ -686,6 +704,12 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
     // M >= 2: the reduce kernel may start launching now; it waits for this
     // grid to finish before it reads any partial.
     grid_dependents_launch();
+    if (multi_row<MODE>() && MAXMAT > 1 && p.per_warp_reduce && lane == 0) {
+      // this warp's split-quad record (the prep kernel has cleared it): does
+      // the quad its range starts in begin in warp wg - 1?
+      const bool split = cc.s != 0 && it_a - cc.s >= I * (wg - 1) / p.W;
+      st_relaxed_u64(p.recs + wg, split_rec(split, cc.mi, cc.q, cc.s));
+    }
 
     float seg[kQuadTiles][NA];
     float tot[kQuadTiles][NA];
@@ -996,12 +1020,20 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Strea
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.status = 0u;
   constexpr int kRows = Pkg<MODE>::kRows;
   const MatParams& m = mat(p, blockIdx.y);
-  // M >= 2 takes no tickets: their array holds each quad's matrix instead, for
-  // the reduce kernel (a load from it replaces a search of the matrix table)
+  // M >= 2 takes no tickets.  For the per-quad reduce their array holds each
+  // quad's matrix instead (a load from it replaces a search of the matrix
+  // table); for the per-warp reduce the streaming warps' split-quad records
+  // are cleared, over the whole grid.
   if constexpr (MAXMAT > 1) {
-    const int nq = div_up(m.N, kQuadTiles * kTileN);
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nq; i += gridDim.x * blockDim.x)
-      p.tickets[m.quad_begin + i] = blockIdx.y;
+    if (p.per_warp_reduce) {
+      const int nthr = gridDim.x * gridDim.y * blockDim.x;
+      for (int i = (blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x; i < p.W; i += nthr)
+        p.recs[i] = 0ull;
+    } else {
+      const int nq = div_up(m.N, kQuadTiles * kTileN);
+      for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nq; i += gridDim.x * blockDim.x)
+        p.tickets[m.quad_begin + i] = blockIdx.y;
+    }
   }
   const int G = m.K / kGroup;
   const int lane = threadIdx.x & 31;
@@ -1048,7 +1080,9 @@ __global__ void __launch_bounds__(32) prep1_kernel(const __grid_constant__ Strea
 // ----------------------------------------------------------------- reduce kernel
 
 // M >= 2: folds the segment partials of every quad the schedule split between
-// warps.  One CTA per quad: the quad's partial slots -- the fold of the
+// warps.  Two forms; a call takes the one with the smaller grid.
+//
+// Per quad (calls with no more quads than streaming warps): one CTA per quad: the quad's partial slots -- the fold of the
 // segments its first warp held, then one slot per later segment -- are one
 // contiguous run of M x 64 fp32 slots, pulled into shared memory by 1-D bulk
 // copies of up to kRedChunk slots (two stages), and each thread folds one
@@ -1065,7 +1099,7 @@ __host__ __device__ constexpr int red_threads(int M) { return ((16 * M + 31) / 3
 __host__ __device__ constexpr int red_smem(int M) { return 2 * kRedChunk * M * 64 * 4 + 16; }
 
 template <int MAXMAT, bool NORM>
-__global__ void __launch_bounds__(kRedThreads) reduce_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
+__global__ void __launch_bounds__(kRedThreads) reduce_quads_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
   extern __shared__ __align__(128) uint8_t rsm[];
   __shared__ int ok;
   const int gq = blockIdx.x;
@@ -1158,6 +1192,88 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(const __grid_consta
     yo[0] = emit2<NORM>(acc.x, acc.y, r0);
     yo[1] = emit2<NORM>(acc.z, acc.w, r1);
   }
+}
+
+// Per streaming warp (calls with more quads than warps: most quads are owned
+// by one warp, and a grid over quads would be mostly idle CTAs): one CTA per
+// streaming warp w.  If the quad w's range starts in began in warp w - 1, w
+// is the quad's second warp and its CTA folds the quad: the slots run from
+// w - 1's last item (its prefix fold) to the quad's last segment.  With one
+// matrix the CTA works out w's quad from the schedule; with several it reads
+// w's record (no search of the matrix table).  Both happen before the wait.
+constexpr int kRedBatch = 8;  // partial loads in flight per thread (register budget)
+
+template <int MAXMAT, bool NORM>
+__global__ void __launch_bounds__(kRedThreads) reduce_warps_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
+  // as in reduce_quads_kernel: every CTA that folds waits for the streaming
+  // grid, and so does the last
+  grid_dependents_launch();
+  const int w = blockIdx.x;
+  const long long I = p.total_items;
+  const long long it_a = I * w / p.W;
+  bool split = false;
+  int mi = 0, q = 0, s = 0;
+  if constexpr (MAXMAT > 1) {
+    __shared__ unsigned long long rec_s;
+    if (threadIdx.x == 0) {
+      unsigned long long r = 0ull;
+      if (!wait_nonzero_bounded(p.recs + w, r)) atomicCAS(p.status, 0u, static_cast<unsigned>(W4G128_ERR_TIMEOUT));
+      rec_s = r;
+    }
+    __syncthreads();
+    const unsigned long long rec = rec_s;
+    split = (rec & kRecSplit) != 0;
+    mi = static_cast<int>((rec >> 44) & 0x1FF);
+    q = static_cast<int>((rec >> 20) & 0xFFFFFF);
+    s = static_cast<int>(rec & 0xFFFFF);
+  } else if (w > 0) {
+    const int S = div_up(p.mats[0].K / kGroup, kSegGroups);
+    q = static_cast<int>(it_a / S);
+    s = static_cast<int>(it_a - static_cast<long long>(q) * S);
+    split = s != 0 && it_a - s >= I * (w - 1) / p.W;
+  }
+  if (!split) {
+    if (blockIdx.x + 1 == gridDim.x) grid_dependency_wait();
+    return;
+  }
+  const MatParams& m = mat(p, mi);
+  const int S = div_up(m.K / kGroup, kSegGroups);
+  const int nslot = S - s + 1;
+  const int cols = kTileN * min(kQuadTiles, m.N / kTileN - kQuadTiles * q);
+  const int u = threadIdx.x, row = u >> 4, col = 4 * (u & 15);
+  const bool active = row < p.M && col < cols;
+  const long long i = static_cast<long long>(row) * m.N + kQuadTiles * kTileN * q + col;
+  uint32_t r0 = 0u, r1 = 0u;  // the residual, loaded before the wait
+  if (active) {
+    r0 = residual2<NORM>(p, i);
+    r1 = residual2<NORM>(p, i + 2);
+  }
+  uint16_t* y = m.y;
+  grid_dependency_wait();  // every partial of the streaming kernel is written and visible
+  if (!active) return;
+  const int per_quad = p.M * 64;  // floats per partial slot
+  const float4* part = reinterpret_cast<const float4*>(p.partials + (it_a - 1) * per_quad + row * 64 + col);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < nslot; s0 += kRedBatch) {  // kRedBatch slots in flight, then fold in order
+    float4 v[kRedBatch];
+#pragma unroll
+    for (int k = 0; k < kRedBatch; ++k)
+      v[k] = (s0 + k < nslot) ? __ldcg(part + static_cast<long long>(s0 + k) * (per_quad / 4))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kRedBatch; ++k) {
+      if (s0 + k < nslot) {
+        if (s0 + k == 0) {
+          acc = v[k];
+        } else {
+          acc.x += v[k].x; acc.y += v[k].y; acc.z += v[k].z; acc.w += v[k].w;
+        }
+      }
+    }
+  }
+  uint32_t* yo = reinterpret_cast<uint32_t*>(y + i);
+  yo[0] = emit2<NORM>(acc.x, acc.y, r0);
+  yo[1] = emit2<NORM>(acc.z, acc.w, r1);
 }
 
 // ----------------------------------------------------------------- RMS norm kernel
@@ -1254,7 +1370,8 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __grid_cons
 
 struct DeviceInfo {
   int sms = 0;
-  int occ[4] = {0, 0, 0, 0};  // CTAs per SM per mode
+  int occ[4] = {0, 0, 0, 0};        // CTAs per SM per mode
+  int red_occ[kMaxRows + 1] = {};   // per-quad reduce CTAs per SM per M
   bool ok = false;
 };
 
@@ -1270,10 +1387,11 @@ void setup_mode(DeviceInfo& d) {
   cudaFuncSetAttribute(stream_kernel<MODE, kFewMatrices, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   cudaFuncSetAttribute(stream_kernel<MODE, W4G128_MAX_MATRICES, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        smem);
-  cudaFuncSetAttribute(reduce_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRedSmem);
-  cudaFuncSetAttribute(reduce_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRedSmem);
-  cudaFuncSetAttribute(reduce_kernel<kFewMatrices, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRedSmem);
-  cudaFuncSetAttribute(reduce_kernel<W4G128_MAX_MATRICES, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaFuncSetAttribute(reduce_quads_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRedSmem);
+  cudaFuncSetAttribute(reduce_quads_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRedSmem);
+  cudaFuncSetAttribute(reduce_quads_kernel<kFewMatrices, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       kRedSmem);
+  cudaFuncSetAttribute(reduce_quads_kernel<W4G128_MAX_MATRICES, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        kRedSmem);
   int occ1 = 0, occ2 = 0, occ3 = 0;
   constexpr int threads = cta_warps_max<MODE>() * 32;
@@ -1305,6 +1423,12 @@ const DeviceInfo* device_info() {
       setup_mode<kMMA>(d);
       setup_mode<kMMA1>(d);
       setup_mode<kMMA16>(d);
+      for (int M = 2; M <= kMaxRows; ++M) {
+        int n = 0;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, reduce_quads_kernel<W4G128_MAX_MATRICES, false>,
+                                                      red_threads(M), red_smem(M));
+        d.red_occ[M] = n > 0 ? n : 1;
+      }
       if (cudaGetLastError() != cudaSuccess) d.ok = false;
     }
     g_dev[dev] = d;
@@ -1315,9 +1439,10 @@ const DeviceInfo* device_info() {
 
 struct Plan {
   int mode = 0, rows = 1, pkg = 0;
+  bool per_warp_reduce = false;
   long long items = 0;
   int W = 0, grid = 0, cta_warps = kNW, total_quads = 0, total_groups = 0, max_groups = 0;
-  size_t off_tickets = 0, off_xpkg = 0, off_partials = 0, bytes = 0;
+  size_t off_tickets = 0, off_recs = 0, off_xpkg = 0, off_partials = 0, bytes = 0;
   std::vector<long long> item_begin, xpkg_off;
   std::vector<int> quad_begin, g_begin;
 };
@@ -1357,9 +1482,14 @@ bool make_plan(const HostMatrix* mats, int count, int M, bool verify, const Devi
   // holds warps gets smaller CTAs rather than fewer SMs.
   pl.cta_warps = std::min(nw, div_up(pl.W, dev.sms));
   pl.grid = div_up(pl.W, pl.cta_warps);
+  // M >= 2: fold per quad unless that grid is larger than one streaming warp
+  // each and than one wave of resident reduce CTAs
+  pl.per_warp_reduce = M >= 2 && pl.total_quads > pl.W &&
+                       static_cast<long long>(pl.total_quads) > static_cast<long long>(dev.red_occ[M]) * dev.sms;
 
   pl.off_tickets = 256;  // after the status word
-  pl.off_xpkg = align_up(pl.off_tickets + sizeof(unsigned) * static_cast<size_t>(quads), 256);
+  pl.off_recs = align_up(pl.off_tickets + sizeof(unsigned) * static_cast<size_t>(quads), 256);
+  pl.off_xpkg = align_up(pl.off_recs + sizeof(unsigned long long) * static_cast<size_t>(pl.W), 256);
   pl.off_partials = align_up(pl.off_xpkg + static_cast<size_t>(xbytes), 256);
   pl.bytes = align_up(pl.off_partials + sizeof(float) * static_cast<size_t>(items) * pl.rows * 64, 256);
   return true;
@@ -1372,6 +1502,7 @@ void fill_params(StreamParams<MAXMAT>& sp, const HostMatrix* mats, int count, in
   sp.total_items = pl.items;
   sp.partials = reinterpret_cast<float*>(base + pl.off_partials);
   sp.tickets = reinterpret_cast<unsigned*>(base + pl.off_tickets);
+  sp.recs = reinterpret_cast<unsigned long long*>(base + pl.off_recs);
   sp.status = reinterpret_cast<unsigned*>(base);
   sp.residual = norm ? norm->residual : nullptr;
   sp.gamma = norm ? norm->gamma : nullptr;
@@ -1380,6 +1511,7 @@ void fill_params(StreamParams<MAXMAT>& sp, const HostMatrix* mats, int count, in
   sp.count = count;
   sp.M = M;
   sp.W = pl.W;
+  sp.per_warp_reduce = pl.per_warp_reduce ? 1 : 0;
   sp.total_quads = pl.total_quads;
   sp.total_groups = pl.total_groups;
   for (int i = 0; i < count; ++i) {
@@ -1432,10 +1564,18 @@ int launch_mode(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, int max
     return W4G128_ERR_CUDA;
   }
   if (multi_row<MODE>()) {  // M >= 2: the split quads are folded by the reduce kernel
-    cfg.gridDim = dim3(static_cast<unsigned>(sp.total_quads));  // one CTA per quad
+    cudaError_t er;
     cfg.blockDim = dim3(red_threads(sp.M));
-    cfg.dynamicSmemBytes = red_smem(sp.M);
-    if (cudaLaunchKernelEx(&cfg, reduce_kernel<MAXMAT, NORM>, sp) != cudaSuccess) {
+    if (sp.per_warp_reduce) {
+      cfg.gridDim = dim3(static_cast<unsigned>(sp.W));  // one CTA per streaming warp
+      cfg.dynamicSmemBytes = 0;
+      er = cudaLaunchKernelEx(&cfg, reduce_warps_kernel<MAXMAT, NORM>, sp);
+    } else {
+      cfg.gridDim = dim3(static_cast<unsigned>(sp.total_quads));  // one CTA per quad
+      cfg.dynamicSmemBytes = red_smem(sp.M);
+      er = cudaLaunchKernelEx(&cfg, reduce_quads_kernel<MAXMAT, NORM>, sp);
+    }
+    if (er != cudaSuccess) {
       cudaGetLastError();
       return W4G128_ERR_CUDA;
     }
