@@ -663,7 +663,7 @@ def run_ours(args):
                      "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
                      "peak_source": ("measured copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                                      if peak_kind == "measured" else "fallback 6.8 TB/s"),
-                     "kernel": "stream_kernel (M=1 CUDA-core path) + its prep kernel, per decode_step call"},
+                     "kernel": "stream_kernel (M=1, one-row warp-MMA path) + its prep kernel, per decode_step call"},
         "m8": {"value": round(value8, 1), "unit": "GB/s", "ms_per_step": round(1e3 * total8 / args.steps, 5),
                "achieved": round(achieved8, 1), "frac": round(achieved8 / peak, 4),
                "verify_cost_ratio_t8_over_t1": round(total8 / total1, 4)},

@@ -146,9 +146,11 @@ W4G128_API int w4g128_quantize(const w4g128_bf16* w, int K, int N, int search, u
  * device (and by w4g128_gemv, M = 1).  Returns 0 for invalid arguments. */
 W4G128_API size_t w4g128_workspace_bytes(int M, int K, int N);
 
-/* y[1][N] = x[1][K] . dequant(W): the batch-1 decode GEMV (CUDA cores,
- * streamed by TMA bulk copies, split-K with a deterministic last-arriver
- * reduction).  Token Rush README, progress table steps 3 and 8-9. */
+/* y[1][N] = x[1][K] . dequant(W): the batch-1 decode GEMV (streamed by TMA
+ * bulk copies, the dequantised weights fed to the warp MMA with the one x row
+ * in every B column, split-K with a deterministic last-arriver reduction).
+ * Bitwise identical to w4g128_gemm_verify at M = 1.  Token Rush README,
+ * progress table steps 3 and 8-9. */
 W4G128_API int w4g128_gemv(const void* packed, const w4g128_bf16* x, w4g128_bf16* y, int K, int N,
                            void* ws, size_t ws_bytes, void* stream);
 
@@ -158,8 +160,7 @@ W4G128_API int w4g128_gemv(const void* packed, const w4g128_bf16* x, w4g128_bf16
  * drafts with two 8-row MMA tiles per weight fragment).  Row m of the result
  * is bitwise identical to this call on row m alone (M = 1), for every M: a
  * verify pass reproduces exactly what the same arithmetic gives one token at
- * a time.  w4g128_gemv (CUDA cores) agrees with
- * it within the acceptance bound, not bitwise.  Token Rush README, progress
+ * a time; w4g128_gemv is this call at M = 1.  Token Rush README, progress
  * table steps 13-14 and 28. */
 W4G128_API int w4g128_gemm_verify(const void* packed, const w4g128_bf16* x, w4g128_bf16* y, int M, int K,
                                   int N, void* ws, size_t ws_bytes, void* stream);
@@ -181,7 +182,7 @@ W4G128_API size_t w4g128_decode_step_workspace_bytes(const w4g128_matrix* mats, 
  * 1 <= count <= W4G128_MAX_MATRICES) in one persistent launch: y_i = x_i .
  * dequant(W_i) for each i, as a whole decode step reads every weight once
  * (Token Rush README, progress table step 4 and the "bandwidth ceiling"
- * paragraph).  M = 1 uses the CUDA-core kernel, M >= 2 the warp-MMA kernel.
+ * paragraph).  Every M runs the warp-MMA kernel.
  * The split-K segments (512 rows) and their summation order depend only on
  * each matrix's shape, so every y_i is bitwise identical to what a separate
  * w4g128_gemv (M = 1) or w4g128_gemm_verify call returns, whatever the SM
@@ -191,13 +192,12 @@ W4G128_API size_t w4g128_decode_step_workspace_bytes(const w4g128_matrix* mats, 
 W4G128_API int w4g128_decode_step(const w4g128_matrix* mats, int count, int M, void* ws, size_t ws_bytes,
                                   void* stream);
 
-/* w4g128_decode_step with the verify arithmetic at every M, M = 1 included:
- * row m of each y_i is bitwise identical to w4g128_gemm_verify on matrix i
- * and row m alone, so decoding with this entry point at M = 1 and verifying
- * drafts with it at M > 1 give the same bits for the same token (the exact
- * speculative-decoding property; Token Rush README, progress table step 28).
- * Same arguments, workspace query and bitwise guarantees as
- * w4g128_decode_step; at M >= 2 the two entry points compute the same thing. */
+/* The verify step over a list of matrices: row m of each y_i is bitwise
+ * identical to w4g128_gemm_verify on matrix i and row m alone, so decoding
+ * at M = 1 and verifying drafts at M > 1 give the same bits for the same
+ * token (the exact speculative-decoding property; Token Rush README, progress
+ * table step 28).  It computes exactly what w4g128_decode_step does (one
+ * arithmetic serves every M); same arguments and workspace query. */
 W4G128_API int w4g128_verify_step(const w4g128_matrix* mats, int count, int M, void* ws, size_t ws_bytes,
                                   void* stream);
 
@@ -209,10 +209,9 @@ W4G128_API int w4g128_verify_step(const w4g128_matrix* mats, int count, int M, v
  * columns:
  *   h[m][n]   = bf16( residual[m][n] + (x . dequant(W))[m][n] )
  *   out[m][n] = bf16( gamma[n] h[m][n] / sqrt( mean_n h[m][n]^2 + eps ) )
- * The product is the one w4g128_decode_step (verify = 0) or
- * w4g128_verify_step (verify = 1) computes, kept in fp32; the residual is
- * added to it in fp32 and h rounded once, so with residual = -0.0 h is bit for
- * bit that call's y.  The norm reads the rounded h (the value the residual
+ * The product is the one w4g128_gemm_verify computes, kept in fp32; the
+ * residual is added to it in fp32 and h rounded once, so with residual = -0.0
+ * h is bit for bit that call's y.  The norm reads the rounded h (the value the residual
  * stream keeps): mean_n h^2 is summed in fp32 in an order fixed by N alone,
  * and every step after it is one correctly rounded fp32 operation, so out is
  * deterministic.  The residual add happens where the split-K sums are
@@ -223,7 +222,8 @@ W4G128_API int w4g128_verify_step(const w4g128_matrix* mats, int count, int M, v
  *   caller-owned; 1 <= M <= W4G128_MAX_M.  h may be the residual itself
  *   (updated in place); out must not overlap x, residual or h
  *   (W4G128_ERR_INVALID_ARG when it is one of them).  residual, gamma, h,
- *   out: 4-byte aligned.  eps: finite and >= 0.  verify: 0 or 1.  ws as for
+ *   out: 4-byte aligned.  eps: finite and >= 0.  verify: 0 or 1 (both
+ *   name the one arithmetic every M uses).  ws as for
  *   w4g128_gemm_verify (w4g128_workspace_bytes(M, K, N) bytes). */
 W4G128_API int w4g128_gemm_add_rmsnorm(const void* packed, const w4g128_bf16* x, const w4g128_bf16* residual,
                                        const w4g128_bf16* gamma, float eps, w4g128_bf16* h, w4g128_bf16* out,

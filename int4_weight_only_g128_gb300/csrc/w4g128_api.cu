@@ -38,15 +38,15 @@ int check_stream_call(const w4g128_matrix* mats, int count, int M, void* ws) {
   return W4G128_OK;
 }
 
-int run_stream(const w4g128_matrix* mats, int count, int M, bool verify, void* ws, size_t ws_bytes,
-               void* stream, const w4g128::NormArgs* norm = nullptr) {
+int run_stream(const w4g128_matrix* mats, int count, int M, void* ws, size_t ws_bytes, void* stream,
+               const w4g128::NormArgs* norm = nullptr) {
   int rc = check_stream_call(mats, count, M, ws);
   if (rc != W4G128_OK) return rc;
   if (!w4g128::device_is_sm103()) return W4G128_ERR_DEVICE;
   static_assert(sizeof(HostMatrix) == sizeof(w4g128_matrix), "descriptor layout");
   HostMatrix hm[W4G128_MAX_MATRICES];
   for (int i = 0; i < count; ++i) hm[i] = HostMatrix{mats[i].packed, mats[i].x, mats[i].y, mats[i].K, mats[i].N};
-  return w4g128::launch_stream(hm, count, M, verify, norm, ws, ws_bytes, as_stream(stream));
+  return w4g128::launch_stream(hm, count, M, norm, ws, ws_bytes, as_stream(stream));
 }
 
 size_t stream_bytes(const w4g128_matrix* mats, int count, int M) {
@@ -56,10 +56,7 @@ size_t stream_bytes(const w4g128_matrix* mats, int count, int M) {
     if (!shape_ok(mats[i].K, mats[i].N)) return 0;
     hm[i] = HostMatrix{mats[i].packed, mats[i].x, mats[i].y, mats[i].K, mats[i].N};
   }
-  // one size serves both arithmetics, so a workspace sized once fits every call
-  const size_t a = w4g128::stream_workspace_bytes(hm, count, M, false);
-  const size_t b = w4g128::stream_workspace_bytes(hm, count, M, true);
-  return (a == 0 || b == 0) ? 0 : (a > b ? a : b);
+  return w4g128::stream_workspace_bytes(hm, count, M);
 }
 
 }  // namespace
@@ -123,13 +120,13 @@ size_t w4g128_workspace_bytes(int M, int K, int N) {
 int w4g128_gemv(const void* packed, const w4g128_bf16* x, w4g128_bf16* y, int K, int N, void* ws,
                 size_t ws_bytes, void* stream) {
   const w4g128_matrix m{packed, x, y, K, N};
-  return run_stream(&m, 1, 1, false, ws, ws_bytes, stream);
+  return run_stream(&m, 1, 1, ws, ws_bytes, stream);
 }
 
 int w4g128_gemm_verify(const void* packed, const w4g128_bf16* x, w4g128_bf16* y, int M, int K, int N,
                        void* ws, size_t ws_bytes, void* stream) {
   const w4g128_matrix m{packed, x, y, K, N};
-  return run_stream(&m, 1, M, true, ws, ws_bytes, stream);
+  return run_stream(&m, 1, M, ws, ws_bytes, stream);
 }
 
 size_t w4g128_decode_step_workspace_bytes(const w4g128_matrix* mats, int count, int M) {
@@ -137,11 +134,11 @@ size_t w4g128_decode_step_workspace_bytes(const w4g128_matrix* mats, int count, 
 }
 
 int w4g128_decode_step(const w4g128_matrix* mats, int count, int M, void* ws, size_t ws_bytes, void* stream) {
-  return run_stream(mats, count, M, false, ws, ws_bytes, stream);
+  return run_stream(mats, count, M, ws, ws_bytes, stream);
 }
 
 int w4g128_verify_step(const w4g128_matrix* mats, int count, int M, void* ws, size_t ws_bytes, void* stream) {
-  return run_stream(mats, count, M, true, ws, ws_bytes, stream);
+  return run_stream(mats, count, M, ws, ws_bytes, stream);  // one arithmetic at every M
 }
 
 int w4g128_gemm_add_rmsnorm(const void* packed, const w4g128_bf16* x, const w4g128_bf16* residual,
@@ -155,7 +152,7 @@ int w4g128_gemm_add_rmsnorm(const void* packed, const w4g128_bf16* x, const w4g1
   if (!aligned(residual, 4) || !aligned(gamma, 4) || !aligned(out, 4)) return W4G128_ERR_ALIGN;
   const w4g128_matrix m{packed, x, h, K, N};
   const w4g128::NormArgs norm{residual, gamma, out, eps};
-  return run_stream(&m, 1, M, verify != 0, ws, ws_bytes, stream, &norm);
+  return run_stream(&m, 1, M, ws, ws_bytes, stream, &norm);
 }
 
 int w4g128_workspace_status(const void* ws, int* status_out, void* stream) {

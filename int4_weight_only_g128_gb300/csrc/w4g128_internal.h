@@ -42,10 +42,9 @@ struct HostMatrix {
   int K, N;
 };
 
-// Workspace bytes for streaming these matrices at this M on the current device
-// (verify: the verify arithmetic also at M = 1).  Returns 0 on invalid
-// arguments.
-size_t stream_workspace_bytes(const HostMatrix* mats, int count, int M, bool verify);
+// Workspace bytes for streaming these matrices at this M on the current
+// device.  Returns 0 on invalid arguments.
+size_t stream_workspace_bytes(const HostMatrix* mats, int count, int M);
 
 // The residual add + RMS norm that a one-matrix call may end in: y becomes
 // h = residual + x W and out = gamma h / rms(h) per row (device pointers).
@@ -57,10 +56,10 @@ struct NormArgs {
 };
 
 // Launches the prep, streaming and (M >= 2) reduce kernels; the API layer
-// validates arguments.  M >= 2 always uses the verify arithmetic (warp MMA);
-// at M = 1 `verify` selects it over the CUDA-core decode arithmetic.  norm:
-// nullptr, or the residual add + RMS norm (count must be 1).
-int launch_stream(const HostMatrix* mats, int count, int M, bool verify, const NormArgs* norm, void* ws,
+// validates arguments.  Every M uses the warp-MMA arithmetic, so row m of a
+// result is bitwise the M = 1 result of row m.  norm: nullptr, or the
+// residual add + RMS norm (count must be 1).
+int launch_stream(const HostMatrix* mats, int count, int M, const NormArgs* norm, void* ws,
                   size_t ws_bytes, cudaStream_t stream);
 
 int read_workspace_status(const void* ws, int* status_out, cudaStream_t stream);

@@ -67,12 +67,12 @@ extern "C" int w4g128_gemv_noalloc(const void* packed, const w4g128_bf16* x, w4g
   if (!aligned(packed, 16) || !aligned(x, 4) || !aligned(y, 4)) return W4G128_ERR_ALIGN;
   if (!w4g128::device_is_sm103()) return W4G128_ERR_DEVICE;
   const w4g128::HostMatrix m{packed, x, y, K, N};
-  const size_t need = w4g128::stream_workspace_bytes(&m, 1, 1, false);
+  const size_t need = w4g128::stream_workspace_bytes(&m, 1, 1);
   if (need == 0) return W4G128_ERR_SHAPE;
   if (need > W4G128_NOALLOC_SCRATCH_BYTES) return W4G128_ERR_WORKSPACE;  // shape too large for the scratch
   void* scratch = nullptr;
   const int rc = scratch_address(&scratch);
   if (rc != W4G128_OK) return rc;
-  return w4g128::launch_stream(&m, 1, 1, false, nullptr, scratch, W4G128_NOALLOC_SCRATCH_BYTES,
+  return w4g128::launch_stream(&m, 1, 1, nullptr, scratch, W4G128_NOALLOC_SCRATCH_BYTES,
                                static_cast<cudaStream_t>(stream));
 }

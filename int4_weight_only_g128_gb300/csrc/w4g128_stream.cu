@@ -1,7 +1,7 @@
 // The weight-streaming kernels: y_i = x_i . dequant(W_i) for a list of
-// int4-g128 matrices -- M = 1 decode on CUDA cores, the M <= 16 verify (M = 1
-// included, so that its rows match bit for bit whatever M) on the warp-level
-// MMA -- and the optional residual add + RMS norm the product feeds.
+// int4-g128 matrices -- M = 1 decode and the M <= 16 verify alike on the
+// warp-level MMA, so that a row's bits do not depend on M -- and the optional
+// residual add + RMS norm the product feeds.
 //
 // Design (sm_103a, one GPU):
 //  * The work is a flat list of items (matrix, 64-column quad, segment of 4
@@ -77,9 +77,8 @@ namespace {
 // ----------------------------------------------------------------- modes
 
 enum Mode : int {
-  kM1 = 0,   // M = 1, CUDA cores: fp16 x fp16 -> fp32 FMA on the dequantised pairs
-  kMMA = 1,  // M <= 8, warp MMA m16n8k16 f16 -> f32 with the weights as the 16-row operand
-  kMMA1 = 2, // M = 1 with the verify arithmetic: the warp MMA, every B column carrying the one x row
+  kMMA = 1,  // 2 <= M <= 8, warp MMA m16n8k16 f16 -> f32 with the weights as the 16-row operand
+  kMMA1 = 2, // M = 1: the warp MMA, every B column carrying the one x row
   kMMA16 = 3, // 9 <= M <= 16: the warp MMA, two 8-row x tiles per dequantised weight fragment
 };
 
@@ -92,9 +91,6 @@ __host__ __device__ constexpr bool multi_row() { return MODE == kMMA || MODE == 
 #endif
 #ifndef W4G128_RING_DEPTH
 #define W4G128_RING_DEPTH 2
-#endif
-#ifndef W4G128_SEG_GROUPS_M1
-#define W4G128_SEG_GROUPS_M1 4
 #endif
 constexpr int kNW = W4G128_WARPS_PER_CTA;  // warps per CTA
 constexpr int kDepth = W4G128_RING_DEPTH;  // ring slots per warp
@@ -109,25 +105,21 @@ constexpr int kDepth = W4G128_RING_DEPTH;  // ring slots per warp
 // The 80-byte stride keeps the 16-byte loads of 8 lanes on distinct bank
 // groups.
 template <int MODE> struct Pkg;
-template <> struct Pkg<kM1> { static constexpr int kRows = 1, kRowBytes = 320, kBytes = 336; };
 template <> struct Pkg<kMMA> { static constexpr int kRows = 8, kRowBytes = 320, kBytes = 2624; };
 template <> struct Pkg<kMMA1> { static constexpr int kRows = 1, kRowBytes = 320, kBytes = 336; };
 template <> struct Pkg<kMMA16> { static constexpr int kRows = 16, kRowBytes = 320, kBytes = 5248; };
 
-// Groups per split-K segment (an item's K extent): fixed per mode, never by
-// the grid, so every summation order depends on the shape and M alone.  Both
-// modes use 512 rows: shorter M = 1 segments (a partial is only 256 bytes
-// there) speed up single small calls but cost more per-segment work on large
-// ones; at M >= 2 a partial is 2 KB.
-template <int MODE>
-__host__ __device__ constexpr int seg_groups() { return MODE == kM1 ? W4G128_SEG_GROUPS_M1 : kSegGroups; }
+// Groups per split-K segment (an item's K extent): kSegGroups (512 rows) in
+// every mode, never set by the grid, so every summation order depends on the
+// shape alone.  Shorter M = 1 segments (a partial is only 256 bytes there)
+// speed up single small calls but cost more per-segment work on large ones.
 
 template <int MODE>
 __host__ __device__ constexpr int slot_bytes() { return kQuadTiles * kBlockBytes + Pkg<MODE>::kBytes; }
 #ifndef W4G128_M1_RING_DEPTH
 #define W4G128_M1_RING_DEPTH 2
 #endif
-// Ring slots per warp: kDepth, or for the small-package M = 1 modes
+// Ring slots per warp: kDepth, or for the small-package M = 1 mode
 // W4G128_M1_RING_DEPTH (three 4688-byte slots per warp still fit 16 warps).
 template <int MODE>
 __host__ __device__ constexpr int ring_depth() { return multi_row<MODE>() ? kDepth : W4G128_M1_RING_DEPTH; }
@@ -144,12 +136,12 @@ __host__ __device__ constexpr int smem_bytes() {
   return kBarBytes + cta_warps_max<MODE>() * ring_depth<MODE>() * slot_bytes<MODE>();
 }
 
-static_assert(slot_bytes<kM1>() % 16 == 0 && slot_bytes<kMMA>() % 16 == 0 && slot_bytes<kMMA16>() % 16 == 0,
+static_assert(slot_bytes<kMMA1>() % 16 == 0 && slot_bytes<kMMA>() % 16 == 0 && slot_bytes<kMMA16>() % 16 == 0,
               "bulk copies need 16-byte slots");
-static_assert(Pkg<kM1>::kBytes % 16 == 0 && Pkg<kMMA>::kBytes % 16 == 0 && Pkg<kMMA16>::kBytes % 16 == 0,
+static_assert(Pkg<kMMA1>::kRows == 1 && Pkg<kMMA>::kRows == 8 && Pkg<kMMA16>::kRows == 16, "x rows per package");
+static_assert(Pkg<kMMA1>::kBytes % 16 == 0 && Pkg<kMMA>::kBytes % 16 == 0 && Pkg<kMMA16>::kBytes % 16 == 0,
               "bulk copies need 16-byte packages");
-static_assert(smem_bytes<kM1>() <= 232448 && smem_bytes<kMMA>() <= 232448 && smem_bytes<kMMA1>() <= 232448 &&
-                  smem_bytes<kMMA16>() <= 232448,
+static_assert(smem_bytes<kMMA>() <= 232448 && smem_bytes<kMMA1>() <= 232448 && smem_bytes<kMMA16>() <= 232448,
               "a CTA's rings must fit the 227 KB of shared memory");
 
 // ----------------------------------------------------------------- parameters
@@ -235,7 +227,7 @@ __device__ __forceinline__ void cursor_load(Cursor& c, const StreamParams<MAXMAT
   const MatParams& m = mat(p, mi);
   c.mi = mi;
   c.G = m.K / kGroup;
-  c.S = div_up(c.G, seg_groups<MODE>());
+  c.S = div_up(c.G, kSegGroups);
   c.T = m.N / kTileN;
   c.NQ = div_up(c.T, kQuadTiles);
 }
@@ -255,8 +247,8 @@ __device__ __forceinline__ void cursor_seek(Cursor& c, const StreamParams<MAXMAT
   c.item = item;
   c.q = static_cast<int>(local / c.S);
   c.s = static_cast<int>(local - static_cast<long long>(c.q) * c.S);
-  c.g = c.s * seg_groups<MODE>();
-  c.g_end = min(c.g + seg_groups<MODE>(), c.G);
+  c.g = c.s * kSegGroups;
+  c.g_end = min(c.g + kSegGroups, c.G);
   c.ntiles = min(kQuadTiles, c.T - kQuadTiles * c.q);
   c.src = mat(p, lo).packed + static_cast<long long>(c.q) * c.G * kQuadBytes +
           static_cast<long long>(c.g) * c.ntiles * kBlockBytes;
@@ -270,7 +262,7 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const StreamParams<MAXMAT
   if (++c.g < c.g_end) return;
   ++c.item;
   if (++c.s < c.S) {
-    c.g_end = min(c.g + seg_groups<MODE>(), c.G);
+    c.g_end = min(c.g + kSegGroups, c.G);
     return;
   }
   c.s = 0;
@@ -278,7 +270,7 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const StreamParams<MAXMAT
   if (++c.q < c.NQ) {  // the next quad starts where this one ended
     c.ntiles = min(kQuadTiles, c.T - kQuadTiles * c.q);
     c.xsrc = mat(p, c.mi).xpkg;
-    c.g_end = min(seg_groups<MODE>(), c.G);
+    c.g_end = min(kSegGroups, c.G);
     return;
   }
   if (c.mi + 1 == p.count) return;  // past the end; never dereferenced
@@ -287,7 +279,7 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const StreamParams<MAXMAT
   c.ntiles = min(kQuadTiles, c.T);
   c.src = mat(p, c.mi).packed;
   c.xsrc = mat(p, c.mi).xpkg;
-  c.g_end = min(seg_groups<MODE>(), c.G);
+  c.g_end = min(kSegGroups, c.G);
 }
 
 // What the M = 1 fold of one split quad needs, recorded by the warp that
@@ -336,29 +328,8 @@ __device__ __forceinline__ void issue_package(const Cursor& c, uint32_t slot, ui
 //   w & 0x00F000F0 -> nibbles 1, 5 (rows 2c, 2c+1, column r+8)    as 1024 + 16q
 //   v & 0x000F000F -> nibbles 2, 6 (rows 2c+8, 2c+9, column r)    as 1024 + q
 //   v & 0x00F000F0 -> nibbles 3, 7 (rows 2c+8, 2c+9, column r+8)  as 1024 + 16q
-// into fp16 pairs; each half is multiplied by the matching fp16 x' and
-// accumulated in fp32 (the products are exact).
-__device__ __forceinline__ float fma_f16_pair(uint32_t wq, uint32_t xx, float acc) {
-  asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
-      "mov.b32 {wl, wh}, %1;\n\t"
-      "mov.b32 {xl, xh}, %2;\n\t"
-      "fma.rn.f32.f16 %0, wl, xl, %0;\n\t"
-      "fma.rn.f32.f16 %0, wh, xh, %0;\n\t}"
-      : "+f"(acc)
-      : "r"(wq), "r"(xx));
-  return acc;
-}
-
+// into fp16 pairs, which are the A fragment of the warp MMA below.
 constexpr uint32_t kMagic = 0x64006400u;  // fp16 1024.0 in both halves
-
-// lo: column r (1024 + q), hi: column r + 8 (1024 + 16q)
-__device__ __forceinline__ void dq_word(uint32_t w, uint32_t xa, uint32_t xb, float& lo, float& hi) {
-  const uint32_t v = w >> 8;
-  lo = fma_f16_pair(lop3_and_or(w, 0x000F000Fu, kMagic), xa, lo);
-  hi = fma_f16_pair(lop3_and_or(w, 0x00F000F0u, kMagic), xa, hi);
-  lo = fma_f16_pair(lop3_and_or(v, 0x000F000Fu, kMagic), xb, lo);
-  hi = fma_f16_pair(lop3_and_or(v, 0x00F000F0u, kMagic), xb, hi);
-}
 
 // Warp MMA: D[16 cols x 8 rows] += A[16 cols x 16 k] * B[16 k x 8 rows]; the
 // four LOP3 outputs of one packed word are exactly this lane's A fragment
@@ -453,14 +424,16 @@ __device__ __forceinline__ uint32_t emit2(float a, float b, uint32_t r) {
   return static_cast<uint32_t>(to_bf16(a)) | (static_cast<uint32_t>(to_bf16(b)) << 16);
 }
 
-// Rows of the per-lane accumulators: M = 1 keeps (column r, column r+8);
-// the MMA keeps (r, 2c), (r, 2c+1), (r+8, 2c), (r+8, 2c+1).
-template <int MODE> struct Acc { static constexpr int kN = (MODE == kM1) ? 2 : (MODE == kMMA16 ? 8 : 4); };
+// Rows of the per-lane accumulators: the MMA keeps (r, 2c), (r, 2c+1),
+// (r+8, 2c), (r+8, 2c+1) (and the same for rows 8 + 2c, 9 + 2c at M > 8);
+// M = 1 keeps (column r, column r+8) of x row 2c, which every lane class
+// holds alike.
+template <int MODE> struct Acc {
+  static constexpr int kN = (MODE == kMMA1) ? 2 : (MODE == kMMA16 ? 8 : 4);
+};
 
 // One chunk: every tile of the quad for one group, added into seg[t][*].
-// FULL: the quad has all 4 tiles, so the tiles form one straight-line block
-// the compiler can interleave.
-template <int MODE, bool FULL>
+template <int MODE>
 __device__ __forceinline__ void compute_chunk(const uint8_t* sl, int ntiles, int lane,
                                               float (&seg)[kQuadTiles][Acc<MODE>::kN]) {
   const int r = lane >> 2, c = lane & 3;
@@ -473,37 +446,7 @@ __device__ __forceinline__ void compute_chunk(const uint8_t* sl, int ntiles, int
     const uint4 v = reinterpret_cast<const uint4*>(xr)[i];
     xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
   }
-  if constexpr (MODE == kM1) {
-    const float2 xf = *reinterpret_cast<const float2*>(xr + 16);  // (X_c, f)
-    const float Xc = xf.x;
-    const float2 ff = make_float2(xf.y, xf.y * 0.0625f);          // x' -> x for columns r and r + 8
-#pragma unroll
-    for (int t = 0; t < kQuadTiles; ++t) {
-      if (FULL || t < ntiles) {
-        const uint8_t* blk = sl + t * kBlockBytes;
-        const uint4 u0 = *reinterpret_cast<const uint4*>(blk + 16 * lane);
-        const uint4 u1 = *reinterpret_cast<const uint4*>(blk + 512 + 16 * lane);
-        const uint2 me = *reinterpret_cast<const uint2*>(blk + kCodeBytes + 8 * r);
-        float lo = 0.f, hi = 0.f;  // sum_k x'_k (1024 + q_k), sum_k x'_k (1024 + 16 q_k): columns r, r+8
-        dq_word(u0.x, xw[0], xw[1], lo, hi);
-        dq_word(u0.y, xw[2], xw[3], lo, hi);
-        dq_word(u0.z, xw[4], xw[5], lo, hi);
-        dq_word(u0.w, xw[6], xw[7], lo, hi);
-        dq_word(u1.x, xw[8], xw[9], lo, hi);
-        dq_word(u1.y, xw[10], xw[11], lo, hi);
-        dq_word(u1.z, xw[12], xw[13], lo, hi);
-        dq_word(u1.w, xw[14], xw[15], lo, hi);
-        // columns r and r+8 side by side:
-        //   seg += scale f S + (min - 1024 scale) X_c,  seg += (scale/16) f S + (min - 64 scale) X_c
-        const float2 s2 = make_float2(bf16_lo(me.x), bf16_lo(me.y));
-        const float2 m2 = ffma2(make_float2(-1024.f, -64.f), s2, make_float2(bf16_hi(me.x), bf16_hi(me.y)));
-        float2 a2 = ffma2(m2, make_float2(Xc, Xc), make_float2(seg[t][0], seg[t][1]));
-        a2 = ffma2(fmul2(s2, ff), make_float2(lo, hi), a2);
-        seg[t][0] = a2.x;
-        seg[t][1] = a2.y;
-      }
-    }
-  } else if constexpr (MODE == kMMA16) {
+  if constexpr (MODE == kMMA16) {
     // rows r (tile 0) and 8 + r (tile 1) of the B operand; (X_g, f) of rows
     // 2c, 2c + 1 and 8 + 2c, 9 + 2c.  Each tile goes through exactly the
     // arithmetic of the 8-row mode, so every row's bits match it.
@@ -519,7 +462,7 @@ __device__ __forceinline__ void compute_chunk(const uint8_t* sl, int ntiles, int
     const float4 xq1 = *reinterpret_cast<const float4*>(tl + 16 + 4 * c);
 #pragma unroll
     for (int t = 0; t < kQuadTiles; ++t) {
-      if (FULL || t < ntiles) {
+      if (t < ntiles) {
         const uint8_t* blk = sl + t * kBlockBytes;
         const uint4 u0 = *reinterpret_cast<const uint4*>(blk + 16 * lane);
         const uint4 u1 = *reinterpret_cast<const uint4*>(blk + 512 + 16 * lane);
@@ -570,7 +513,7 @@ __device__ __forceinline__ void compute_chunk(const uint8_t* sl, int ntiles, int
     const float2 fab16 = make_float2(xq.y * 0.0625f, xq.w * 0.0625f);
 #pragma unroll
     for (int t = 0; t < kQuadTiles; ++t) {
-      if (FULL || t < ntiles) {
+      if (t < ntiles) {
         const uint8_t* blk = sl + t * kBlockBytes;
         const uint4 u0 = *reinterpret_cast<const uint4*>(blk + 16 * lane);
         const uint4 u1 = *reinterpret_cast<const uint4*>(blk + 512 + 16 * lane);
@@ -589,36 +532,33 @@ __device__ __forceinline__ void compute_chunk(const uint8_t* sl, int ntiles, int
         const float sl0 = bf16_lo(me.x), sh0 = bf16_lo(me.y);
         const float ml0 = fmaf(-1024.f, sl0, bf16_hi(me.x));
         const float mh0 = fmaf(-64.f, sh0, bf16_hi(me.y));
-        float2 lo2 = ffma2(make_float2(ml0, ml0), Xab, make_float2(seg[t][0], seg[t][1]));
-        lo2 = ffma2(fmul2(make_float2(sl0, sl0), fab), make_float2(d0[0] + d1[0], d0[1] + d1[1]), lo2);
-        float2 hi2 = ffma2(make_float2(mh0, mh0), Xab, make_float2(seg[t][2], seg[t][3]));
-        hi2 = ffma2(fmul2(make_float2(sh0, sh0), fab16), make_float2(d0[2] + d1[2], d0[3] + d1[3]), hi2);
-        seg[t][0] = lo2.x;
-        seg[t][1] = lo2.y;
-        seg[t][2] = hi2.x;
-        seg[t][3] = hi2.y;
+        if constexpr (MODE == kMMA1) {
+          // the first lane of each pair below, alone: the same roundings
+          seg[t][0] = __fmaf_rn(__fmul_rn(sl0, fab.x), d0[0] + d1[0], __fmaf_rn(ml0, Xab.x, seg[t][0]));
+          seg[t][1] = __fmaf_rn(__fmul_rn(sh0, fab16.x), d0[2] + d1[2], __fmaf_rn(mh0, Xab.x, seg[t][1]));
+        } else {
+          float2 lo2 = ffma2(make_float2(ml0, ml0), Xab, make_float2(seg[t][0], seg[t][1]));
+          lo2 = ffma2(fmul2(make_float2(sl0, sl0), fab), make_float2(d0[0] + d1[0], d0[1] + d1[1]), lo2);
+          float2 hi2 = ffma2(make_float2(mh0, mh0), Xab, make_float2(seg[t][2], seg[t][3]));
+          hi2 = ffma2(fmul2(make_float2(sh0, sh0), fab16), make_float2(d0[2] + d1[2], d0[3] + d1[3]), hi2);
+          seg[t][0] = lo2.x;
+          seg[t][1] = lo2.y;
+          seg[t][2] = hi2.x;
+          seg[t][3] = hi2.y;
+        }
       }
     }
   }
 }
 
-// Select v[t][e] for a runtime t without local memory.
-template <int NA>
-__device__ __forceinline__ float pick(const float (&v)[kQuadTiles][NA], int t, int e) {
-  float out = v[0][e];
-#pragma unroll
-  for (int i = 1; i < kQuadTiles; ++i) out = (t == i) ? v[i][e] : out;
-  return out;
-}
-
 // ----------------------------------------------------------------- the streaming kernel
 
 template <int MODE, int MAXMAT, bool NORM>
-// M = 1 (CUDA cores) is held to 120 registers (no spills): 4096 of the SM's
-// 65536 registers stay free for the next call's one-warp prep CTAs.
+// M = 1 is held to 120 registers (no spills): 4096 of the
+// SM's 65536 registers stay free for the next call's one-warp prep CTAs.
 // M <= 16 (8 warps) may use up to 255.
 __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
-    __maxnreg__(MODE == kM1 ? 120 : (MODE == kMMA16 ? 255 : 128))
+    __maxnreg__(MODE == kMMA1 ? 120 : (MODE == kMMA16 ? 255 : 128))
     stream_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int NA = Acc<MODE>::kN;
@@ -735,12 +675,7 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
         break;
       }
       const int ntiles = cc.ntiles;
-      // M = 1: a straight-line body for full quads lets the compiler interleave
-      // the four tiles; the MMA path keeps per-tile blocks (register budget).
-      if (MODE == kM1 && ntiles == kQuadTiles)
-        compute_chunk<MODE, true>(ring + slot * kSlot, ntiles, lane, seg);
-      else
-        compute_chunk<MODE, false>(ring + slot * kSlot, ntiles, lane, seg);
+      compute_chunk<MODE>(ring + slot * kSlot, ntiles, lane, seg);
 
       // Slot consumed: refill it with the chunk kDepth ahead.
       __syncwarp();
@@ -767,19 +702,7 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
         // quad continues in later warps) keeps their left fold too and stores it
         // as one partial: the fold over segments then starts from it.
         const bool prefix = (q_first >= it_a) && !owned;
-        if constexpr (MODE == kM1) {
-          // reduce the 4 lane classes c of each column (same tree on every lane)
-#pragma unroll
-          for (int t = 0; t < kQuadTiles; ++t)
-#pragma unroll
-            for (int e = 0; e < NA; ++e) {
-              float v = seg[t][e];
-              v += __shfl_xor_sync(0xffffffffu, v, 1);
-              v += __shfl_xor_sync(0xffffffffu, v, 2);
-              seg[t][e] = v;
-            }
-        }
-        const int rows = (MODE == kM1) ? 1 : p.M;
+        const int rows = multi_row<MODE>() ? p.M : 1;
         if (owned || prefix) {
 #pragma unroll
           for (int t = 0; t < kQuadTiles; ++t)
@@ -790,11 +713,16 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
           // one slot per (matrix, quad, segment): the segment sum, or at the last
           // segment of a prefix run the fold of segments 0 .. s
           float* part = p.partials + cc.item * rows * 64;
-          if constexpr (MODE == kM1) {
-            // lane (r, c) stores tile c's columns r and r + 8
-            if (c < ntiles) {
-              part[16 * c + r] = prefix ? pick(tot, c, 0) : pick(seg, c, 0);
-              part[16 * c + r + 8] = prefix ? pick(tot, c, 1) : pick(seg, c, 1);
+          if constexpr (MODE == kMMA1) {
+            // lanes c == 0 store columns r and r + 8 of every tile
+            if (c == 0) {
+#pragma unroll
+              for (int t = 0; t < kQuadTiles; ++t) {
+                if (t < ntiles) {
+                  part[16 * t + r] = prefix ? tot[t][0] : seg[t][0];
+                  part[16 * t + r + 8] = prefix ? tot[t][1] : seg[t][1];
+                }
+              }
             }
           } else {
             // accumulator 4h + {0, 1, 2, 3}: rows 8h + 2c, 8h + 2c + 1 of columns r, r + 8
@@ -826,11 +754,16 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
         if (quad_end) {
           const int n0 = kQuadTiles * kTileN * cc.q;
           if (owned) {
-            if constexpr (MODE == kM1) {
-              if (c < ntiles) {
-                const int n = n0 + 16 * c + r;
-                m.y[n] = emit<NORM>(p, n, pick(tot, c, 0));
-                m.y[n + 8] = emit<NORM>(p, n + 8, pick(tot, c, 1));
+            if constexpr (MODE == kMMA1) {
+              if (c == 0) {
+#pragma unroll
+                for (int t = 0; t < kQuadTiles; ++t) {
+                  if (t < ntiles) {
+                    const int n = n0 + 16 * t + r;
+                    m.y[n] = emit<NORM>(p, n, tot[t][0]);
+                    m.y[n + 8] = emit<NORM>(p, n + 8, tot[t][1]);
+                  }
+                }
               }
             } else {
 #pragma unroll
@@ -1051,7 +984,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Strea
   }
 }
 
-// M = 1 (either arithmetic): the one-row package needs four lanes, so a warp
+// M = 1: the one-row package needs four lanes, so a warp
 // builds eight groups at once, lane (j, c) class c of group 8 k + j of its
 // share.  One-warp CTAs with few registers fit on an SM beside a streaming
 // CTA: the next call's prep is resident before the previous call has ended,
@@ -1419,7 +1352,6 @@ const DeviceInfo* device_info() {
     cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     d.ok = (major == 10 && minor == 3);
     if (d.ok) {
-      setup_mode<kM1>(d);
       setup_mode<kMMA>(d);
       setup_mode<kMMA1>(d);
       setup_mode<kMMA16>(d);
@@ -1449,17 +1381,17 @@ struct Plan {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-bool make_plan(const HostMatrix* mats, int count, int M, bool verify, const DeviceInfo& dev, Plan& pl) {
-  pl.mode = (M > 8) ? kMMA16 : (M > 1) ? kMMA : (verify ? kMMA1 : kM1);
+bool make_plan(const HostMatrix* mats, int count, int M, const DeviceInfo& dev, Plan& pl) {
+  pl.mode = (M > 8) ? kMMA16 : (M > 1) ? kMMA : kMMA1;
   pl.rows = M;
-  pl.pkg = (pl.mode == kMMA16) ? Pkg<kMMA16>::kBytes : (pl.mode == kMMA) ? Pkg<kMMA>::kBytes : Pkg<kM1>::kBytes;
+  pl.pkg = (pl.mode == kMMA16) ? Pkg<kMMA16>::kBytes : (pl.mode == kMMA) ? Pkg<kMMA>::kBytes : Pkg<kMMA1>::kBytes;
   pl.item_begin.resize(count);
   pl.quad_begin.resize(count);
   pl.g_begin.resize(count);
   pl.xpkg_off.resize(count);
   long long items = 0, xbytes = 0, quads = 0, groups = 0;
   for (int i = 0; i < count; ++i) {
-    const int seg = (pl.mode == kM1) ? seg_groups<kM1>() : seg_groups<kMMA>();  // kMMA1 folds like kMMA
+    const int seg = kSegGroups;
     const int G = mats[i].K / kGroup, S = div_up(G, seg), NQ = div_up(mats[i].N, kTileN * kQuadTiles);
     pl.item_begin[i] = items;
     pl.quad_begin[i] = static_cast<int>(quads);
@@ -1603,15 +1535,13 @@ int launch_with(const HostMatrix* mats, int count, int M, const Plan& pl, const 
     if (norm != nullptr) {
       if (pl.mode == kMMA16) return launch_mode<kMMA16, 1, true>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
       if (pl.mode == kMMA) return launch_mode<kMMA, 1, true>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
-      if (pl.mode == kMMA1) return launch_mode<kMMA1, 1, true>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
-      return launch_mode<kM1, 1, true>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
+      return launch_mode<kMMA1, 1, true>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
     }
   }
   if (pl.mode == kMMA16)
     return launch_mode<kMMA16, MAXMAT, false>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
   if (pl.mode == kMMA) return launch_mode<kMMA, MAXMAT, false>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
-  if (pl.mode == kMMA1) return launch_mode<kMMA1, MAXMAT, false>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
-  return launch_mode<kM1, MAXMAT, false>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
+  return launch_mode<kMMA1, MAXMAT, false>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
 }
 
 }  // namespace
@@ -1621,20 +1551,20 @@ bool device_is_sm103() {
   return d != nullptr && d->ok;
 }
 
-size_t stream_workspace_bytes(const HostMatrix* mats, int count, int M, bool verify) {
+size_t stream_workspace_bytes(const HostMatrix* mats, int count, int M) {
   const DeviceInfo* d = device_info();
   if (d == nullptr || !d->ok) return 0;
   Plan pl;
-  if (!make_plan(mats, count, M, verify, *d, pl)) return 0;
+  if (!make_plan(mats, count, M, *d, pl)) return 0;
   return pl.bytes;
 }
 
-int launch_stream(const HostMatrix* mats, int count, int M, bool verify, const NormArgs* norm, void* ws,
+int launch_stream(const HostMatrix* mats, int count, int M, const NormArgs* norm, void* ws,
                   size_t ws_bytes, cudaStream_t stream) {
   const DeviceInfo* d = device_info();
   if (d == nullptr || !d->ok) return W4G128_ERR_DEVICE;
   Plan pl;
-  if (!make_plan(mats, count, M, verify, *d, pl)) return W4G128_ERR_SHAPE;
+  if (!make_plan(mats, count, M, *d, pl)) return W4G128_ERR_SHAPE;
   if (ws_bytes < pl.bytes) return W4G128_ERR_WORKSPACE;
   if (norm != nullptr && count != 1) return W4G128_ERR_INVALID_ARG;
   if (count == 1) return launch_with<1>(mats, count, M, pl, norm, ws, stream);

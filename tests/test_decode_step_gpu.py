@@ -51,7 +51,7 @@ def verify_step(mats, xs, M):
 @pytest.mark.gpu
 def test_verify_step_rows_equal_single_row_verify():
     """w4g128_verify_step: at M = 1 each output equals gemm_verify(M = 1) on
-    its matrix; at M = 8 row m equals the M = 1 step on row m; at M >= 2 it
+    its matrix; at M = 8 row m equals the M = 1 step on row m; at every M it
     equals w4g128_decode_step -- all bit for bit, and within the bound."""
     shapes = [(128, 16), (640, 80), (4096, 4096), (1152, 208), (384, 48), (17408, 5120)]
     mats = [DevMatrix(K, N, matrix_id=400 + i) for i, (K, N) in enumerate(shapes)]
@@ -62,6 +62,8 @@ def test_verify_step_rows_equal_single_row_verify():
         assert np.array_equal(a, b)
     for m in range(8):
         y1 = verify_step(mats, [to_dev(x[m:m + 1]) for x in x8], 1)
+        for a, b in zip(y1, decode_step(mats, [to_dev(x[m:m + 1]) for x in x8], 1)):
+            assert np.array_equal(a, b)
         for mat, x, a, b in zip(mats, x8, y1, y8):
             assert np.array_equal(a[0], b[m]), m
             if m == 0:
