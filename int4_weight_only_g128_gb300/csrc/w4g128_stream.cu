@@ -186,6 +186,7 @@ struct StreamParams {
   float eps;
   int count, M, W, total_quads, total_groups;
   int per_warp_reduce;   // M >= 2: the split quads are folded per streaming warp (else per quad)
+  int depth;             // ring slots per warp (ring_depth of the mode)
   MatParams mats[MAXMAT];
 };
 
@@ -563,7 +564,11 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int NA = Acc<MODE>::kN;
   constexpr int kSlot = slot_bytes<MODE>();
-  constexpr int kDepth = ring_depth<MODE>();  // shadows the default depth
+  // Ring slots per warp, read from the parameters although fixed per mode:
+  // with a compile-time depth the compiler schedules the MMA modes' main loop
+  // worse (measured: layer step M = 8 44.2 vs 43.0 us, lm_head M = 8 113.2 vs
+  // 109.9 us).
+  const int D = p.depth;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane >> 2, c = lane & 3;
   const int wg = blockIdx.x * (blockDim.x >> 5) + warp;  // CTAs hold up to kNW warps
@@ -590,14 +595,13 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
   bool failed = false;
   if (wg < p.W) {
 
-    const uint32_t bar0 = smem_addr(smem) + warp * kDepth * 8;
-    const uint32_t ring0 = smem_addr(smem) + kBarBytes + warp * kDepth * kSlot;
-    const uint8_t* ring = smem + kBarBytes + warp * kDepth * kSlot;
+    const uint32_t bar0 = smem_addr(smem) + warp * D * 8;
+    const uint32_t ring0 = smem_addr(smem) + kBarBytes + warp * D * kSlot;
+    const uint8_t* ring = smem + kBarBytes + warp * D * kSlot;
 
     uint64_t pol_w = 0, pol_x = 0;
     if (lane == 0) {
-#pragma unroll
-      for (int d = 0; d < kDepth; ++d) mbar_init(bar0 + 8 * d, 1);
+      for (int d = 0; d < D; ++d) mbar_init(bar0 + 8 * d, 1);
       fence_mbar_init();
       pol_w = l2_policy_evict_first();
       pol_x = l2_policy_evict_last();
@@ -615,7 +619,7 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
     // call's tail and with the prep kernel (measured on back-to-back layer
     // steps at M = 1: 40.4 -> 40.1 us; lm_head M = 8 115.1 -> 113.8 us).
     constexpr int kEarly = 1;
-    Cursor pre[kDepth];
+    Cursor pre[kEarly];
     int n_pre = 0;
 #pragma unroll
     for (int d = 0; d < kEarly; ++d) {
@@ -629,11 +633,11 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
     grid_dependency_wait();
     if (lane == 0) {
 #pragma unroll
-      for (int d = 0; d < kDepth; ++d)
+      for (int d = 0; d < kEarly; ++d)
         if (d < n_pre) issue_package<MODE>(pre[d], ring0 + d * kSlot, bar0 + 8 * d, pol_x);
     }
     unsigned issued = static_cast<unsigned>(n_pre);
-    while (issued < static_cast<unsigned>(kDepth) && ic.item < it_b) {  // the rest of the ring
+    while (issued < static_cast<unsigned>(D) && ic.item < it_b) {  // the rest of the ring
       if (lane == 0) {
         issue_weights<MODE>(ic, ring0 + issued * kSlot, bar0 + 8 * issued, pol_w);
         issue_package<MODE>(ic, ring0 + issued * kSlot, bar0 + 8 * issued, pol_x);
@@ -659,16 +663,16 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
       for (int e = 0; e < NA; ++e) seg[t][e] = tot[t][e] = 0.f;
 
     unsigned done = 0;  // chunks consumed
+    int slot = 0;          // done % D
+    uint32_t parity = 0u;  // (done / D) & 1
     while (cc.item < it_b) {
-      const int slot = static_cast<int>(done % kDepth);
-      const uint32_t parity = (done / kDepth) & 1u;
       if (!mbar_wait_bounded(bar0 + 8 * slot, parity)) {
         // Give up: record the timeout, drain this warp's copies in flight
         // (again bounded) and leave.  Quads this warp shared stay unreduced.
         if (lane == 0) {
           atomicCAS(p.status, 0u, static_cast<unsigned>(W4G128_ERR_TIMEOUT));
           for (unsigned k = done + 1; k < issued; ++k)
-            (void)mbar_wait_bounded(bar0 + 8 * static_cast<int>(k % kDepth), (k / kDepth) & 1u);
+            (void)mbar_wait_bounded(bar0 + 8 * static_cast<int>(k % D), (k / D) & 1u);
         }
         __syncwarp();
         failed = true;
@@ -677,7 +681,7 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
       const int ntiles = cc.ntiles;
       compute_chunk<MODE>(ring + slot * kSlot, ntiles, lane, seg);
 
-      // Slot consumed: refill it with the chunk kDepth ahead.
+      // Slot consumed: refill it with the chunk D ahead.
       __syncwarp();
       if (ic.item < it_b) {
         if (lane == 0) {
@@ -690,6 +694,10 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
         ++issued;
       }
       ++done;
+      if (++slot == D) {
+        slot = 0;
+        parity ^= 1u;
+      }
 
       if (cc.g + 1 == cc.g_end) {
         // ---- end of a segment
@@ -1370,7 +1378,7 @@ const DeviceInfo* device_info() {
 }
 
 struct Plan {
-  int mode = 0, rows = 1, pkg = 0;
+  int mode = 0, rows = 1, pkg = 0, depth = 2;
   bool per_warp_reduce = false;
   long long items = 0;
   int W = 0, grid = 0, cta_warps = kNW, total_quads = 0, total_groups = 0, max_groups = 0;
@@ -1414,6 +1422,7 @@ bool make_plan(const HostMatrix* mats, int count, int M, const DeviceInfo& dev, 
   // holds warps gets smaller CTAs rather than fewer SMs.
   pl.cta_warps = std::min(nw, div_up(pl.W, dev.sms));
   pl.grid = div_up(pl.W, pl.cta_warps);
+  pl.depth = (pl.mode == kMMA1) ? ring_depth<kMMA1>() : ring_depth<kMMA>();
   // M >= 2: fold per quad unless that grid is larger than one streaming warp
   // each and than one wave of resident reduce CTAs
   pl.per_warp_reduce = M >= 2 && pl.total_quads > pl.W &&
@@ -1444,6 +1453,7 @@ void fill_params(StreamParams<MAXMAT>& sp, const HostMatrix* mats, int count, in
   sp.M = M;
   sp.W = pl.W;
   sp.per_warp_reduce = pl.per_warp_reduce ? 1 : 0;
+  sp.depth = pl.depth;
   sp.total_quads = pl.total_quads;
   sp.total_groups = pl.total_groups;
   for (int i = 0; i < count; ++i) {
@@ -1490,6 +1500,9 @@ int launch_mode(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, int max
   }
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(cta_warps * 32);
+  // the full CTA's shared memory even for smaller CTAs: one CTA per SM, so a
+  // call with few warps still spreads over every SM instead of packing two
+  // CTAs onto one
   cfg.dynamicSmemBytes = smem_bytes<MODE>();
   if (cudaLaunchKernelEx(&cfg, stream_kernel<MODE, MAXMAT, NORM>, sp) != cudaSuccess) {
     cudaGetLastError();

@@ -172,3 +172,21 @@ def test_degenerate_rows():
     _, out0 = fused(mat, x, res, gam, eps=0.0)
     _, ref0 = oracle.Oracle().add_rmsnorm(np.zeros((M, N)), res, gam, 0.0)
     assert np.all(np.isnan(ref0)) and np.all(np.isnan(bf16_to_f64(out0)))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M", [4, 8, 16])
+def test_add_rmsnorm_with_the_per_warp_fold(M):
+    """2560 quads of 2 segments: more quads than streaming warps and than one
+    wave of per-quad reduce CTAs, so the split quads are folded per warp with
+    the residual added there.  h with a -0 residual is the plain call's y bit
+    for bit; at M = 4 h and out are also checked against the oracle."""
+    K, N = 1024, 163840
+    mat = DevMatrix(K, N, matrix_id=900 + M)
+    x, res, gam = inputs(mat, M, 900 + M)
+    zero = np.full((M, N), 0x8000, np.uint16)
+    h0, _ = fused(mat, x, zero, gam, verify=1)
+    assert np.array_equal(h0, run(mat, x, verify=True))
+    if M == 4:
+        h, out = fused(mat, x, res, gam, verify=1)
+        check(mat, x, res, gam, h, out)
