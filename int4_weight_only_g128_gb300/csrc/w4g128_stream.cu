@@ -96,12 +96,13 @@ constexpr int kNW = W4G128_WARPS_PER_CTA;  // warps per CTA
 constexpr int kDepth = W4G128_RING_DEPTH;  // ring slots per warp
 
 // Activation package per group: rows x 4 lane classes c x (16 fp16-pair
-// words + X_c + f + 2 pad) = rows x 320 bytes, then per row m the pair
+// words + 4 unused) = rows x 320 bytes, then per row m the pair
 // (X_g[m], f[m]) as fp32.  Row (m, c) word 2i holds x'[m][k0+2c],
 // x'[m][k0+2c+1] and word 2i+1 holds x'[m][k0+2c+8], x'[m][k0+2c+9] for
 // k0 = 128g + 16i: exactly the fp16 operand pairs lane class c multiplies (the
-// MMA B fragment of row m).  x' = x * 2^s is the scaled copy, f = 2^-s, X_c the
-// true sum of the 32 values of lane class c and X_g = sum of x over the group.
+// MMA B fragment of row m).  x' = x * 2^s is the scaled copy, f = 2^-s and
+// X_g the sum of x over the group, added as ((X_0 + X_1) + X_2) + X_3 from
+// the sums X_c of the 32 values of each lane class c.
 // The 80-byte stride keeps the 16-byte loads of 8 lanes on distinct bank
 // groups.
 template <int MODE> struct Pkg;
@@ -433,12 +434,12 @@ template <int MODE> struct Acc {
   static constexpr int kN = (MODE == kMMA1) ? 2 : (MODE == kMMA16 ? 8 : 4);
 };
 
-// One chunk: every tile of the quad for one group, added into seg[t][*].
+// One chunk: every tile of the quad for one group (weights in the ring slot
+// sl, the group's activation package at pk), added into seg[t][*].
 template <int MODE>
-__device__ __forceinline__ void compute_chunk(const uint8_t* sl, int ntiles, int lane,
+__device__ __forceinline__ void compute_chunk(const uint8_t* sl, const uint8_t* pk, int ntiles, int lane,
                                               float (&seg)[kQuadTiles][Acc<MODE>::kN]) {
   const int r = lane >> 2, c = lane & 3;
-  const uint8_t* pk = sl + kQuadTiles * kBlockBytes;
   const int row = multi_row<MODE>() ? r : 0;
   const uint32_t* xr = reinterpret_cast<const uint32_t*>(pk + row * Pkg<MODE>::kRowBytes + c * 80);
   uint32_t xw[16];
@@ -679,7 +680,8 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
         break;
       }
       const int ntiles = cc.ntiles;
-      compute_chunk<MODE>(ring + slot * kSlot, ntiles, lane, seg);
+      const uint8_t* sl = ring + slot * kSlot;
+      compute_chunk<MODE>(sl, sl + kQuadTiles * kBlockBytes, ntiles, lane, seg);
 
       // Slot consumed: refill it with the chunk D ahead.
       __syncwarp();
@@ -881,8 +883,8 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
 // Lane class c of one (group, x row) package row, built by four consecutive
 // lanes (lane & ~3 .. + 3, one per class), which agree on the row's scale 2^s
 // from the largest magnitude among their 128 values: x' = x 2^s as fp16 pairs
-// in operand order, the class sum X_c and f = 2^-s go to dst + 80 c, and lane
-// c == 0 writes the row's (X_g, f) to tail[0..1].  xg: the row's 128 values of
+// in operand order go to dst + 80 c (64 bytes), and lane c == 0 writes the
+// row's (X_g, f), f = 2^-s, to tail[0..1].  xg: the row's 128 values of
 // the group, or nullptr for a zero row (then the row is written as zeros);
 // dst == nullptr writes nothing.  Every lane of the warp must call it (it
 // shuffles).
@@ -919,18 +921,15 @@ __device__ __forceinline__ void build_row_class(const uint16_t* xg, int c, int l
   const float up = __int_as_float((127 + sft) << 23);
   const float f = __int_as_float((127 - sft) << 23);
   if (dst != nullptr) {
-    uint32_t h[20];
+    uint32_t h[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const float2 v = fmul2(make_float2(bf16_lo(w[i]), bf16_hi(w[i])), make_float2(up, up));
       asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h[i]) : "f"(v.y), "f"(v.x));  // (hi, lo)
     }
-    h[16] = __float_as_uint(X);
-    h[17] = __float_as_uint(f);
-    h[18] = h[19] = 0u;
     uint4* o = reinterpret_cast<uint4*>(dst + c * 80);
 #pragma unroll
-    for (int i = 0; i < 5; ++i) o[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+    for (int i = 0; i < 4; ++i) o[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
   }
   // group sum of the row: ((X_0 + X_1) + X_2) + X_3 over its four lane classes
   const float X0 = __shfl_sync(0xffffffffu, X, lane & ~3);
