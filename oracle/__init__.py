@@ -49,6 +49,7 @@ def _load(mutant=0):
     lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
     lib.oracle_bf16_rn.restype = ctypes.c_uint16
     lib.oracle_bf16_rn.argtypes = [ctypes.c_double]
+    lib.oracle_bf16_rn_array.argtypes = [p, ctypes.c_size_t, p]
     lib.oracle_bf16_ulp.restype = ctypes.c_double
     lib.oracle_bf16_ulp.argtypes = [ctypes.c_double]
     lib.oracle_pack_canonical.argtypes = [p, i, i, p]
@@ -86,6 +87,13 @@ class Oracle:
 
     def bf16_rn(self, v):
         return int(self.lib.oracle_bf16_rn(float(v)))
+
+    def bf16_rn_array(self, v):
+        """bf16_rn of every element: uint16 bits, same shape."""
+        v, vp = _c(v, np.float64)
+        out = np.empty(v.shape, dtype=np.uint16)
+        self.lib.oracle_bf16_rn_array(vp, v.size, out.ctypes.data_as(ctypes.c_void_p))
+        return out
 
     def bf16_ulp(self, v):
         return self.lib.oracle_bf16_ulp(float(v))
@@ -215,7 +223,7 @@ def _add_rmsnorm(self, y, residual, gamma, eps):
 Oracle.add_rmsnorm = _add_rmsnorm
 
 
-def norm_bounds(h_ref, out_ref, a, gamma, eps, oracle=None):
+def norm_bounds(h_ref, out_ref, a, gamma, eps, oracle=None, mutant=0):
     """Acceptance bounds for the fused residual add + RMS norm.
 
     h: the product's bound carried over, |h_gpu - h_ref| <= dh = 4e-3*a +
@@ -227,16 +235,35 @@ def norm_bounds(h_ref, out_ref, a, gamma, eps, oracle=None):
     products), and
         |out_gpu - out_ref| <= |gamma| r (1 + rho) dh + |out_ref| rho + ulp_bf16(out_ref),
     r = 1/sqrt(ms).  Returns (dh, dout); rows whose D reaches ms get an
-    infinite bound (no information left)."""
+    infinite bound (no information left).
+
+    mutant (negative controls for the pins only): 1 drops the |out_ref| rho
+    term, 2 drops the (1 + rho) factor of the first term, 3 drops the factor 2
+    in D."""
     o = oracle or Oracle()
     h_ref = np.asarray(h_ref, dtype=np.float64)
     out_ref = np.asarray(out_ref, dtype=np.float64)
     g = np.abs(bf16_bits_to_f64(gamma))[None, :]
     dh = 4e-3 * np.asarray(a, dtype=np.float64) + o.bf16_ulp_array(h_ref)
     ms = np.mean(h_ref * h_ref, axis=1, keepdims=True) + float(eps)
-    D = np.mean(2.0 * np.abs(h_ref) * dh + dh * dh, axis=1, keepdims=True)
+    two = 1.0 if mutant == 3 else 2.0
+    D = np.mean(two * np.abs(h_ref) * dh + dh * dh, axis=1, keepdims=True)
     with np.errstate(divide="ignore", invalid="ignore"):
         rho = np.where(D < ms, 1.0 / np.sqrt(np.maximum(1.0 - D / ms, 1e-300)) - 1.0, np.inf) + 2.0 ** -20
         r = 1.0 / np.sqrt(ms)
-    dout = g * r * (1.0 + rho) * dh + np.abs(out_ref) * rho + o.bf16_ulp_array(out_ref)
+    first = g * r * dh if mutant == 2 else g * r * (1.0 + rho) * dh
+    with np.errstate(invalid="ignore"):
+        second = 0.0 if mutant == 1 else np.abs(out_ref) * rho
+    dout = first + second + o.bf16_ulp_array(out_ref)
+    # rows with no information left: infinite everywhere (0 * inf would be NaN)
+    dout = np.where(np.isinf(rho), np.inf, dout)
     return dh, dout
+
+
+def accept_norm(h_gpu, out_gpu, h_ref, out_ref, a, gamma, eps, oracle=None):
+    """Per-element acceptance of the residual add + RMS norm call: h within
+    dh and out within dout of norm_bounds.  Returns (ok_h, ok_out)."""
+    dh, dout = norm_bounds(h_ref, out_ref, a, gamma, eps, oracle)
+    ok_h = np.abs(np.asarray(h_gpu, dtype=np.float64) - h_ref) <= dh
+    ok_out = np.abs(np.asarray(out_gpu, dtype=np.float64) - out_ref) <= dout
+    return ok_h, ok_out

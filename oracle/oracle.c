@@ -96,6 +96,11 @@ uint16_t oracle_bf16_rn(double v) {
     return (uint16_t)(sign | (u >> 16));
 }
 
+/* oracle_bf16_rn over an array (for comparing whole outputs bit for bit). */
+void oracle_bf16_rn_array(const double* v, size_t n, uint16_t* out) {
+    for (size_t i = 0; i < n; i++) out[i] = oracle_bf16_rn(v[i]);
+}
+
 /* One unit in the last place of bf16 at v: 2^(max(floor(log2|v|), -126) - 7);
  * 2^-133 at v = 0. */
 double oracle_bf16_ulp(double v) {

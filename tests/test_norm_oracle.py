@@ -123,14 +123,132 @@ def test_composition_with_gemm():
     assert np.array_equal(h, y)
 
 
-def test_bounds_shape():
+BOUNDS_GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "norm_bounds_rows.txt")
+
+
+def bounds_rows():
+    rows = []
+    for line in open(BOUNDS_GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        name, eps, h, out, gam, a, dh, dout = [f.strip() for f in line.split(";")]
+        fl = lambda s: np.array([float(v) for v in s.split(",")])
+        hx = lambda s: np.array([int(v, 16) for v in s.split(",")], dtype=np.uint16)
+        rows.append((name, float(eps), fl(h), fl(out), hx(gam), fl(a), fl(dh), fl(dout)))
+    return rows
+
+
+def bounds_golden_mismatches(mutant=0):
+    O = oracle.Oracle()
+    bad = 0
+    for name, eps, h, out, gam, a, dh_exp, dout_exp in bounds_rows():
+        dh, dout = oracle.norm_bounds(h[None, :], out[None, :], a[None, :], gam, eps, O, mutant=mutant)
+        bad += not np.allclose(dh[0], dh_exp, rtol=1e-12, atol=0)
+        fin = np.isfinite(dout_exp)
+        bad += not np.array_equal(np.isfinite(dout[0]), fin)
+        bad += not np.allclose(dout[0][fin], dout_exp[fin], rtol=1e-12, atol=0)
+    return bad
+
+
+def test_bounds_golden_rows():
+    """The bound's value on hand-worked rows (tests/golden/norm_bounds_rows.txt)."""
+    assert len(bounds_rows()) == 2
+    assert bounds_golden_mismatches() == 0
+
+
+def worst_corner_deviation(h, gam, eps, dh):
+    """Largest |out'_n - out_n| over h' in the box |h'_j - h_j| <= dh_j, exact
+    in fp64 for each n: out'_n = gamma_n h'_n / sqrt(mean h'^2 + eps) is
+    monotone in h'_n's own offset and in the mean square, so the extremes sit
+    at h'_n = h_n +- dh_n with every other |h'_j| at its smallest or largest."""
+    N = h.size
+    g = oracle.bf16_bits_to_f64(gam)
+    out = g * h / np.sqrt(np.mean(h * h) + eps)
+    lo = np.maximum(np.abs(h) - dh, 0.0) ** 2
+    hi = (np.abs(h) + dh) ** 2
+    best = np.zeros(N)
+    for sign in (1.0, -1.0):
+        hn = h + sign * dh
+        for total, own in ((lo.sum(), lo), (hi.sum(), hi)):
+            o = g * hn / np.sqrt((total - own + hn * hn) / N + eps)
+            best = np.maximum(best, np.abs(o - out))
+    return best, out
+
+
+def random_bound_rows(seed, count=150):
+    rng = np.random.default_rng(seed)
+    for _ in range(count):
+        N = int(rng.integers(2, 300))
+        eps = float(rng.choice([0.0, 1e-6, 0.5]))
+        h = np.round(rng.standard_normal(N) * 64) / 64 * float(rng.choice([1.0, 0.01, 100.0]))
+        gam = bits(np.round((1 + 0.25 * rng.standard_normal(N)) * 128) / 128)
+        a = np.abs(h) * rng.uniform(1, 40, N) * float(rng.choice([0.1, 1.0, 5.0]))
+        yield h, gam, eps, a
+
+
+def bound_violations(mutant):
+    """Over random rows: (elements whose worst-case deviation exceeds the
+    bound, largest deviation / (bound - ulp(out)))."""
+    O = oracle.Oracle()
+    viol, tight = 0, 0.0
+    for h, gam, eps, a in random_bound_rows(11):
+        g = oracle.bf16_bits_to_f64(gam)
+        out = g * h / np.sqrt(np.mean(h * h) + eps)
+        dh, dout = oracle.norm_bounds(h[None, :], out[None, :], a[None, :], gam, eps, O, mutant=mutant)
+        if not np.all(np.isfinite(dout)):
+            continue
+        dev, _ = worst_corner_deviation(h, gam, eps, dh[0])
+        viol += int(np.sum(dev > dout[0]))
+        tight = max(tight, float(np.max(dev / (dout[0] - O.bf16_ulp_array(out)))))
+    return viol, tight
+
+
+def test_bound_is_sound_and_tight():
+    """Every h within dh of h_ref moves out by no more than dout (sound), and
+    the worst such h comes within 10% of the bound's arithmetic part (tight,
+    so a loose bound cannot pass every GPU test unnoticed)."""
+    viol, tight = bound_violations(0)
+    assert viol == 0
+    assert tight > 0.9
+
+
+@pytest.mark.parametrize("mutant", [1, 2, 3])
+def test_planted_bound_mistakes_are_caught(mutant):
+    """Dropping the |out| rho term (1), the (1 + rho) factor (2) or the factor
+    2 in the mean-square shift (3) fails the hand-worked rows and lets some
+    admissible h move out past the bound."""
+    assert bounds_golden_mismatches(mutant) >= 1
+    viol, _ = bound_violations(mutant)
+    assert viol > 0
+
+
+def test_bound_infinite_where_no_information_is_left():
+    """D >= ms: dout is +inf for every element of the row, zero outputs included."""
+    O = oracle.Oracle()
+    h = np.array([[0.5, 0.0, -0.5]])
+    gam = bits(np.ones(3))
+    out = oracle.bf16_bits_to_f64(gam)[None, :] * h / np.sqrt(np.mean(h * h))
+    _, dout = oracle.norm_bounds(h, out, np.full((1, 3), 1000.0), gam, 0.0, O)
+    assert np.all(np.isposinf(dout))
+
+
+def test_accept_norm_at_the_bound():
+    """An output moved to 0.99 of the bound passes, to 1.01 of it fails; the
+    same for h."""
     O = oracle.Oracle()
     rng = np.random.default_rng(5)
     y, res, gam = random_case(rng, 2, 64)
     h, out = O.add_rmsnorm(y, res, gam, 1e-6)
-    dh, dout = oracle.norm_bounds(h, out, np.abs(y) * 10, gam, 1e-6)
+    a = np.abs(y) * 10 + 1.0
+    dh, dout = oracle.norm_bounds(h, out, a, gam, 1e-6, O)
     assert dh.shape == dout.shape == (2, 64)
     assert np.all(np.isfinite(dout)) and np.all(dout > 0) and np.all(dh > 0)
+    sign = np.where(rng.random((2, 64)) < 0.5, -1.0, 1.0)
+    ok_h, ok_o = oracle.accept_norm(h + 0.99 * sign * dh, out + 0.99 * sign * dout, h, out, a, gam, 1e-6, O)
+    assert ok_h.all() and ok_o.all()
+    ok_h, ok_o = oracle.accept_norm(h + 1.01 * sign * dh, out + 1.01 * sign * dout, h, out, a, gam, 1e-6, O)
+    assert not ok_h.any() and not ok_o.any()
 
 
 @pytest.mark.parametrize("mutant", [7, 8, 9])
