@@ -17,7 +17,7 @@ def L():
 
 def test_every_header_symbol_is_exported(L):
     names = w.exported_symbols()
-    assert len(names) == 17
+    assert len(names) == 19
     for n in names:
         assert hasattr(L, n), n
 
@@ -131,3 +131,51 @@ def test_error_raises_in_binding():
         w.w4g128_gemv(FAKE, FAKE, FAKE, 100, 16, FAKE, ws_bytes=1 << 20, stream=0)
     assert ei.value.status == E_SHAPE
     assert ctypes.sizeof(w._Matrix) == 32
+
+
+def test_selftest_argument_errors(L):
+    assert L.w4g128_selftest_wait(None, 512, 1000, 0, None) == E_INVALID
+    assert L.w4g128_selftest_wait(FAKE, 512, 1000, 2, None) == E_INVALID
+    assert L.w4g128_selftest_wait(FAKE, 512, 0, 0, None) == E_INVALID
+    assert L.w4g128_selftest_wait(FAKE, 512, 3_000_000_000, 0, None) == E_INVALID
+    assert L.w4g128_selftest_wait(FAKE + 8, 512, 1000, 0, None) == E_ALIGN
+    assert L.w4g128_selftest_wait(FAKE, 511, 1000, 0, None) == E_WS
+    assert L.w4g128_noalloc_status(None, None) == E_INVALID
+
+
+_FAULT_CHILD = """
+import sys
+sys.path.insert(0, {root!r})
+import int4_weight_only_g128_gb300 as w
+L = w.lib()
+F = 0x10000
+mats = (w._Matrix * 1)()
+mats[0] = w._Matrix(F, F, F, 128, 16)
+print(L.w4g128_gemv(F, F, F, 128, 16, F, 1 << 20, None),
+      L.w4g128_gemm_verify(F, F, F, 8, 128, 16, F, 1 << 20, None),
+      L.w4g128_decode_step(mats, 1, 1, F, 1 << 20, None),
+      L.w4g128_gemm_add_rmsnorm(F, F + 0x800, F + 0x1000, F + 0x2000, 1e-6, F + 0x1000, F + 0x3000, 1, 128, 16,
+                                0, F, 1 << 20, None),
+      L.w4g128_gemv_noalloc(F, F, F, 128, 16, None),
+      L.w4g128_pack(F, F, F, 128, 16, F, None),
+      L.w4g128_selftest_wait(F, 512, 1000, 0, None),
+      L.w4g128_gemv(F, F, F, 100, 16, F, 1 << 20, None))
+"""
+
+
+@pytest.mark.parametrize("mode,status", [("launch", E_CUDA), ("workspace", E_WS)])
+def test_host_fault_hook(mode, status):
+    """W4G128_FAULT makes every compute entry point return the injected error
+    after argument validation and before touching the device (no GPU needed);
+    argument errors still come first."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, W4G128_FAULT=mode)
+    out = subprocess.run([sys.executable, "-c", _FAULT_CHILD.format(root=root)], env=env, capture_output=True,
+                         text=True, timeout=120)
+    assert out.returncode == 0, out.stderr
+    codes = [int(v) for v in out.stdout.split()]
+    assert codes[:-1] == [status] * 7
+    assert codes[-1] == E_SHAPE

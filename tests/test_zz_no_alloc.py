@@ -4,10 +4,11 @@ Some callers cannot give the library a device workspace because they must
 not allocate device memory -- plugin hooks of another runtime that owns the
 memory budget, fixed-pool servers, latency-critical threads that must not call
 cudaMalloc.  This entry point keeps its scratch in a fixed array inside the
-library.  The test calls it through the C ABI several times in a row and
-checks every output against the regular w4g128_gemv (same tolerance as the
-parity tests, and in fact the same bits), so stale scratch contents from one
-call cannot leak into the next.  It lives in its own file so that it runs last.
+library.  The test calls it through the C ABI several times in a row, with
+and without synchronising between calls, and checks every output against the
+fp64 oracle (same tolerance as the parity tests) and bit for bit against the
+regular w4g128_gemv, so stale scratch contents from one call cannot leak into
+the next.  It lives in its own file so that it runs last.
 """
 import numpy as np
 import pytest
@@ -20,12 +21,16 @@ import synth  # noqa: E402
 from gpu_helpers import SEED, DevMatrix, to_dev, to_host, workspace  # noqa: E402
 
 
-def noalloc(mat, x_bits):
+def noalloc(mat, x_bits, sync=True):
     y = torch.empty(mat.N, dtype=torch.int16, device="cuda")
-    rc = w.lib().w4g128_gemv_noalloc(mat.packed.data_ptr(), to_dev(x_bits).data_ptr(), y.data_ptr(),
+    xd = to_dev(x_bits)
+    rc = w.lib().w4g128_gemv_noalloc(mat.packed.data_ptr(), xd.data_ptr(), y.data_ptr(),
                                      mat.K, mat.N, torch.cuda.current_stream().cuda_stream)
     assert rc == 0, w.w4g128_status_string(rc)
+    if not sync:
+        return y, xd
     torch.cuda.synchronize()
+    assert w.w4g128_noalloc_status() == 0
     return to_host(y, np.uint16)
 
 
@@ -38,6 +43,8 @@ def regular(mat, x_bits):
 
 @pytest.mark.gpu
 def test_noalloc_matches_gemv_on_consecutive_calls():
+    """Against the fp64 oracle (the bound of the parity tests) and bit for bit
+    against w4g128_gemv, on calls in a row that reuse the scratch."""
     O = oracle.Oracle()
     # split-K everywhere (tickets and partials live in the scratch), then a
     # different shape, then the first shape again with new activations
@@ -46,12 +53,25 @@ def test_noalloc_matches_gemv_on_consecutive_calls():
     for mat, xid in cases:
         x = synth.x(SEED, 600 + xid, 1, mat.K)
         y_new = noalloc(mat, x)
-        y_ref = regular(mat, x)
-        _, a = O.gemm(x, mat.codes, mat.scales, mat.mins)
-        ok, _ = oracle.accept(oracle.bf16_bits_to_f64(y_new)[None, :],
-                              oracle.bf16_bits_to_f64(y_ref)[None, :], a, O)
+        y_ref, a = O.gemm(x, mat.codes, mat.scales, mat.mins)
+        ok, _ = oracle.accept(oracle.bf16_bits_to_f64(y_new)[None, :], y_ref, a, O)
         assert ok.all()
-        assert np.array_equal(y_new, y_ref)
+        assert np.array_equal(y_new, regular(mat, x))
+
+
+@pytest.mark.gpu
+def test_noalloc_back_to_back_without_synchronising():
+    """Three calls on one stream with no synchronisation between them: each
+    call's first kernel waits for the previous call before it rewrites the
+    shared scratch, so every output is still bitwise w4g128_gemv's."""
+    mats = [DevMatrix(5120, 6144, matrix_id=511), DevMatrix(6144, 5120, matrix_id=512),
+            DevMatrix(1152, 208, matrix_id=513)]
+    xs = [synth.x(SEED, 620 + i, 1, m.K) for i, m in enumerate(mats)]
+    pending = [noalloc(m, x, sync=False) for m, x in zip(mats, xs)]
+    torch.cuda.synchronize()
+    assert w.w4g128_noalloc_status() == 0
+    for m, x, (y, _) in zip(mats, xs, pending):
+        assert np.array_equal(to_host(y, np.uint16), regular(m, x))
 
 
 @pytest.mark.gpu
