@@ -110,18 +110,29 @@ typedef uint16_t w4g128_bf16;
 /* Human-readable name of a status code (static string). */
 W4G128_API const char* w4g128_status_string(int status);
 
-/* Exact byte size of the packed form of a K x N matrix: K*N/2 + 4*(K/128)*N.
- * Returns 0 for an invalid shape. */
+/* Exact byte size of the packed form of a K x N matrix: K*N/2 + 4*(K/128)*N,
+ * i.e. 4 bits per code plus one bf16 scale and one bf16 minimum per 128
+ * weights, 4.25 bits per weight (Token Rush README, intro bullet "4.25 bits
+ * per weight" and the "Quantization" section).  Returns 0 for an invalid
+ * shape. */
 W4G128_API size_t w4g128_packed_bytes(int K, int N);
 
-/* Canonical -> packed layout (a bit permutation; bit-exact).  codes, scales,
- * mins and packed are device pointers; packed must hold
- * w4g128_packed_bytes(K, N) bytes.  Runs once per weight matrix, not per
- * decode step. */
+/* Canonical -> packed layout (a bit permutation; bit-exact).  The format is
+ * the pages' group-wise asymmetric int4 with one bf16 scale and minimum per
+ * 128 weights (Token Rush README, "Quantization" section); the packed byte
+ * order is this library's own (PACKED LAYOUT above).  codes, scales, mins and
+ * packed are device pointers (caller-owned); packed must hold
+ * w4g128_packed_bytes(K, N) bytes and is written in full, nothing past it.
+ * Runs once per weight matrix, not per decode step.  Asynchronous on
+ * `stream`; argument errors are returned before anything is launched. */
 W4G128_API int w4g128_pack(const uint32_t* codes, const w4g128_bf16* scales, const w4g128_bf16* mins,
                            int K, int N, void* packed, void* stream);
 
-/* Exact inverse of w4g128_pack (for round-trip checks and export). */
+/* Exact inverse of w4g128_pack (for round-trip checks and export): the
+ * canonical codes, scales and mins of the "Quantization" section's format
+ * (Token Rush README) back from the packed layout.  Device pointers, caller-
+ * owned; same shapes and alignment as w4g128_pack.  Asynchronous on
+ * `stream`. */
 W4G128_API int w4g128_unpack(const void* packed, int K, int N, uint32_t* codes, w4g128_bf16* scales,
                              w4g128_bf16* mins, void* stream);
 
@@ -143,7 +154,11 @@ W4G128_API int w4g128_quantize(const w4g128_bf16* w, int K, int N, int search, u
                                w4g128_bf16* scales, w4g128_bf16* mins, void* stream);
 
 /* Workspace bytes needed by w4g128_gemm_verify(M, K, N) on the current
- * device (and by w4g128_gemv, M = 1).  Returns 0 for invalid arguments. */
+ * device (and by w4g128_gemv, M = 1): the activation packages, the split-K
+ * partial sums (Token Rush README, progress table steps 8-9: the split-K
+ * GEMV's partial sums), the fold counters and the status word.  The size
+ * depends on the SM count of the current device.  Returns 0 for invalid
+ * arguments or when the current device is not compute capability 10.3. */
 W4G128_API size_t w4g128_workspace_bytes(int M, int K, int N);
 
 /* y[1][N] = x[1][K] . dequant(W): the batch-1 decode GEMV (streamed by TMA
@@ -175,7 +190,11 @@ typedef struct {
 } w4g128_matrix;
 
 /* Workspace bytes for w4g128_decode_step or w4g128_verify_step over these
- * matrices at this M. */
+ * matrices at this M (Token Rush README, progress table step 4 and the
+ * "bandwidth ceiling" paragraph: one pass over every weight of a step); the
+ * same parts as w4g128_workspace_bytes, for all matrices at once.  `mats`
+ * is a host array; only K and N are read.  Returns 0 for invalid
+ * arguments. */
 W4G128_API size_t w4g128_decode_step_workspace_bytes(const w4g128_matrix* mats, int count, int M);
 
 /* Streams every matrix of `mats` (a HOST array of `count` descriptors,
@@ -244,11 +263,13 @@ W4G128_API int w4g128_gemm_add_rmsnorm(const void* packed, const w4g128_bf16* x,
  * until the process exits.  Shapes whose workspace would exceed it (the
  * limit is reached near K*N = 2^31 weights; a 5120 x 248320 lm_head needs
  * 10 MB) return W4G128_ERR_WORKSPACE before anything is launched.  The first
- * call on each device looks up the array's device address; make that first
- * call before any stream capture.  All calls share the one array, so calls
- * that can overlap on the GPU (other streams, other host threads) race and
- * corrupt each other; serialise them.  The status word of the last call is
- * not readable through w4g128_workspace_status. */
+ * call on each device loads the array's module and looks up its device
+ * address (every call repeats the lookup, so a reset device is handled);
+ * make that first call before any stream capture.  All calls share the one
+ * array, so calls that can overlap on the GPU (other streams, other host
+ * threads) race and corrupt each other; serialise them (calls in order on
+ * one stream are fine).  The status word of the last call is read with
+ * w4g128_noalloc_status. */
 W4G128_API int w4g128_gemv_noalloc(const void* packed, const w4g128_bf16* x, w4g128_bf16* y, int K, int N,
                                    void* stream);
 
@@ -256,6 +277,37 @@ W4G128_API int w4g128_gemv_noalloc(const void* packed, const w4g128_bf16* x, w4g
  * W4G128_ERR_TIMEOUT if a bounded device wait gave up).  Synchronises
  * `stream`. */
 W4G128_API int w4g128_workspace_status(const void* ws, int* status_out, void* stream);
+
+/* The status word the last w4g128_gemv_noalloc call on the current device
+ * left in the library's scratch array (W4G128_OK, or W4G128_ERR_TIMEOUT if a
+ * bounded device wait gave up, in which case that call's y is incomplete).
+ * No counterpart in the pages, like the entry point it serves.  Synchronises
+ * `stream`. */
+W4G128_API int w4g128_noalloc_status(int* status_out, void* stream);
+
+/* Workspace bytes w4g128_selftest_wait needs. */
+#define W4G128_SELFTEST_WS_BYTES 512u
+
+/* Diagnostic of the bounded device-side waits; the pages have no
+ * counterpart (no wait in this library's kernels can spin forever: each
+ * gives up after a time limit and records W4G128_ERR_TIMEOUT in the status
+ * word instead).  Launches one small kernel on `stream` that clears the
+ * status word of `ws`, stores 1 (set_flag = 1) or 0 (set_flag = 0) in a flag
+ * word of `ws`, and then waits with the library's bounded flag wait for the
+ * flag to be nonzero, for at most limit_ns nanoseconds (1 .. 2e9).  With
+ * set_flag = 0 nothing ever sets the flag: the wait runs out and
+ * w4g128_workspace_status(ws) then reads W4G128_ERR_TIMEOUT; with
+ * set_flag = 1 it reads W4G128_OK.  Either way the kernel returns on its own
+ * and `ws` is usable by any later call (every call re-initialises what it
+ * needs).  ws: device, 16-byte aligned, ws_bytes >= W4G128_SELFTEST_WS_BYTES.
+ *
+ * Every compute entry point of this header also honours the environment
+ * variable W4G128_FAULT, read once per process, for tests of callers' error
+ * handling: "launch" makes it return W4G128_ERR_CUDA and "workspace"
+ * W4G128_ERR_WORKSPACE after argument validation, without touching the
+ * device. */
+W4G128_API int w4g128_selftest_wait(void* ws, size_t ws_bytes, unsigned long long limit_ns, int set_flag,
+                                    void* stream);
 
 #ifdef __cplusplus
 }

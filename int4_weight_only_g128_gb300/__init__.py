@@ -16,13 +16,15 @@ __all__ = [
     "w4g128_workspace_bytes", "w4g128_gemv", "w4g128_gemm_verify",
     "w4g128_decode_step_workspace_bytes", "w4g128_decode_step", "w4g128_verify_step", "w4g128_workspace_status",
     "w4g128_probe_read", "w4g128_probe_copy", "w4g128_probe_sink_bytes", "w4g128_gemv_noalloc",
-    "MAX_M", "MAX_MATRICES",
+    "w4g128_noalloc_status", "w4g128_selftest_wait", "w4g128_gemm_add_rmsnorm",
+    "MAX_M", "MAX_MATRICES", "SELFTEST_WS_BYTES",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
-MAX_M = 8
-MAX_MATRICES = 512
+MAX_M = 16          # W4G128_MAX_M
+MAX_MATRICES = 512  # W4G128_MAX_MATRICES
+SELFTEST_WS_BYTES = 512  # W4G128_SELFTEST_WS_BYTES
 
 _lib = None
 
@@ -95,6 +97,10 @@ def lib():
     L.w4g128_verify_step.argtypes = [ctypes.POINTER(_Matrix), i, i, p, sz, p]
     L.w4g128_gemv_noalloc.restype = i
     L.w4g128_gemv_noalloc.argtypes = [p, p, p, i, i, p]
+    L.w4g128_noalloc_status.restype = i
+    L.w4g128_noalloc_status.argtypes = [ctypes.POINTER(ctypes.c_int), p]
+    L.w4g128_selftest_wait.restype = i
+    L.w4g128_selftest_wait.argtypes = [p, sz, ctypes.c_ulonglong, i, p]
     L.w4g128_gemm_add_rmsnorm.restype = i
     L.w4g128_gemm_add_rmsnorm.argtypes = [p, p, p, p, ctypes.c_float, p, p, i, i, i, i, p, sz, p]
     _lib = L
@@ -225,3 +231,17 @@ def w4g128_gemv_noalloc(packed, x, y, K, N, stream=None):
     allocate device memory (see include/w4g128.h)."""
     _check("w4g128_gemv_noalloc", lib().w4g128_gemv_noalloc(_ptr(packed), _ptr(x), _ptr(y), K, N,
                                                             _stream(stream)))
+
+
+def w4g128_noalloc_status(stream=None):
+    """Status word the last w4g128_gemv_noalloc call on this device left."""
+    out = ctypes.c_int(0)
+    _check("w4g128_noalloc_status", lib().w4g128_noalloc_status(ctypes.byref(out), _stream(stream)))
+    return out.value
+
+
+def w4g128_selftest_wait(ws, limit_ns, set_flag, ws_bytes=None, stream=None):
+    """Diagnostic: a bounded device wait on a flag of `ws` (see include/w4g128.h)."""
+    wb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    _check("w4g128_selftest_wait", lib().w4g128_selftest_wait(_ptr(ws), wb, int(limit_ns), int(set_flag),
+                                                              _stream(stream)))

@@ -42,6 +42,8 @@ int run_stream(const w4g128_matrix* mats, int count, int M, void* ws, size_t ws_
                const w4g128::NormArgs* norm = nullptr) {
   int rc = check_stream_call(mats, count, M, ws);
   if (rc != W4G128_OK) return rc;
+  rc = w4g128::fault_hook();
+  if (rc != W4G128_OK) return rc;
   if (!w4g128::device_is_sm103()) return W4G128_ERR_DEVICE;
   static_assert(sizeof(HostMatrix) == sizeof(w4g128_matrix), "descriptor layout");
   HostMatrix hm[W4G128_MAX_MATRICES];
@@ -88,6 +90,7 @@ int w4g128_pack(const uint32_t* codes, const w4g128_bf16* scales, const w4g128_b
   if (!shape_ok(K, N)) return W4G128_ERR_SHAPE;
   if (!aligned(codes, 4) || !aligned(scales, 4) || !aligned(mins, 4) || !aligned(packed, 16))
     return W4G128_ERR_ALIGN;
+  if (w4g128::fault_hook() != W4G128_OK) return w4g128::fault_hook();
   if (!w4g128::device_is_sm103()) return W4G128_ERR_DEVICE;
   return w4g128::launch_pack(codes, scales, mins, K, N, packed, as_stream(stream));
 }
@@ -98,6 +101,7 @@ int w4g128_unpack(const void* packed, int K, int N, uint32_t* codes, w4g128_bf16
   if (!shape_ok(K, N)) return W4G128_ERR_SHAPE;
   if (!aligned(codes, 4) || !aligned(scales, 4) || !aligned(mins, 4) || !aligned(packed, 16))
     return W4G128_ERR_ALIGN;
+  if (w4g128::fault_hook() != W4G128_OK) return w4g128::fault_hook();
   if (!w4g128::device_is_sm103()) return W4G128_ERR_DEVICE;
   return w4g128::launch_unpack(packed, K, N, codes, scales, mins, as_stream(stream));
 }
@@ -108,6 +112,7 @@ int w4g128_quantize(const w4g128_bf16* w, int K, int N, int search, uint32_t* co
   if (search != 0 && search != 1) return W4G128_ERR_INVALID_ARG;
   if (!shape_ok(K, N)) return W4G128_ERR_SHAPE;
   if (!aligned(w, 4) || !aligned(codes, 4) || !aligned(scales, 4) || !aligned(mins, 4)) return W4G128_ERR_ALIGN;
+  if (w4g128::fault_hook() != W4G128_OK) return w4g128::fault_hook();
   if (!w4g128::device_is_sm103()) return W4G128_ERR_DEVICE;
   return w4g128::launch_quantize(w, K, N, search, codes, scales, mins, as_stream(stream));
 }

@@ -67,4 +67,10 @@ int read_workspace_status(const void* ws, int* status_out, cudaStream_t stream);
 // Current device is compute capability 10.3; caches per device.
 bool device_is_sm103();
 
+// Host-only fault injection for tests of the error paths: W4G128_OK, or the
+// status that the environment variable W4G128_FAULT ("launch" ->
+// W4G128_ERR_CUDA, "workspace" -> W4G128_ERR_WORKSPACE) makes every compute
+// entry point return before it touches the device.  Read once per process.
+int fault_hook();
+
 }  // namespace w4g128

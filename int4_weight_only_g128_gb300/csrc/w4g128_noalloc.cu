@@ -11,13 +11,16 @@
 // loads it, for the life of the process.
 //
 // The scratch array is a plain __device__ variable.  In host code its name is
-// a host-side stand-in, not a device address, so the address is fetched once
-// per device with cudaGetSymbolAddress (with that device current) and passed
-// to the kernels like any caller-owned workspace.
+// a host-side stand-in, not a device address, so every call looks the address
+// up with cudaGetSymbolAddress (with the call's device current) and passes it
+// to the kernels like any caller-owned workspace.  The lookup is repeated on
+// every call rather than cached: after cudaDeviceReset, or after the primary
+// context is released and created again, the module is loaded afresh and the
+// array may sit at another address.  The first call on a device loads the
+// module there (the set-up); make it before any stream capture.
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "w4g128.h"
 #include "w4g128_internal.h"
@@ -30,28 +33,14 @@ static __device__ __align__(256) unsigned char g_w4g128_scratch[W4G128_NOALLOC_S
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device, looked up once
-// per device (the first call on each device does this set-up).
+// Device address of the scratch array in the current context.
 int scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_w4g128_scratch) != cudaSuccess || p == nullptr) {
     cudaGetLastError();
-    return W4G128_ERR_DEVICE;
+    return W4G128_ERR_CUDA;
   }
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_w4g128_scratch) != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return W4G128_ERR_CUDA;
-    }
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return W4G128_OK;
 }
 
@@ -65,6 +54,7 @@ extern "C" int w4g128_gemv_noalloc(const void* packed, const w4g128_bf16* x, w4g
   if (!(K >= 128 && K <= 65536 && K % 128 == 0 && N >= 16 && N <= (1 << 24) && N % 16 == 0))
     return W4G128_ERR_SHAPE;
   if (!aligned(packed, 16) || !aligned(x, 4) || !aligned(y, 4)) return W4G128_ERR_ALIGN;
+  if (w4g128::fault_hook() != W4G128_OK) return w4g128::fault_hook();
   if (!w4g128::device_is_sm103()) return W4G128_ERR_DEVICE;
   const w4g128::HostMatrix m{packed, x, y, K, N};
   const size_t need = w4g128::stream_workspace_bytes(&m, 1, 1);
@@ -75,4 +65,13 @@ extern "C" int w4g128_gemv_noalloc(const void* packed, const w4g128_bf16* x, w4g
   if (rc != W4G128_OK) return rc;
   return w4g128::launch_stream(&m, 1, 1, nullptr, scratch, W4G128_NOALLOC_SCRATCH_BYTES,
                                static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int w4g128_noalloc_status(int* status_out, void* stream) {
+  if (status_out == nullptr) return W4G128_ERR_INVALID_ARG;
+  if (!w4g128::device_is_sm103()) return W4G128_ERR_DEVICE;
+  void* scratch = nullptr;
+  const int rc = scratch_address(&scratch);
+  if (rc != W4G128_OK) return rc;
+  return w4g128::read_workspace_status(scratch, status_out, static_cast<cudaStream_t>(stream));
 }

@@ -7,8 +7,9 @@
 
 namespace w4g128 {
 
-// Give up on a device-side wait after this many nanoseconds.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Default limit of a device-side wait, in nanoseconds; kernels take the
+// limit as a parameter (a diagnostic entry point shortens it).
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -54,13 +55,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait: returns false if the phase did not complete within
-// kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// limit_ns nanoseconds.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -76,8 +77,9 @@ __device__ __forceinline__ void st_relaxed_u64(unsigned long long* a, unsigned l
 }
 
 // Bounded wait until the word at `a` is nonzero; its last value goes to
-// `seen`.  Returns false if that did not happen within kWaitLimitNs.
-__device__ __forceinline__ bool wait_nonzero_bounded(const unsigned long long* a, unsigned long long& seen) {
+// `seen`.  Returns false if that did not happen within limit_ns nanoseconds.
+__device__ __forceinline__ bool wait_nonzero_bounded(const unsigned long long* a, unsigned long long& seen,
+                                                     uint64_t limit_ns) {
   seen = ld_relaxed_u64(a);
   if (seen != 0ull) return true;
   const uint64_t t0 = global_timer_ns();
@@ -85,7 +87,7 @@ __device__ __forceinline__ bool wait_nonzero_bounded(const unsigned long long* a
     __nanosleep(64);
     seen = ld_relaxed_u64(a);
     if (seen != 0ull) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 

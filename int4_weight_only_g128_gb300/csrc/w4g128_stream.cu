@@ -188,6 +188,7 @@ struct StreamParams {
   int count, M, W, total_quads, total_groups;
   int per_warp_reduce;   // M >= 2: the split quads are folded per streaming warp (else per quad)
   int depth;             // ring slots per warp (ring_depth of the mode)
+  unsigned long long wait_ns;  // limit of every device-side wait
   MatParams mats[MAXMAT];
 };
 
@@ -667,13 +668,13 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
     int slot = 0;          // done % D
     uint32_t parity = 0u;  // (done / D) & 1
     while (cc.item < it_b) {
-      if (!mbar_wait_bounded(bar0 + 8 * slot, parity)) {
+      if (!mbar_wait_bounded(bar0 + 8 * slot, parity, p.wait_ns)) {
         // Give up: record the timeout, drain this warp's copies in flight
         // (again bounded) and leave.  Quads this warp shared stay unreduced.
         if (lane == 0) {
           atomicCAS(p.status, 0u, static_cast<unsigned>(W4G128_ERR_TIMEOUT));
           for (unsigned k = done + 1; k < issued; ++k)
-            (void)mbar_wait_bounded(bar0 + 8 * static_cast<int>(k % D), (k / D) & 1u);
+            (void)mbar_wait_bounded(bar0 + 8 * static_cast<int>(k % D), (k / D) & 1u, p.wait_ns);
         }
         __syncwarp();
         failed = true;
@@ -1099,11 +1100,11 @@ __global__ void __launch_bounds__(kRedThreads) reduce_quads_kernel(const __grid_
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int ch = 0; ch < nchunks; ++ch) {
     if (threadIdx.x == 0) {
-      const bool got = mbar_wait_bounded(bar0 + 8 * (ch & 1), (ch >> 1) & 1);
+      const bool got = mbar_wait_bounded(bar0 + 8 * (ch & 1), (ch >> 1) & 1, p.wait_ns);
       if (!got) {
         // record the timeout and wait (bounded) for the other stage's copy
         atomicCAS(p.status, 0u, static_cast<unsigned>(W4G128_ERR_TIMEOUT));
-        if (ch + 1 < nchunks) (void)mbar_wait_bounded(bar0 + 8 * ((ch + 1) & 1), ((ch + 1) >> 1) & 1);
+        if (ch + 1 < nchunks) (void)mbar_wait_bounded(bar0 + 8 * ((ch + 1) & 1), ((ch + 1) >> 1) & 1, p.wait_ns);
       }
       ok = got;
     }
@@ -1157,7 +1158,8 @@ __global__ void __launch_bounds__(kRedThreads) reduce_warps_kernel(const __grid_
     __shared__ unsigned long long rec_s;
     if (threadIdx.x == 0) {
       unsigned long long r = 0ull;
-      if (!wait_nonzero_bounded(p.recs + w, r)) atomicCAS(p.status, 0u, static_cast<unsigned>(W4G128_ERR_TIMEOUT));
+      if (!wait_nonzero_bounded(p.recs + w, r, p.wait_ns))
+        atomicCAS(p.status, 0u, static_cast<unsigned>(W4G128_ERR_TIMEOUT));
       rec_s = r;
     }
     __syncthreads();
@@ -1376,6 +1378,17 @@ const DeviceInfo* device_info() {
   return &g_dev[dev];
 }
 
+// Drops the current device's cached set-up (kernel attributes, occupancy).
+void forget_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_dev_init[dev] = false;
+}
+
 struct Plan {
   int mode = 0, rows = 1, pkg = 0, depth = 2;
   bool per_warp_reduce = false;
@@ -1453,6 +1466,7 @@ void fill_params(StreamParams<MAXMAT>& sp, const HostMatrix* mats, int count, in
   sp.W = pl.W;
   sp.per_warp_reduce = pl.per_warp_reduce ? 1 : 0;
   sp.depth = pl.depth;
+  sp.wait_ns = kDefaultWaitNs;
   sp.total_quads = pl.total_quads;
   sp.total_groups = pl.total_groups;
   for (int i = 0; i < count; ++i) {
@@ -1579,9 +1593,14 @@ int launch_stream(const HostMatrix* mats, int count, int M, const NormArgs* norm
   if (!make_plan(mats, count, M, *d, pl)) return W4G128_ERR_SHAPE;
   if (ws_bytes < pl.bytes) return W4G128_ERR_WORKSPACE;
   if (norm != nullptr && count != 1) return W4G128_ERR_INVALID_ARG;
-  if (count == 1) return launch_with<1>(mats, count, M, pl, norm, ws, stream);
-  if (count <= kFewMatrices) return launch_with<kFewMatrices>(mats, count, M, pl, norm, ws, stream);
-  return launch_with<W4G128_MAX_MATRICES>(mats, count, M, pl, norm, ws, stream);
+  int rc;
+  if (count == 1) rc = launch_with<1>(mats, count, M, pl, norm, ws, stream);
+  else if (count <= kFewMatrices) rc = launch_with<kFewMatrices>(mats, count, M, pl, norm, ws, stream);
+  else rc = launch_with<W4G128_MAX_MATRICES>(mats, count, M, pl, norm, ws, stream);
+  // A failed launch may mean the context was reset since the kernels'
+  // attributes were set: the next call sets them up again.
+  if (rc == W4G128_ERR_CUDA) forget_device();
+  return rc;
 }
 
 int read_workspace_status(const void* ws, int* status_out, cudaStream_t stream) {
