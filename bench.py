@@ -542,6 +542,59 @@ def run_ours(args):
         del mats
     torch.cuda.synchronize()
 
+    # ---- a dependent chain of single calls: o -> gate+up -> down, each x the previous y (down reads the first
+    # 17408 outputs of gate+up: the activation between them is not part of the weight stream); the realistic
+    # decode order, which one decode_step cannot batch
+    chain = {}
+    CHAIN = [(6144, 5120), (5120, 34816), (17408, 5120)]
+    cbytes = sum(weight_bytes(K, N) for K, N in CHAIN)
+    ncp = max(1, -(-2 * L2_BYTES // cbytes))
+    cmats = [[pack_device(K, N, 90 + j) for j, (K, N) in enumerate(CHAIN)]]
+    for _ in range(ncp - 1):
+        cmats.append([m.clone() for m in cmats[0]])
+    for M in (1, 8):
+        x0 = torch.from_numpy(synth.x(SEED, 330, M, 6144).view(np.int16)).cuda()
+        yo = torch.empty(M * 5120, dtype=torch.int16, device="cuda")
+        yg = torch.empty(M * 34816, dtype=torch.int16, device="cuda")
+        yd = torch.empty(M * 5120, dtype=torch.int16, device="cuda")
+        wsc = torch.empty(max(w.w4g128_workspace_bytes(M, K, N) for K, N in CHAIN), dtype=torch.uint8,
+                          device="cuda")
+
+        def one(cs, r, M=M, x0=x0, yo=yo, yg=yg, yd=yd, wsc=wsc):
+            ms = cmats[r % len(cmats)]
+            if M == 1:
+                w.w4g128_gemv(ms[0], x0, yo, 6144, 5120, wsc, stream=cs)
+                w.w4g128_gemv(ms[1], yo, yg, 5120, 34816, wsc, stream=cs)
+                w.w4g128_gemv(ms[2], yg, yd, 17408, 5120, wsc, stream=cs)  # x = y_gate_up[:17408]
+            else:
+                w.w4g128_gemm_verify(ms[0], x0, yo, M, 6144, 5120, wsc, stream=cs)
+                w.w4g128_gemm_verify(ms[1], yo, yg, M, 5120, 34816, wsc, stream=cs)
+                # rows of 34816 -> rows of 17408: a strided view is not a plain [M][K] array, so
+                # the verify step reads the first M * 17408 values (each x row a slice of y)
+                w.w4g128_gemm_verify(ms[2], yg, yd, M, 17408, 5120, wsc, stream=cs)
+        us = graph_us(one, 32)
+        chain[f"M{M}"] = {"us_per_chain": round(us, 3), "GBps": round(cbytes / us / 1e3, 1),
+                          "frac": round(cbytes / us / 1e3 / peak, 4), "copies": len(cmats)}
+    chain["chain"] = "o 6144x5120 -> gate+up 5120x34816 -> down 17408x5120, single calls, each x the previous y"
+    del cmats
+    torch.cuda.synchronize()
+
+    # ---- host cost of one call (enqueue time while the GPU is busy): the list-of-tuples API, the
+    # prepared DecodeStep, and a single gemv
+    host_us = {}
+    _, _, _, descs_h, ws_h = io[1][:5]
+    step_h = w.DecodeStep(descs_h[0], 1, ws_h, stream=st)
+    for name, fn in (("decode_step_list_api", lambda: w.w4g128_decode_step(descs_h[0], 1, ws_h, stream=st)),
+                     ("decode_step_prepared", step_h.run)):
+        for _ in range(20):
+            fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(200):
+            fn()
+        host_us[name] = round((time.perf_counter() - t0) / 200 * 1e6, 2)
+        torch.cuda.synchronize()
+
     # ---- the whole decode-step weight stream: 64 layer sets + the lm_head, one decode_step call
     full = {}
     fmats = [(K, N) for _ in range(N_LAYERS) for _, K, N in LAYER] + [LM_HEAD]
@@ -615,16 +668,17 @@ def run_ours(args):
     y_pin = torch.empty(y_all.numel(), dtype=torch.int16).pin_memory()
     h2d = x_pin.numel() * 2
     d2h = y_pin.numel() * 2
+    # one w4g128_decode_step_host call per step: x in from pinned host memory, the layer streamed, y out
+    steps_e2e = [w.DecodeStep(descs[c], 1, ws, stream=st, x_host=x_pin, x_dev=x_all, y_host=y_pin, y_dev=y_all)
+                 for c in range(NCOPY)]
     for i in range(args.warmup):
-        w.w4g128_decode_step(descs[i % NCOPY], 1, ws, stream=st)
+        steps_e2e[i % NCOPY].run_host()
     barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
-        x_all.copy_(x_pin, non_blocking=True)
-        w.w4g128_decode_step(descs[i % NCOPY], 1, ws, stream=st)
-        y_pin.copy_(y_all, non_blocking=True)
+        steps_e2e[i % NCOPY].run_host()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -672,12 +726,19 @@ def run_ours(args):
         "us_per_call": per_call,
         "residual_add_rmsnorm_us": norm_fused,
         "full_decode_step": full,
+        "dependent_chain": chain,
+        "host_us_per_call": host_us,
         "bandwidth_probes": probe,
         "frac_of_read_probe": {"m1": round(achieved / probe["read_GBps"], 4),
                                "m8": round(achieved8 / probe["read_GBps"], 4)},
         "parity": {"checked": "sampled columns of all 6 matrices, M=1 and M=8, vs fp64 oracle",
                    "worst_error_over_bound": {str(k): round(v, 5) for k, v in worst.items()}},
-        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "api": "w4g128_decode_step_host (one C call per step: x in, layer streamed, y out)"},
+        "value_full_decode_step": {"workload": "64 x layer set + lm_head 5120x248320, 385 matrices, 14.04 GB, "
+                                               "one decode_step call", "M1_GBps": full["M1"]["GBps"],
+                                   "M8_GBps": full["M8"]["GBps"], "M1_frac": full["M1"]["frac"],
+                                   "M8_frac": full["M8"]["frac"]},
         "gpu_launches": 2 * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,

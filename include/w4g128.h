@@ -98,7 +98,8 @@ typedef enum {
   W4G128_ERR_WORKSPACE = 4,   /* ws_bytes smaller than the workspace query returns */
   W4G128_ERR_CUDA = 5,        /* a CUDA runtime call or a launch failed */
   W4G128_ERR_DEVICE = 6,      /* the current device is not compute capability 10.3 */
-  W4G128_ERR_TIMEOUT = 7      /* (status word only) a bounded device-side wait gave up */
+  W4G128_ERR_TIMEOUT = 7,     /* (status word only) a bounded device-side wait gave up */
+  W4G128_ERR_INTERNAL = 8     /* (status word only) a kernel found its launch inconsistent and skipped its work */
 } w4g128_status;
 
 #define W4G128_MAX_M 16
@@ -210,6 +211,29 @@ W4G128_API size_t w4g128_decode_step_workspace_bytes(const w4g128_matrix* mats, 
  * (W4G128_ERR_SHAPE beyond). */
 W4G128_API int w4g128_decode_step(const w4g128_matrix* mats, int count, int M, void* ws, size_t ws_bytes,
                                   void* stream);
+
+/* w4g128_decode_step for activations that live in host memory between
+ * steps: copies x_bytes from x_host to x_dev, streams the matrices, then
+ * copies y_bytes from y_dev to y_host -- three operations issued in that
+ * order on `stream` by one call, so a step whose input arrives from and
+ * whose output returns to the host costs one library call.  The pages keep
+ * the token on the device for the whole step (Token Rush README, progress
+ * table step 4: the whole decode step captured as one graph); this entry
+ * serves callers whose activations cross the host boundary every step.
+ * The descriptors' x must lie inside [x_dev, x_dev + x_bytes) and their y
+ * inside [y_dev, y_dev + y_bytes) (device, caller-owned); x_host and y_host
+ * are host buffers.  Pinned (device-mapped) buffers with 16-byte aligned
+ * ends and sizes that are multiples of 16 are moved by two small kernels
+ * that keep the step's kernels overlapping the previous call (a copy-engine
+ * copy between kernels would not); other buffers by cudaMemcpyAsync (with
+ * pageable memory the CUDA runtime may return only after staging them).
+ * Do not change x_host before the call has run.  x_bytes / y_bytes may be
+ * 0 (no move).  Returns what w4g128_decode_step
+ * returns, or W4G128_ERR_CUDA if a copy could not be issued; argument
+ * errors are returned before anything is issued. */
+W4G128_API int w4g128_decode_step_host(const w4g128_matrix* mats, int count, int M, const void* x_host,
+                                       void* x_dev, size_t x_bytes, void* y_host, const void* y_dev,
+                                       size_t y_bytes, void* ws, size_t ws_bytes, void* stream);
 
 /* The verify step over a list of matrices: row m of each y_i is bitwise
  * identical to w4g128_gemm_verify on matrix i and row m alone, so decoding

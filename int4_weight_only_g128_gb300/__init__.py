@@ -16,7 +16,8 @@ __all__ = [
     "w4g128_workspace_bytes", "w4g128_gemv", "w4g128_gemm_verify",
     "w4g128_decode_step_workspace_bytes", "w4g128_decode_step", "w4g128_verify_step", "w4g128_workspace_status",
     "w4g128_probe_read", "w4g128_probe_copy", "w4g128_probe_sink_bytes", "w4g128_gemv_noalloc",
-    "w4g128_noalloc_status", "w4g128_selftest_wait", "w4g128_gemm_add_rmsnorm",
+    "w4g128_noalloc_status", "w4g128_selftest_wait", "w4g128_gemm_add_rmsnorm", "w4g128_decode_step_host",
+    "DecodeStep",
     "MAX_M", "MAX_MATRICES", "SELFTEST_WS_BYTES",
 ]
 
@@ -93,6 +94,8 @@ def lib():
     L.w4g128_probe_copy.argtypes = [p, p, sz, p]
     L.w4g128_probe_sink_bytes.restype = sz
     L.w4g128_probe_sink_bytes.argtypes = []
+    L.w4g128_decode_step_host.restype = i
+    L.w4g128_decode_step_host.argtypes = [ctypes.POINTER(_Matrix), i, i, p, p, sz, p, p, sz, p, sz, p]
     L.w4g128_verify_step.restype = i
     L.w4g128_verify_step.argtypes = [ctypes.POINTER(_Matrix), i, i, p, sz, p]
     L.w4g128_gemv_noalloc.restype = i
@@ -245,3 +248,48 @@ def w4g128_selftest_wait(ws, limit_ns, set_flag, ws_bytes=None, stream=None):
     wb = _nbytes(ws) if ws_bytes is None else ws_bytes
     _check("w4g128_selftest_wait", lib().w4g128_selftest_wait(_ptr(ws), wb, int(limit_ns), int(set_flag),
                                                               _stream(stream)))
+
+
+def w4g128_decode_step_host(mats, M, x_host, x_dev, x_bytes, y_host, y_dev, y_bytes, ws, ws_bytes=None,
+                            stream=None):
+    """decode_step with the activations copied from / to host buffers in the same call."""
+    arr = _matrices(mats)
+    wb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    _check("w4g128_decode_step_host",
+           lib().w4g128_decode_step_host(arr, len(mats), M, _ptr(x_host), _ptr(x_dev), x_bytes, _ptr(y_host),
+                                         _ptr(y_dev), y_bytes, _ptr(ws), wb, _stream(stream)))
+
+
+class DecodeStep:
+    """A decode step whose arguments are marshalled once: the descriptor
+    array and the pointers are fixed, so each call is one C call.
+
+    mats: sequence of (packed, x, y, K, N); ws: the workspace.  ``run`` calls
+    w4g128_decode_step, ``run_host`` w4g128_decode_step_host with the host
+    and device buffers given here."""
+
+    def __init__(self, mats, M, ws, stream=None, x_host=None, x_dev=None, y_host=None, y_dev=None):
+        self._keep = (mats, ws, x_host, x_dev, y_host, y_dev)  # the buffers outlive the step
+        self._arr = _matrices(mats)
+        self._n = len(mats)
+        self._M = M
+        self._ws = _ptr(ws)
+        self._wb = _nbytes(ws)
+        self._stream = _stream(stream)
+        self._xh, self._xd = _ptr(x_host), _ptr(x_dev)
+        self._xb = 0 if x_host is None else _nbytes(x_host)
+        self._yh, self._yd = _ptr(y_host), _ptr(y_dev)
+        self._yb = 0 if y_host is None else _nbytes(y_host)
+        self._fn = lib().w4g128_decode_step
+        self._fn_host = lib().w4g128_decode_step_host
+
+    def run(self):
+        rc = self._fn(self._arr, self._n, self._M, self._ws, self._wb, self._stream)
+        if rc != 0:
+            raise W4G128Error("w4g128_decode_step", rc)
+
+    def run_host(self):
+        rc = self._fn_host(self._arr, self._n, self._M, self._xh, self._xd, self._xb, self._yh, self._yd, self._yb,
+                           self._ws, self._wb, self._stream)
+        if rc != 0:
+            raise W4G128Error("w4g128_decode_step_host", rc)

@@ -14,7 +14,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libw4g128.so")
 
 SOURCES = ["w4g128_api.cu", "w4g128_pack.cu", "w4g128_stream.cu", "w4g128_probe.cu", "w4g128_noalloc.cu",
-           "w4g128_quant.cu", "w4g128_selftest.cu"]
+           "w4g128_quant.cu", "w4g128_selftest.cu", "w4g128_hostio.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-I", INCLUDE, "-I", CSRC]

@@ -75,6 +75,7 @@ const char* w4g128_status_string(int status) {
     case W4G128_ERR_CUDA: return "CUDA runtime or launch error";
     case W4G128_ERR_DEVICE: return "current device is not compute capability 10.3 (sm_103)";
     case W4G128_ERR_TIMEOUT: return "a bounded device-side wait timed out";
+    case W4G128_ERR_INTERNAL: return "a kernel found its launch inconsistent and skipped its work";
     default: return "unknown status";
   }
 }
@@ -140,6 +141,46 @@ size_t w4g128_decode_step_workspace_bytes(const w4g128_matrix* mats, int count, 
 
 int w4g128_decode_step(const w4g128_matrix* mats, int count, int M, void* ws, size_t ws_bytes, void* stream) {
   return run_stream(mats, count, M, ws, ws_bytes, stream);
+}
+
+int w4g128_decode_step_host(const w4g128_matrix* mats, int count, int M, const void* x_host, void* x_dev,
+                            size_t x_bytes, void* y_host, const void* y_dev, size_t y_bytes, void* ws,
+                            size_t ws_bytes, void* stream) {
+  if ((x_bytes > 0 && (x_host == nullptr || x_dev == nullptr)) ||
+      (y_bytes > 0 && (y_host == nullptr || y_dev == nullptr)))
+    return W4G128_ERR_INVALID_ARG;
+  int rc = check_stream_call(mats, count, M, ws);
+  if (rc != W4G128_OK) return rc;
+  rc = w4g128::fault_hook();
+  if (rc != W4G128_OK) return rc;
+  if (!w4g128::device_is_sm103()) return W4G128_ERR_DEVICE;
+  const cudaStream_t s = as_stream(stream);
+  // Pinned (device-mapped) host buffers move through small kernels that keep
+  // the chain of programmatic dependent launches; other memory through the
+  // copy engines.
+  if (x_bytes > 0) {
+    const void* xh = aligned(x_dev, 16) ? w4g128::mapped_host(x_host, x_bytes) : nullptr;
+    if (xh != nullptr) {
+      rc = w4g128::launch_upload(xh, x_dev, x_bytes, s);
+      if (rc != W4G128_OK) return rc;
+    } else if (cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+      cudaGetLastError();
+      return W4G128_ERR_CUDA;
+    }
+  }
+  rc = run_stream(mats, count, M, ws, ws_bytes, stream);
+  if (rc != W4G128_OK) return rc;
+  if (y_bytes > 0) {
+    const void* yh = aligned(y_dev, 16) ? w4g128::mapped_host(y_host, y_bytes) : nullptr;
+    if (yh != nullptr) {
+      rc = w4g128::launch_download(y_dev, const_cast<void*>(yh), y_bytes, s);
+      if (rc != W4G128_OK) return rc;
+    } else if (cudaMemcpyAsync(y_host, y_dev, y_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+      cudaGetLastError();
+      return W4G128_ERR_CUDA;
+    }
+  }
+  return W4G128_OK;
 }
 
 int w4g128_verify_step(const w4g128_matrix* mats, int count, int M, void* ws, size_t ws_bytes, void* stream) {

@@ -64,6 +64,16 @@ int launch_stream(const HostMatrix* mats, int count, int M, const NormArgs* norm
 
 int read_workspace_status(const void* ws, int* status_out, cudaStream_t stream);
 
+// Device address of a pinned, device-mapped host buffer (16-byte aligned,
+// `bytes` a multiple of 16), or nullptr when the GPU cannot reach it.
+const void* mapped_host(const void* host, size_t bytes);
+
+// Moves `bytes` (a multiple of 16, 16-byte aligned ends) between a mapped
+// host buffer and device memory with a small kernel launched as a
+// programmatic dependent of whatever precedes it on the stream.
+int launch_upload(const void* host_dev, void* dev, size_t bytes, cudaStream_t stream);
+int launch_download(const void* dev, void* host_dev, size_t bytes, cudaStream_t stream);
+
 // Current device is compute capability 10.3; caches per device.
 bool device_is_sm103();
 

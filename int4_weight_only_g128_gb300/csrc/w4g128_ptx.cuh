@@ -102,6 +102,18 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (this thread), cached in L2 only;
+// dst and src 16-byte aligned.  Completed by cp_async_wait_all.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Waits for every cp.async this thread issued (then a barrier makes them
+// visible to the CTA).
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // L2 policies: weight bytes are read exactly once (evict first); activation
 // packages are re-read by many warps (evict last).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {

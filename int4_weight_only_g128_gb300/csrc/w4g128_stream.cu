@@ -64,6 +64,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 #include <vector>
@@ -189,6 +190,9 @@ struct StreamParams {
   int per_warp_reduce;   // M >= 2: the split quads are folded per streaming warp (else per quad)
   int depth;             // ring slots per warp (ring_depth of the mode)
   unsigned long long wait_ns;  // limit of every device-side wait
+  int cta_warps;         // warps per streaming CTA
+  int local_pkg_off;     // M = 1 with CTA-local packages: shared-memory offsets of the package area
+  int local_part_off;    //   and of the partial-slot area
   MatParams mats[MAXMAT];
 };
 
@@ -889,31 +893,49 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
 // the group, or nullptr for a zero row (then the row is written as zeros);
 // dst == nullptr writes nothing.  Every lane of the warp must call it (it
 // shuffles).
-__device__ __forceinline__ void build_row_class(const uint16_t* xg, int c, int lane, uint8_t* dst, float* tail) {
-  uint32_t w[16];  // bf16 pairs in operand order
-  float X = 0.f;   // sum of this lane's 32 values
-  uint32_t amax = 0u;  // largest |x| among them, as bf16 magnitude bits
-  if (xg != nullptr) {
-    // x rows start 4-byte aligned (K even, x 4-byte aligned): one 32-bit
-    // load per operand pair, through L2: x may be the output of the kernel
-    // this one was launched behind, written while this CTA was resident
-    const uint32_t* xr = reinterpret_cast<const uint32_t*>(xg);
+// The 16 bf16 pairs of lane class c of one (group, x row), in operand order:
+// words 2i, 2i + 1 hold x[16i + 2c], x[16i + 2c + 1] and x[16i + 2c + 8],
+// x[16i + 2c + 9].  xg: the row's 128 values of the group, or nullptr for a
+// zero row.
+template <bool kSharedX = false>
+__device__ __forceinline__ void load_row_class(const uint16_t* xg, int c, uint32_t (&w)[16]) {
+  if (xg == nullptr) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 16; ++i) w[i] = 0u;
+    return;
+  }
+  // x rows start 4-byte aligned (K even, x 4-byte aligned): one 32-bit load
+  // per operand pair; from global memory through L2, since x may be the
+  // output of the kernel this one was launched behind
+  const uint32_t* xr = reinterpret_cast<const uint32_t*>(xg);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if constexpr (kSharedX) {  // x staged in this CTA's shared memory
+      w[2 * i] = xr[8 * i + c];
+      w[2 * i + 1] = xr[8 * i + c + 4];
+    } else {
       w[2 * i] = __ldcg(xr + 8 * i + c);
       w[2 * i + 1] = __ldcg(xr + 8 * i + c + 4);
     }
-    uint32_t mag2 = 0u;  // per-half maxima of |x| bits
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      X = (((X + bf16_lo(w[2 * i])) + bf16_hi(w[2 * i])) + bf16_lo(w[2 * i + 1])) + bf16_hi(w[2 * i + 1]);
-      mag2 = __vmaxu2(mag2, __vmaxu2(w[2 * i] & 0x7FFF7FFFu, w[2 * i + 1] & 0x7FFF7FFFu));
-    }
-    amax = max(mag2 & 0xFFFFu, mag2 >> 16);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) w[i] = 0u;
   }
+}
+
+// Lane class c of one (group, x row) package row from its loaded words, built
+// by four consecutive lanes (lane & ~3 .. + 3, one per class), which agree on
+// the row's scale 2^s from the largest magnitude among their 128 values:
+// x' = x 2^s as fp16 pairs in operand order go to dst + 80 c (64 bytes), and
+// lane c == 0 writes the row's (X_g, f), f = 2^-s, to tail[0..1].  dst ==
+// nullptr writes nothing.  Every lane of the warp must call it (it shuffles).
+__device__ __forceinline__ void finish_row_class(const uint32_t (&w)[16], int c, int lane, uint8_t* dst,
+                                                 float* tail) {
+  float X = 0.f;       // sum of this lane's 32 values
+  uint32_t mag2 = 0u;  // per-half maxima of |x| bits
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    X = (((X + bf16_lo(w[2 * i])) + bf16_hi(w[2 * i])) + bf16_lo(w[2 * i + 1])) + bf16_hi(w[2 * i + 1]);
+    mag2 = __vmaxu2(mag2, __vmaxu2(w[2 * i] & 0x7FFF7FFFu, w[2 * i + 1] & 0x7FFF7FFFu));
+  }
+  uint32_t amax = max(mag2 & 0xFFFFu, mag2 >> 16);  // largest |x| as bf16 magnitude bits
   amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
   amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
   // biased exponent e of the row's largest |x|: x 2^(141 - e) lies in
@@ -941,6 +963,13 @@ __device__ __forceinline__ void build_row_class(const uint16_t* xg, int c, int l
     tail[0] = ((X0 + X1) + X2) + X3;
     tail[1] = f;
   }
+}
+
+// load_row_class + finish_row_class (xg == nullptr: a zero row).
+__device__ __forceinline__ void build_row_class(const uint16_t* xg, int c, int lane, uint8_t* dst, float* tail) {
+  uint32_t w[16];
+  load_row_class(xg, c, w);
+  finish_row_class(w, c, lane, dst, tail);
 }
 
 // The prep kernels run on a 2-D grid, blockIdx.y = matrix, so no CTA
@@ -1016,6 +1045,490 @@ __global__ void __launch_bounds__(32) prep1_kernel(const __grid_constant__ Strea
     uint8_t* out = in ? m.xpkg + static_cast<long long>(g) * Pkg<MODE>::kBytes : nullptr;
     build_row_class(in ? m.x + kGroup * g : nullptr, c, lane, out, reinterpret_cast<float*>(out + Pkg<MODE>::kRowBytes));
   }
+}
+
+// ----------------------------------------------------------------- M = 1 with CTA-local packages
+
+// A call at M = 1 whose CTAs' working sets fit in shared memory runs without
+// the prep kernel ("local" calls):
+//  * each CTA stages, after its dependency wait, the groups of x its warps
+//    need (16-byte cp.async copies by every thread, at a 272-byte stride per
+//    group so that the lanes reading them hit distinct banks) and builds
+//    those groups' activation packages in its own shared memory, with exactly
+//    the prep kernel's arithmetic (load_row_class, finish_row_class), so
+//    every bit matches; the staging sits at the far end of the package area
+//    and is converted in place, pass by pass;
+//  * the ring slots carry weights only, and every slot is filled before the
+//    dependency wait;
+//  * a split quad whose segments all lie in this CTA's item range is folded
+//    from shared-memory partial slots at the CTA's end; a quad that begins in
+//    this CTA and continues in the next gets this CTA's left fold of its
+//    segments stored as one global slot; the segments of a quad that began in
+//    an earlier CTA go to global slots one by one; fold1_kernel, launched
+//    behind the streaming kernel, folds those boundary quads once every CTA
+//    has finished (one bulk copy pulls each quad's slots).  The fold order is
+//    the left fold over segments either way.
+// This removes a dependent kernel (prep -> stream) from every call.  Calls
+// whose CTAs would need more shared memory than is free (e.g. the whole
+// decode step of hundreds of matrices) or whose x is not 16-byte aligned take
+// the prep-kernel path.  (Folding the boundary quads inside the streaming
+// kernel instead, through tickets, was measured slower: the fence and the
+// atomic round trips behind every CTA's stream cost more than the fold
+// kernel's launch.)
+
+constexpr int kLocalMaxEntries = 8;                       // matrices one CTA's range may touch
+constexpr int kLocalSlot = kQuadTiles * kBlockBytes;      // ring slot: weights only (4352 bytes)
+constexpr int kLocalSlots = 2 * kNW;                      // ring slots per CTA: 2 per warp at 16 warps
+constexpr int kLocalBarBytes = 512;                       // ring mbarriers (32 x 8)
+constexpr int kLocalRing = kLocalSlots * kLocalSlot;      // slot d of warp w at (d * warps + w)
+constexpr int kLocalDyn = 232448 - 4096;                  // dynamic shared memory (static use stays below 4 KB)
+constexpr int kLocalSpace = kLocalDyn - kLocalBarBytes - kLocalRing;  // packages + partial slots
+constexpr int kPkg1 = Pkg<kMMA1>::kBytes;                 // one M = 1 package (336 bytes)
+constexpr int kStageStride = kGroup * 2 + 16;             // a staged group of x (272 bytes)
+constexpr int kMaxFoldSlots = 65536 / (kGroup * kSegGroups) + 1;  // slots of one boundary fold, at most
+constexpr int kFoldSmem = kMaxFoldSlots * 64 * 4 + 16;    // fold1_kernel: the slots and an mbarrier
+static_assert(kLocalSpace > 0 && kLocalRing % 128 == 0, "local layout");
+
+// The groups of matrix mi that a CTA's items touch, and where their packages
+// sit in the CTA's package area.
+struct LocalEntry {
+  int mi, g_lo, g_hi, pkg;
+};
+
+// Groups [g_lo, g_hi) needed by local items [lo, hi) of one matrix (S
+// segments per quad, G groups): the items' segments when they stay within
+// one quad, every group when they cross a quad boundary.
+__host__ __device__ inline void local_groups(long long lo, long long hi, int S, int G, int& g_lo, int& g_hi) {
+  const long long qa = lo / S, qb = (hi - 1) / S;
+  if (qa == qb) {
+    g_lo = static_cast<int>(lo - qa * S) * kSegGroups;
+    const int e = static_cast<int>(hi - 1 - qb * S) * kSegGroups + kSegGroups;
+    g_hi = e < G ? e : G;
+  } else {
+    g_lo = 0;
+    g_hi = G;
+  }
+}
+
+// The table of a CTA whose items are [A, B) (A < B): returns the number of
+// entries (-1 if more than kLocalMaxEntries) and the total package count.
+// `at` gives item_begin(i), K(i), N(i) of matrix i; the host and the device
+// build the same table from it.
+#pragma nv_exec_check_disable
+template <class MatAt>
+__host__ __device__ inline int local_table(long long A, long long B, int count, const MatAt& at, LocalEntry* t,
+                                           int& npkg) {
+  int lo = 0, hi = count - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (at.begin(mid) <= A) lo = mid; else hi = mid - 1;
+  }
+  int n = 0;
+  npkg = 0;
+  for (int mi = lo; mi < count && at.begin(mi) < B; ++mi) {
+    if (n == kLocalMaxEntries) return -1;
+    const int G = at.K(mi) / kGroup, S = div_up(G, kSegGroups), NQ = div_up(at.N(mi), kQuadTiles * kTileN);
+    const long long b0 = at.begin(mi), b1 = b0 + static_cast<long long>(NQ) * S;
+    const long long lo_it = (A > b0 ? A : b0) - b0, hi_it = (B < b1 ? B : b1) - b0;
+    LocalEntry& e = t[n++];
+    e.mi = mi;
+    local_groups(lo_it, hi_it, S, G, e.g_lo, e.g_hi);
+    e.pkg = npkg;
+    npkg += e.g_hi - e.g_lo;
+  }
+  return n;
+}
+
+template <int MAXMAT>
+struct DevMats {
+  const StreamParams<MAXMAT>& p;
+  __device__ long long begin(int i) const { return mat(p, i).item_begin; }
+  __device__ int K(int i) const { return mat(p, i).K; }
+  __device__ int N(int i) const { return mat(p, i).N; }
+};
+
+// The status word of a local call is 64 bits: the code in bits 0..7 (what
+// w4g128_workspace_status reports) and, above it, a tag of the streaming
+// grid that wrote it.  A call clears the word when it starts (CTA 0, after
+// its dependency wait) and records a failure at any time; both are
+// compare-and-swap loops on the tag, so a failure recorded by another CTA of
+// the same grid before the clear survives it, and a stale or uninitialised
+// word is replaced.  (Replays of one CUDA graph node share their %gridid and
+// so their tag: a failure of one replay stays reported by the next.)
+__device__ __forceinline__ unsigned long long grid_tag() {
+  unsigned long long g;
+  asm volatile("mov.u64 %0, %%gridid;" : "=l"(g));
+  // a multiplicative hash (odd constant: a bijection), so that small launch
+  // numbers do not look like words with zero upper bytes
+  return ((g + 1ull) * 0x9E3779B97F4A7C15ull) >> 8;
+}
+
+__device__ __forceinline__ void status_begin(unsigned* status) {
+  auto* st = reinterpret_cast<unsigned long long*>(status);
+  const unsigned long long tag = grid_tag();
+  unsigned long long cur = ld_relaxed_u64(st);
+  while ((cur >> 8) != tag) {
+    const unsigned long long prev = atomicCAS(st, cur, tag << 8);
+    if (prev == cur) return;
+    cur = prev;
+  }
+}
+
+__device__ __forceinline__ void status_fail(unsigned* status, unsigned code) {
+  auto* st = reinterpret_cast<unsigned long long*>(status);
+  const unsigned long long tag = grid_tag();
+  unsigned long long cur = ld_relaxed_u64(st);
+  while (!((cur >> 8) == tag && (cur & 0xFFull) != 0ull)) {
+    const unsigned long long prev = atomicCAS(st, cur, (tag << 8) | code);
+    if (prev == cur) return;
+    cur = prev;
+  }
+}
+
+// A fold the CTA does at its end: slots [first, first + nslot) of its
+// shared-memory partial area (indices relative to its first item), written
+// to y (a quad inside the CTA's range) or, for the quad that continues into
+// the next CTA, stored as one global partial slot.
+struct LocalFold {
+  long long first;  // first slot (CTA item index)
+  uint16_t* y;      // the quad's first output column (internal), or nullptr
+  float* gslot;     // the global slot for the CTA's prefix fold (boundary), or nullptr
+  int nslot;
+  int cols;
+  int n0;
+  int pad;
+};
+
+// 120 registers (no spills), as the prep-kernel M = 1 path: 512 threads fit,
+// with registers left for fold1_kernel's small CTAs beside them.
+template <int MAXMAT, bool NORM>
+__global__ void __maxnreg__(120) stream1_local_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int NA = Acc<kMMA1>::kN;
+  __shared__ LocalEntry tbl[kLocalMaxEntries];
+  __shared__ int tbl_n, tbl_npkg;
+  __shared__ int fold_n;
+  __shared__ LocalFold folds[2 * kNW];
+  __shared__ int fold_fail;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = lane >> 2, c = lane & 3;
+  const int cw = blockDim.x >> 5;
+  // a CTA's 32 ring slots are shared out among its warps: 2 each at 16 warps,
+  // up to 8 each in smaller CTAs, whose warps then keep more bytes in flight
+  const int D = p.depth;
+  const int wg = blockIdx.x * cw + warp;
+  const long long I = p.total_items;
+  const int wl = min((static_cast<int>(blockIdx.x) + 1) * cw, p.W);
+  const long long A = I * (static_cast<long long>(blockIdx.x) * cw) / p.W;
+  const long long B = I * wl / p.W;
+  const uint32_t bars = smem_addr(smem);
+  const uint32_t ring0 = bars + kLocalBarBytes;
+  uint8_t* const pkg_area = smem + p.local_pkg_off;
+  float* const part_area = reinterpret_cast<float*>(smem + p.local_part_off);
+
+  if (threadIdx.x == 0) {
+    fold_n = 0;
+    fold_fail = 0;
+    int np = 0;
+    tbl_n = local_table(A, B, p.count, DevMats<MAXMAT>{p}, tbl, np);
+    tbl_npkg = np;
+  }
+  if (lane == 0) {
+    for (int d = 0; d < D; ++d) mbar_init(bars + 8 * (warp * D + d), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // The host launches this kernel only for M = 1 calls whose every CTA fits
+  // (the same table function); a CTA that does not fit records the error and
+  // touches nothing.
+  if (tbl_n <= 0 || p.M != 1 || p.local_pkg_off != kLocalBarBytes + kLocalRing || D < 2 || D * cw > kLocalSlots ||
+      p.local_pkg_off + static_cast<long long>(tbl_npkg) * kPkg1 > p.local_part_off ||
+      p.local_part_off + (B - A) * 64 * 4 > kLocalDyn) {
+    if (threadIdx.x == 0) status_fail(p.status, W4G128_ERR_INTERNAL);
+    return;
+  }
+  const int mi_a = tbl[0].mi;
+  const int npkg = tbl_npkg;
+  // x of the CTA's package t is staged at stage + t * kStageStride, at the far
+  // end of the package area (package t is built at pkg_area + t * kPkg1)
+  uint8_t* const stage = pkg_area + static_cast<long long>(npkg) * (kPkg1 - kStageStride);
+  // package of (matrix mi, group g) in the CTA's package area
+  auto local_pkg = [&](int mi, int g) -> const uint8_t* {
+    const LocalEntry& e = tbl[mi - mi_a];
+    return pkg_area + static_cast<long long>(e.pkg + g - e.g_lo) * kPkg1;
+  };
+
+  const long long it_a = I * wg / p.W, it_b = I * (wg + 1) / p.W;
+  const bool streams = wg < p.W;
+  uint64_t pol_w = 0;
+  Cursor cc, ic;
+  unsigned issued = 0u;
+  if (streams) {
+    if (lane == 0) pol_w = l2_policy_evict_first();
+    cursor_seek<kMMA1>(cc, p, it_a);
+    ic = cc;
+    // the weights do not depend on earlier work: fill the ring now
+    while (issued < static_cast<unsigned>(D) && ic.item < it_b) {
+      if (lane == 0) {
+        const uint32_t sa = ring0 + (issued * cw + warp) * kLocalSlot, ba = bars + 8 * (warp * D + issued);
+        mbar_arrive_expect_tx(ba, ic.ntiles * kBlockBytes);
+        bulk_g2s(sa, ic.src, ic.ntiles * kBlockBytes, ba, pol_w);
+      }
+      cursor_next<kMMA1>(ic, p);
+      ++issued;
+    }
+  }
+  grid_dependency_wait();  // the previous kernel has finished: x is final, the workspace free
+  grid_dependents_launch();  // the boundary fold may launch; it waits for this grid
+
+  // ---- stage x (16-byte cp.async copies by every thread), then build the packages
+  for (int idx = threadIdx.x; idx < npkg * 16; idx += blockDim.x) {
+    const int t = idx >> 4, part = idx & 15;
+    int e = 0;
+    while (e + 1 < tbl_n && tbl[e + 1].pkg <= t) ++e;
+    const int g = tbl[e].g_lo + (t - tbl[e].pkg);
+    cp_async16(smem_addr(stage + t * kStageStride + part * 16),
+               mat(p, tbl[e].mi).x + static_cast<long long>(g) * kGroup + part * 8);
+  }
+  cp_async_wait_all();
+  // the status word is cleared by a thread of the second warp (thread 0 of a
+  // one-warp CTA)
+  if (blockIdx.x == 0 && threadIdx.x == (blockDim.x > 32 ? 32u : 0u)) status_begin(p.status);
+  __syncthreads();  // x staged
+  {
+    // lanes (j, c): lane class c of package base + j, eight packages per warp
+    // per pass; each pass reads its staged groups into registers, then (after
+    // a barrier) overwrites the bytes below the next pass's staging
+    const int npass = div_up(npkg, 8 * cw);
+    for (int ps = 0; ps < npass; ++ps) {
+      const int t = ps * 8 * cw + 8 * warp + (lane >> 2);
+      const bool in = t < npkg;
+      uint32_t wx[16];
+      load_row_class<true>(in ? reinterpret_cast<const uint16_t*>(stage + t * kStageStride) : nullptr, c, wx);
+      __syncthreads();
+      uint8_t* out = in ? pkg_area + static_cast<long long>(t) * kPkg1 : nullptr;
+      finish_row_class(wx, c, lane, out, reinterpret_cast<float*>(out + Pkg<kMMA1>::kRowBytes));
+    }
+  }
+  __syncthreads();  // packages written
+
+  bool failed = false;
+  float seg[kQuadTiles][NA], tot[kQuadTiles][NA];
+  int n_pend = 0;
+  if (streams) {
+    cc.xsrc = local_pkg(cc.mi, cc.g);
+#pragma unroll
+    for (int t = 0; t < kQuadTiles; ++t)
+#pragma unroll
+      for (int e = 0; e < NA; ++e) seg[t][e] = tot[t][e] = 0.f;
+
+    unsigned done = 0;
+    int slot = 0;
+    uint32_t parity = 0u;
+    while (cc.item < it_b) {
+      if (!mbar_wait_bounded(bars + 8 * (warp * D + slot), parity, p.wait_ns)) {
+        if (lane == 0) {
+          status_fail(p.status, W4G128_ERR_TIMEOUT);
+          for (unsigned k = done + 1; k < issued; ++k)
+            (void)mbar_wait_bounded(bars + 8 * (warp * D + static_cast<int>(k % D)), (k / D) & 1u, p.wait_ns);
+        }
+        __syncwarp();
+        failed = true;
+        break;
+      }
+      const int ntiles = cc.ntiles;
+      const uint8_t* sl = smem + kLocalBarBytes + (slot * cw + warp) * kLocalSlot;
+      compute_chunk<kMMA1>(sl, cc.xsrc, ntiles, lane, seg);
+      __syncwarp();
+      if (ic.item < it_b) {
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          const uint32_t sa = ring0 + (slot * cw + warp) * kLocalSlot, ba = bars + 8 * (warp * D + slot);
+          mbar_arrive_expect_tx(ba, ic.ntiles * kBlockBytes);
+          bulk_g2s(sa, ic.src, ic.ntiles * kBlockBytes, ba, pol_w);
+        }
+        cursor_next<kMMA1>(ic, p);
+        ++issued;
+      }
+      ++done;
+      if (++slot == D) {
+        slot = 0;
+        parity ^= 1u;
+      }
+
+      if (cc.g + 1 == cc.g_end) {
+        // ---- end of a segment
+        const MatParams& m = mat(p, cc.mi);
+        const int S = cc.S;
+        const long long q_first = m.item_begin + static_cast<long long>(cc.q) * S;
+        const long long q_last = q_first + S - 1;
+        const bool owned = (q_first >= it_a) && (q_last < it_b);
+        const bool prefix = (q_first >= it_a) && !owned;
+        if (owned || prefix) {
+#pragma unroll
+          for (int t = 0; t < kQuadTiles; ++t)
+#pragma unroll
+            for (int e = 0; e < NA; ++e) tot[t][e] = (cc.s == 0) ? seg[t][e] : tot[t][e] + seg[t][e];
+        }
+        if (!owned && (!prefix || cc.item + 1 == it_b)) {
+          // a quad that began before this CTA: the segment sum goes to its
+          // global slot for the boundary fold; otherwise to this CTA's slot
+          float* part = (q_first < A) ? p.partials + cc.item * 64 : part_area + (cc.item - A) * 64;
+          if (c == 0) {
+#pragma unroll
+            for (int t = 0; t < kQuadTiles; ++t) {
+              if (t < ntiles) {
+                part[16 * t + r] = prefix ? tot[t][0] : seg[t][0];
+                part[16 * t + r + 8] = prefix ? tot[t][1] : seg[t][1];
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < kQuadTiles; ++t)
+#pragma unroll
+          for (int e = 0; e < NA; ++e) seg[t][e] = 0.f;
+
+        const bool quad_end = (cc.s == S - 1) || (cc.item + 1 == it_b);
+        if (quad_end) {
+          const int n0 = kQuadTiles * kTileN * cc.q;
+          if (owned) {
+            if (c == 0) {
+#pragma unroll
+              for (int t = 0; t < kQuadTiles; ++t) {
+                if (t < ntiles) {
+                  const int n = n0 + 16 * t + r;
+                  m.y[n] = emit<NORM>(p, n, tot[t][0]);
+                  m.y[n + 8] = emit<NORM>(p, n + 8, tot[t][1]);
+                }
+              }
+            }
+          } else if (q_first >= A && n_pend < 2 && (cc.s == S - 1 || (q_last >= B && cc.item + 1 == B))) {
+            // this warp holds the last segment of a quad inside the CTA's
+            // range (fold it to y), or the CTA's last item inside a quad that
+            // continues in the next CTA (fold the CTA's share to one global slot)
+            if (lane == 0) {
+              const long long first = I * (owner_of(q_first, I, p.W) + 1) / p.W - 1;
+              LocalFold& f = folds[atomicAdd(&fold_n, 1)];
+              const bool inner = cc.s == S - 1;
+              f.first = first - A;
+              f.nslot = static_cast<int>((inner ? q_last : B - 1) + 1 - first);
+              f.y = inner ? m.y + n0 : nullptr;
+              f.gslot = inner ? nullptr : p.partials + (B - 1) * 64;
+              f.cols = kTileN * ntiles;
+              f.n0 = n0;
+            }
+            ++n_pend;
+          }
+        }
+      }
+      cursor_next<kMMA1>(cc, p);
+      if (cc.g == 0 && cc.item < it_b) cc.xsrc = local_pkg(cc.mi, 0);
+    }
+    if (failed && lane == 0) atomicOr(&fold_fail, 1);
+  }
+  __syncthreads();  // every warp's slots are written
+  if (fold_fail) return;  // a timed-out warp left its quads unreduced (the status word says so)
+
+  // ---- the CTA's folds: one thread per (fold, 4 columns), slots in order
+  const int nunit = fold_n * 16;
+  for (int idx = threadIdx.x; idx < nunit; idx += blockDim.x) {
+    const LocalFold& f = folds[idx >> 4];
+    const int col = 4 * (idx & 15);
+    if (col >= f.cols) continue;
+    const float4* part = reinterpret_cast<const float4*>(part_area + f.first * 64 + col);
+    uint32_t r0 = 0u, r1 = 0u;
+    if (f.y != nullptr) {
+      r0 = residual2<NORM>(p, f.n0 + col);
+      r1 = residual2<NORM>(p, f.n0 + col + 2);
+    }
+    float4 acc = part[0];
+    for (int k = 1; k < f.nslot; ++k) {
+      const float4 v = part[static_cast<long long>(k) * 16];
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    if (f.y != nullptr) {
+      uint32_t* yo = reinterpret_cast<uint32_t*>(f.y + col);
+      yo[0] = emit2<NORM>(acc.x, acc.y, r0);
+      yo[1] = emit2<NORM>(acc.z, acc.w, r1);
+    } else {
+      *reinterpret_cast<float4*>(f.gslot + col) = acc;
+    }
+  }
+}
+
+// The boundary quads of a local call: for each boundary cb between streaming
+// CTAs cb - 1 and cb whose first item lies inside a quad that began in CTA
+// cb - 1, fold that quad's slots -- CTA cb - 1's fold of its share, then the
+// later segments one by one, a contiguous run -- once the streaming grid has
+// finished.  A quad spanning more CTAs is folded at its first boundary only.
+// One 32-thread CTA per boundary: lane 0 pulls the run into shared memory
+// with one bulk copy, lanes 0..15 fold one 4-column unit each.
+template <int MAXMAT, bool NORM>
+__global__ void __launch_bounds__(32) fold1_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
+  extern __shared__ __align__(128) uint8_t fsm[];
+  // the next kernel may launch now; it waits for this grid, which does not
+  // finish before the streaming grid (the last CTA always waits for it)
+  grid_dependents_launch();
+  const int cb = blockIdx.x + 1;
+  const long long I = p.total_items;
+  const long long Ac = I * (static_cast<long long>(cb) * p.cta_warps) / p.W;
+  const long long Ap = I * (static_cast<long long>(cb - 1) * p.cta_warps) / p.W;
+  int lo = 0;
+  if constexpr (MAXMAT > 1) {
+    int hi = p.count - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.mats[mid].item_begin <= Ac) lo = mid; else hi = mid - 1;
+    }
+  }
+  const MatParams& m = mat(p, lo);
+  const int S = div_up(m.K / kGroup, kSegGroups);
+  const long long local = Ac - m.item_begin;
+  const int q = static_cast<int>(local / S);
+  const int s = static_cast<int>(local - static_cast<long long>(q) * S);
+  if (Ac >= I || s == 0 || Ac - s < Ap) {  // no quad begins in CTA cb - 1 and continues here
+    if (blockIdx.x + 1 == gridDim.x) grid_dependency_wait();
+    return;
+  }
+  const int nslot = S - s + 1;  // CTA cb - 1's slot (item Ac - 1), then segments s .. S - 1
+  const int cols = kTileN * min(kQuadTiles, m.N / kTileN - kQuadTiles * q);
+  const int col = 4 * threadIdx.x;
+  const bool active = col < cols && threadIdx.x < 16;
+  const int n = kQuadTiles * kTileN * q + col;
+  uint32_t r0 = 0u, r1 = 0u;
+  if (active) {
+    r0 = residual2<NORM>(p, n);
+    r1 = residual2<NORM>(p, n + 2);
+  }
+  uint16_t* y = m.y;
+  const uint32_t bar = smem_addr(fsm + kMaxFoldSlots * 64 * 4);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  grid_dependency_wait();  // every slot of the streaming grid is written and visible
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nslot) * 256u);
+    bulk_g2s(smem_addr(fsm), p.partials + (Ac - 1) * 64, static_cast<uint32_t>(nslot) * 256u, bar,
+             l2_policy_evict_first());
+  }
+  if (!mbar_wait_bounded(bar, 0u, p.wait_ns)) {
+    if (threadIdx.x == 0) status_fail(p.status, W4G128_ERR_TIMEOUT);
+    return;
+  }
+  if (!active) return;
+  const float4* part = reinterpret_cast<const float4*>(fsm) + threadIdx.x;
+  float4 acc = part[0];
+  for (int k = 1; k < nslot; ++k) {
+    const float4 v = part[k * 16];
+    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+  }
+  uint32_t* yo = reinterpret_cast<uint32_t*>(y + n);
+  yo[0] = emit2<NORM>(acc.x, acc.y, r0);
+  yo[1] = emit2<NORM>(acc.z, acc.w, r1);
 }
 
 // ----------------------------------------------------------------- reduce kernel
@@ -1264,7 +1777,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __grid_cons
   // The next call's prep kernel may launch now; it waits for this grid.
   grid_dependents_launch();
   grid_dependency_wait();
-  if (*reinterpret_cast<volatile unsigned*>(p.status) != 0u) return;  // the product failed: out left unwritten
+  if ((*reinterpret_cast<volatile unsigned*>(p.status) & 0xFFu) != 0u) return;  // the product failed: out left unwritten
   const MatParams& m = p.mats[0];
   const int row = blockIdx.y, j0 = blockIdx.x * kNormSlice, t = threadIdx.x;
   const int npairs = m.N >> 1, nchunk = npairs >> 2;
@@ -1319,7 +1832,21 @@ struct DeviceInfo {
 
 std::mutex g_mu;
 DeviceInfo g_dev[64];
-bool g_dev_init[64] = {false};
+std::atomic<bool> g_dev_init[64];  // set once g_dev[i] is filled (released under g_mu)
+
+void setup_local() {
+  cudaFuncSetAttribute(fold1_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFoldSmem);
+  cudaFuncSetAttribute(fold1_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFoldSmem);
+  cudaFuncSetAttribute(fold1_kernel<kFewMatrices, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFoldSmem);
+  cudaFuncSetAttribute(fold1_kernel<W4G128_MAX_MATRICES, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       kFoldSmem);
+  cudaFuncSetAttribute(stream1_local_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalDyn);
+  cudaFuncSetAttribute(stream1_local_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalDyn);
+  cudaFuncSetAttribute(stream1_local_kernel<kFewMatrices, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       kLocalDyn);
+  cudaFuncSetAttribute(stream1_local_kernel<W4G128_MAX_MATRICES, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       kLocalDyn);
+}
 
 template <int MODE>
 void setup_mode(DeviceInfo& d) {
@@ -1352,8 +1879,9 @@ const DeviceInfo* device_info() {
     cudaGetLastError();
     return nullptr;
   }
+  if (g_dev_init[dev].load(std::memory_order_acquire)) return &g_dev[dev];  // the per-call path
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_dev_init[dev]) {
+  if (!g_dev_init[dev].load(std::memory_order_relaxed)) {
     DeviceInfo d;
     int major = 0, minor = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
@@ -1364,6 +1892,7 @@ const DeviceInfo* device_info() {
       setup_mode<kMMA>(d);
       setup_mode<kMMA1>(d);
       setup_mode<kMMA16>(d);
+      setup_local();
       for (int M = 2; M <= kMaxRows; ++M) {
         int n = 0;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, reduce_quads_kernel<W4G128_MAX_MATRICES, false>,
@@ -1373,7 +1902,7 @@ const DeviceInfo* device_info() {
       if (cudaGetLastError() != cudaSuccess) d.ok = false;
     }
     g_dev[dev] = d;
-    g_dev_init[dev] = true;
+    g_dev_init[dev].store(true, std::memory_order_release);
   }
   return &g_dev[dev];
 }
@@ -1386,12 +1915,15 @@ void forget_device() {
     return;
   }
   std::lock_guard<std::mutex> lock(g_mu);
-  g_dev_init[dev] = false;
+  g_dev_init[dev].store(false, std::memory_order_release);
 }
 
 struct Plan {
   int mode = 0, rows = 1, pkg = 0, depth = 2;
   bool per_warp_reduce = false;
+  bool local = false;   // M = 1 with CTA-local packages (when x is 16-byte aligned)
+  int local_depth = 2;  // ring slots per warp of a local call
+  int local_pkg_off = 0, local_part_off = 0;
   long long items = 0;
   int W = 0, grid = 0, cta_warps = kNW, total_quads = 0, total_groups = 0, max_groups = 0;
   size_t off_tickets = 0, off_recs = 0, off_xpkg = 0, off_partials = 0, bytes = 0;
@@ -1402,6 +1934,7 @@ struct Plan {
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool make_plan(const HostMatrix* mats, int count, int M, const DeviceInfo& dev, Plan& pl) {
+  pl = Plan();  // cached plans are reused: start from the defaults
   pl.mode = (M > 8) ? kMMA16 : (M > 1) ? kMMA : kMMA1;
   pl.rows = M;
   pl.pkg = (pl.mode == kMMA16) ? Pkg<kMMA16>::kBytes : (pl.mode == kMMA) ? Pkg<kMMA>::kBytes : Pkg<kMMA1>::kBytes;
@@ -1429,7 +1962,13 @@ bool make_plan(const HostMatrix* mats, int count, int M, const DeviceInfo& dev, 
   pl.total_groups = static_cast<int>(groups);
   const int nw = (pl.mode == kMMA16) ? cta_warps_max<kMMA16>() : kNW;
   const long long max_warps = static_cast<long long>(dev.sms) * dev.occ[pl.mode] * nw;
-  pl.W = static_cast<int>(std::min<long long>(items, max_warps));
+  // Warps: as many as the grid holds, but with a whole number of items each
+  // when a warp gets only a few: the warps of a call finish together instead
+  // of some streaming one item more than the rest (2720 items on 2432 warps
+  // would give most warps one item and some two).  The summation order
+  // depends on the segments alone, so the schedule changes no bit.
+  const long long per = (items + max_warps - 1) / max_warps;  // items per warp, at least
+  pl.W = static_cast<int>(per < 4 ? (items + per - 1) / per : std::min<long long>(items, max_warps));
   // Spread the warps over every SM: a call with fewer items than the grid
   // holds warps gets smaller CTAs rather than fewer SMs.
   pl.cta_warps = std::min(nw, div_up(pl.W, dev.sms));
@@ -1439,6 +1978,34 @@ bool make_plan(const HostMatrix* mats, int count, int M, const DeviceInfo& dev, 
   // each and than one wave of resident reduce CTAs
   pl.per_warp_reduce = M >= 2 && pl.total_quads > pl.W &&
                        static_cast<long long>(pl.total_quads) > static_cast<long long>(dev.red_occ[M]) * dev.sms;
+
+  // M = 1: can every CTA hold its packages and partial slots in shared memory?
+  if (pl.mode == kMMA1) {
+    struct HostMats {
+      const Plan& pl;
+      const HostMatrix* m;
+      long long begin(int i) const { return pl.item_begin[i]; }
+      int K(int i) const { return m[i].K; }
+      int N(int i) const { return m[i].N; }
+    } at{pl, mats};
+    int pmax = 0;
+    long long smax = 0;
+    bool ok = true;
+    for (int c = 0; c < pl.grid && ok; ++c) {
+      const long long A = items * (static_cast<long long>(c) * pl.cta_warps) / pl.W;
+      const long long B = items * std::min((c + 1) * pl.cta_warps, pl.W) / pl.W;
+      LocalEntry t[kLocalMaxEntries];
+      int np = 0;
+      if (local_table(A, B, count, at, t, np) < 0) ok = false;
+      pmax = std::max(pmax, np);
+      smax = std::max(smax, B - A);
+    }
+    ok = ok && static_cast<long long>(pmax) * kPkg1 + smax * 64 * 4 <= kLocalSpace;
+    pl.local = ok;
+    pl.local_depth = std::min(8, kLocalSlots / pl.cta_warps);
+    pl.local_pkg_off = kLocalBarBytes + kLocalRing;
+    pl.local_part_off = pl.local_pkg_off + pmax * kPkg1;
+  }
 
   pl.off_tickets = 256;  // after the status word
   pl.off_recs = align_up(pl.off_tickets + sizeof(unsigned) * static_cast<size_t>(quads), 256);
@@ -1467,6 +2034,9 @@ void fill_params(StreamParams<MAXMAT>& sp, const HostMatrix* mats, int count, in
   sp.per_warp_reduce = pl.per_warp_reduce ? 1 : 0;
   sp.depth = pl.depth;
   sp.wait_ns = kDefaultWaitNs;
+  sp.cta_warps = pl.cta_warps;
+  sp.local_pkg_off = pl.local_pkg_off;
+  sp.local_part_off = pl.local_part_off;
   sp.total_quads = pl.total_quads;
   sp.total_groups = pl.total_groups;
   for (int i = 0; i < count; ++i) {
@@ -1481,6 +2051,47 @@ void fill_params(StreamParams<MAXMAT>& sp, const HostMatrix* mats, int count, in
     m.quad_begin = pl.quad_begin[i];
     m.g_begin = pl.g_begin[i];
   }
+}
+
+// M = 1 with CTA-local packages: the streaming kernel (a programmatic
+// dependent of whatever precedes it), the boundary fold behind it when there
+// is more than one CTA, and the norm behind that.
+template <int MAXMAT, bool NORM>
+int launch_local(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(cta_warps * 32);
+  cfg.dynamicSmemBytes = kLocalDyn;
+  if (cudaLaunchKernelEx(&cfg, stream1_local_kernel<MAXMAT, NORM>, sp) != cudaSuccess) {
+    cudaGetLastError();
+    return W4G128_ERR_CUDA;
+  }
+  if (grid > 1) {
+    cfg.gridDim = dim3(grid - 1);
+    cfg.blockDim = dim3(32);
+    cfg.dynamicSmemBytes = kFoldSmem;
+    if (cudaLaunchKernelEx(&cfg, fold1_kernel<MAXMAT, NORM>, sp) != cudaSuccess) {
+      cudaGetLastError();
+      return W4G128_ERR_CUDA;
+    }
+  }
+  if constexpr (NORM) {
+    const int nchunk = sp.mats[0].N / 8;
+    cfg.gridDim = dim3(static_cast<unsigned>(div_up(nchunk, kNormSlice)), static_cast<unsigned>(sp.M));
+    cfg.blockDim = dim3(kNormThreads);
+    cfg.dynamicSmemBytes = 0;
+    if (cudaLaunchKernelEx(&cfg, rmsnorm_kernel, sp) != cudaSuccess) {
+      cudaGetLastError();
+      return W4G128_ERR_CUDA;
+    }
+  }
+  return W4G128_OK;
 }
 
 template <int MODE, int MAXMAT, bool NORM>
@@ -1552,11 +2163,25 @@ int launch_mode(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, int max
   return W4G128_OK;
 }
 
+// Local calls stage x with bulk copies, which need 16-byte aligned sources.
+bool x_aligned(const HostMatrix* mats, int count) {
+  for (int i = 0; i < count; ++i)
+    if ((reinterpret_cast<uintptr_t>(mats[i].x) & 15u) != 0u) return false;
+  return true;
+}
+
 template <int MAXMAT>
 int launch_with(const HostMatrix* mats, int count, int M, const Plan& pl, const NormArgs* norm, void* ws,
                 cudaStream_t stream) {
   static thread_local StreamParams<MAXMAT> sp;  // large for MAXMAT = 512: keep it off the stack
   fill_params(sp, mats, count, M, pl, norm, ws);
+  if (pl.local && x_aligned(mats, count)) {
+    sp.depth = pl.local_depth;
+    if constexpr (MAXMAT == 1) {
+      if (norm != nullptr) return launch_local<1, true>(sp, pl.grid, pl.cta_warps, stream);
+    }
+    return launch_local<MAXMAT, false>(sp, pl.grid, pl.cta_warps, stream);
+  }
   if constexpr (MAXMAT == 1) {
     if (norm != nullptr) {
       if (pl.mode == kMMA16) return launch_mode<kMMA16, 1, true>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
@@ -1570,6 +2195,47 @@ int launch_with(const HostMatrix* mats, int count, int M, const Plan& pl, const 
   return launch_mode<kMMA1, MAXMAT, false>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
 }
 
+// The last few plans of this host thread, keyed by device, M and the list of
+// shapes: a decode loop repeats the same calls, and a plan (the schedule, the
+// workspace layout, the per-CTA check of the local mode) depends on nothing
+// else.
+struct PlanCache {
+  static constexpr int kEntries = 8;
+  struct Entry {
+    int dev = -1, M = 0;
+    std::vector<int> shapes;  // K0, N0, K1, N1, ...
+    Plan plan;
+  } e[kEntries];
+  int next = 0;
+};
+
+const Plan* cached_plan(const HostMatrix* mats, int count, int M, const DeviceInfo& info) {
+  static thread_local PlanCache cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  for (auto& en : cache.e) {
+    if (en.dev != dev || en.M != M || static_cast<int>(en.shapes.size()) != 2 * count) continue;
+    bool same = true;
+    for (int i = 0; i < count && same; ++i) same = en.shapes[2 * i] == mats[i].K && en.shapes[2 * i + 1] == mats[i].N;
+    if (same) return &en.plan;
+  }
+  auto& en = cache.e[cache.next];
+  cache.next = (cache.next + 1) % PlanCache::kEntries;
+  en.dev = -1;
+  if (!make_plan(mats, count, M, info, en.plan)) return nullptr;
+  en.shapes.resize(2 * count);
+  for (int i = 0; i < count; ++i) {
+    en.shapes[2 * i] = mats[i].K;
+    en.shapes[2 * i + 1] = mats[i].N;
+  }
+  en.dev = dev;
+  en.M = M;
+  return &en.plan;
+}
+
 }  // namespace
 
 bool device_is_sm103() {
@@ -1580,17 +2246,17 @@ bool device_is_sm103() {
 size_t stream_workspace_bytes(const HostMatrix* mats, int count, int M) {
   const DeviceInfo* d = device_info();
   if (d == nullptr || !d->ok) return 0;
-  Plan pl;
-  if (!make_plan(mats, count, M, *d, pl)) return 0;
-  return pl.bytes;
+  const Plan* pl = cached_plan(mats, count, M, *d);
+  return pl == nullptr ? 0 : pl->bytes;
 }
 
 int launch_stream(const HostMatrix* mats, int count, int M, const NormArgs* norm, void* ws,
                   size_t ws_bytes, cudaStream_t stream) {
   const DeviceInfo* d = device_info();
   if (d == nullptr || !d->ok) return W4G128_ERR_DEVICE;
-  Plan pl;
-  if (!make_plan(mats, count, M, *d, pl)) return W4G128_ERR_SHAPE;
+  const Plan* cached = cached_plan(mats, count, M, *d);
+  if (cached == nullptr) return W4G128_ERR_SHAPE;
+  const Plan& pl = *cached;
   if (ws_bytes < pl.bytes) return W4G128_ERR_WORKSPACE;
   if (norm != nullptr && count != 1) return W4G128_ERR_INVALID_ARG;
   int rc;
@@ -1607,7 +2273,7 @@ int read_workspace_status(const void* ws, int* status_out, cudaStream_t stream) 
   unsigned v = 0;
   if (cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return W4G128_ERR_CUDA;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return W4G128_ERR_CUDA;
-  *status_out = static_cast<int>(v);
+  *status_out = static_cast<int>(v & 0xFFu);  // the code byte (local calls tag the rest)
   return W4G128_OK;
 }
 

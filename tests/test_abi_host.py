@@ -17,7 +17,7 @@ def L():
 
 def test_every_header_symbol_is_exported(L):
     names = w.exported_symbols()
-    assert len(names) == 19
+    assert len(names) == 20
     for n in names:
         assert hasattr(L, n), n
 
@@ -34,7 +34,7 @@ def test_packed_bytes_exact():
 
 
 def test_status_strings():
-    for s in range(8):
+    for s in range(9):
         assert isinstance(w.w4g128_status_string(s), str) and w.w4g128_status_string(s)
     assert "unknown" in w.w4g128_status_string(99)
 
@@ -179,3 +179,13 @@ def test_host_fault_hook(mode, status):
     codes = [int(v) for v in out.stdout.split()]
     assert codes[:-1] == [status] * 7
     assert codes[-1] == E_SHAPE
+
+
+def test_decode_step_host_argument_errors(L):
+    mats = (w._Matrix * 1)()
+    mats[0] = w._Matrix(FAKE, FAKE, FAKE, 128, 16)
+    assert L.w4g128_decode_step_host(mats, 1, 1, None, FAKE, 16, FAKE, FAKE, 16, FAKE, 1 << 20, None) == E_INVALID
+    assert L.w4g128_decode_step_host(mats, 1, 1, FAKE, FAKE, 16, FAKE, None, 16, FAKE, 1 << 20, None) == E_INVALID
+    assert L.w4g128_decode_step_host(mats, 0, 1, FAKE, FAKE, 16, FAKE, FAKE, 16, FAKE, 1 << 20, None) == E_INVALID
+    mats[0] = w._Matrix(FAKE, FAKE, FAKE, 128, 24)
+    assert L.w4g128_decode_step_host(mats, 1, 1, FAKE, FAKE, 16, FAKE, FAKE, 16, FAKE, 1 << 20, None) == E_SHAPE

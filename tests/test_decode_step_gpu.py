@@ -100,3 +100,41 @@ def test_full_decode_step_every_output(M):
     for i, (K, N) in enumerate(shapes):
         c, s, mn = canonical_from_device(K, N, 10000 + i)
         check_against_oracle(ys[i], xh[i], c, s, mn)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("M", [1, 8])
+def test_decode_step_host_buffers(M, pinned):
+    """w4g128_decode_step_host: x moved in from host memory, the matrices
+    streamed, y moved back -- one call (pinned buffers through the library's
+    upload and download kernels, pageable ones through copy-engine copies);
+    y equals w4g128_decode_step's bit for bit, also through the prepared
+    DecodeStep (run_host) twice in a row with new activations."""
+    shapes = [(5120, 6144), (6144, 5120), (640, 80)]
+    mats = [DevMatrix(K, N, matrix_id=1200 + i) for i, (K, N) in enumerate(shapes)]
+    xoff = np.cumsum([0] + [M * K for K, _ in shapes])
+    yoff = np.cumsum([0] + [M * N for _, N in shapes])
+    x_dev = torch.zeros(int(xoff[-1]), dtype=torch.int16, device="cuda")
+    y_dev = torch.zeros(int(yoff[-1]), dtype=torch.int16, device="cuda")
+    x_host = torch.empty(int(xoff[-1]), dtype=torch.int16)
+    y_host = torch.empty(int(yoff[-1]), dtype=torch.int16)
+    if pinned:
+        x_host, y_host = x_host.pin_memory(), y_host.pin_memory()
+    descs = [(m.packed, x_dev[xoff[i]:xoff[i + 1]], y_dev[yoff[i]:yoff[i + 1]], K, N)
+             for i, (m, (K, N)) in enumerate(zip(mats, shapes))]
+    ws = torch.empty(w.w4g128_decode_step_workspace_bytes(descs, M), dtype=torch.uint8, device="cuda")
+    step = w.DecodeStep(descs, M, ws, x_host=x_host, x_dev=x_dev, y_host=y_host, y_dev=y_dev)
+    for rep in range(3):
+        xh = [synth.x(SEED, 1300 + 10 * rep + i, M, K) for i, (K, _) in enumerate(shapes)]
+        x_host.copy_(torch.from_numpy(np.concatenate([x.ravel() for x in xh]).view(np.int16)))
+        if rep == 0:
+            w.w4g128_decode_step_host(descs, M, x_host, x_dev, x_dev.numel() * 2, y_host, y_dev, y_dev.numel() * 2, ws)
+        else:
+            step.run_host()
+        torch.cuda.synchronize()
+        assert w.w4g128_workspace_status(ws) == 0
+        got = y_host.numpy().view(np.uint16).copy()
+        expect = decode_step(mats, [to_dev(x) for x in xh], M)
+        for i in range(len(shapes)):
+            assert np.array_equal(got[yoff[i]:yoff[i + 1]].reshape(M, -1), expect[i])

@@ -178,3 +178,42 @@ def test_largest_n_every_output():
         x = synth.x(SEED, 102 + M, M, K)
         y = run(mat, x, verify=(M > 1))
         check_against_oracle(y, x, mat.codes, mat.scales, mat.mins)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("K,N", [(4096, 4096), (17408, 5120), (1152, 208), (5120, 248320)])
+def test_local_and_prep_paths_agree(K, N):
+    """An M = 1 call builds its activation packages inside each streaming CTA
+    when x is 16-byte aligned (and the CTAs' working sets fit in shared
+    memory), else through the prep kernel; with x only 4-byte aligned the
+    call takes the prep path.  Both paths give the same bits, within the
+    bound, through w4g128_gemv and through a two-matrix decode step."""
+    mat = DevMatrix(K, N, matrix_id=K + 7)
+    x = synth.x(SEED, K + 7, 1, K)
+    xa = to_dev(x)
+    buf = torch.zeros(K + 8, dtype=torch.int16, device="cuda")
+    xm = buf[2:2 + K]  # 4 bytes past a 16-byte boundary
+    xm.copy_(xa.view(-1))
+    assert xm.data_ptr() % 16 == 4
+    ys = []
+    for xd in (xa, xm):
+        y = torch.empty(N, dtype=torch.int16, device="cuda")
+        ws = workspace(1, K, N)
+        w.w4g128_gemv(mat.packed, xd, y, K, N, ws)
+        torch.cuda.synchronize()
+        assert w.w4g128_workspace_status(ws) == 0
+        ys.append(to_host(y, np.uint16))
+    assert np.array_equal(ys[0], ys[1])
+    check_against_oracle(ys[0].reshape(1, N), x, mat.codes, mat.scales, mat.mins)
+    small = DevMatrix(640, 80, matrix_id=K + 8)
+    xs = synth.x(SEED, K + 8, 1, 640)
+    for xd in (xa, xm):
+        y = torch.empty(N, dtype=torch.int16, device="cuda")
+        y2 = torch.empty(80, dtype=torch.int16, device="cuda")
+        descs = [(mat.packed, xd, y, K, N), (small.packed, to_dev(xs), y2, 640, 80)]
+        ws = torch.empty(w.w4g128_decode_step_workspace_bytes(descs, 1), dtype=torch.uint8, device="cuda")
+        w.w4g128_decode_step(descs, 1, ws)
+        torch.cuda.synchronize()
+        assert w.w4g128_workspace_status(ws) == 0
+        assert np.array_equal(to_host(y, np.uint16), ys[0])
+        assert np.array_equal(to_host(y2, np.uint16), run(small, xs)[0])
