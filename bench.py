@@ -51,7 +51,7 @@ L2_BYTES = 129 * 1024 * 1024
 SEED = 20260001
 NCOPY = 4
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0}
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "stream_kernel_layer_m1.md")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "stream1_local_kernel_layer_m1.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "int4_weight_only_g128_gb300", "csrc", f)
                   for f in ("w4g128_stream.cu", "w4g128_ptx.cuh", "w4g128_internal.h")]
 
@@ -299,6 +299,7 @@ def run_reference(args):
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out), flush=True)
+    record(args, out)
     return 0
 
 
@@ -717,7 +718,7 @@ def run_ours(args):
                      "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
                      "peak_source": ("measured copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                                      if peak_kind == "measured" else "fallback 6.8 TB/s"),
-                     "kernel": "stream_kernel (M=1, one-row warp-MMA path) + its prep kernel, per decode_step call"},
+                     "kernel": "stream1_local_kernel (M=1: activation packages built in each CTA) + fold1_kernel, per decode_step call"},
         "m8": {"value": round(value8, 1), "unit": "GB/s", "ms_per_step": round(1e3 * total8 / args.steps, 5),
                "achieved": round(achieved8, 1), "frac": round(achieved8 / peak, 4),
                "verify_cost_ratio_t8_over_t1": round(total8 / total1, 4)},
@@ -746,7 +747,23 @@ def run_ours(args):
         "measured_tok_per_s_full_decode_step_M1": full["M1"]["steps_per_s"],
     }
     print(json.dumps(out), flush=True)
+    record(args, out)
     return 0
+
+
+def record(args, out):
+    """With --record DIR, append the line to DIR/<date>-<host>/bench.jsonl
+    (the run history the tables of measured figures are written from)."""
+    if not args.record:
+        return
+    import datetime
+    import socket
+    day = datetime.datetime.now(datetime.timezone.utc).strftime("%Y-%m-%d")
+    d = os.path.join(args.record, f"{day}-{socket.gethostname()}")
+    os.makedirs(d, exist_ok=True)
+    line = dict(out, recorded_utc=datetime.datetime.now(datetime.timezone.utc).isoformat(timespec="seconds"))
+    with open(os.path.join(d, "bench.jsonl"), "a") as f:
+        f.write(json.dumps(line) + "\n")
 
 
 def run_target(args):
@@ -807,6 +824,7 @@ def main():
     ap.add_argument("--target", choices=["layer", "lm_head"], help="profiler target: untimed calls, no JSON")
     ap.add_argument("--m", default="1", help="with --target: comma-separated M values")
     ap.add_argument("--calls", type=int, default=2, help="with --target: calls per M")
+    ap.add_argument("--record", default=None, help="append the JSON line to DIR/<date>-<host>/bench.jsonl")
     args = ap.parse_args()
     if args.target:
         return run_target(args)
