@@ -11,7 +11,7 @@ import ctypes
 import os
 
 __all__ = [
-    "W4G128Error", "lib", "exported_symbols",
+    "W4G128Error", "lib", "lib_debug", "exported_symbols",
     "w4g128_status_string", "w4g128_packed_bytes", "w4g128_pack", "w4g128_unpack", "w4g128_quantize",
     "w4g128_workspace_bytes", "w4g128_gemv", "w4g128_gemm_verify",
     "w4g128_decode_step_workspace_bytes", "w4g128_decode_step", "w4g128_verify_step", "w4g128_workspace_status",
@@ -55,6 +55,9 @@ def exported_symbols():
     return names
 
 
+_lib_debug = None
+
+
 def lib():
     """Load libw4g128.so (building it in-tree if it is missing)."""
     global _lib
@@ -64,7 +67,28 @@ def lib():
     path = _build.LIB
     if not os.path.exists(path):
         _build.build()
-    L = ctypes.CDLL(path)
+    _lib = _declare(ctypes.CDLL(path))
+    return _lib
+
+
+def lib_debug():
+    """Load libw4g128_debug.so, the range-checked build of the same sources
+    (W4G128_DEBUG: every global access derived from the schedule is checked,
+    a failure recorded as W4G128_ERR_INTERNAL in the status word); for tests.
+    Call its functions directly (the wrappers below use lib())."""
+    global _lib_debug
+    if _lib_debug is not None:
+        return _lib_debug
+    from . import build as _build
+    path = _build.LIB_DEBUG
+    if not os.path.exists(path):
+        _build.build(debug=True)
+    _lib_debug = _declare(ctypes.CDLL(path))
+    return _lib_debug
+
+
+def _declare(L):
+    """Argument and result types of every entry point."""
     p, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     L.w4g128_status_string.restype = ctypes.c_char_p
     L.w4g128_status_string.argtypes = [i]
@@ -106,7 +130,6 @@ def lib():
     L.w4g128_selftest_wait.argtypes = [p, sz, ctypes.c_ulonglong, i, p]
     L.w4g128_gemm_add_rmsnorm.restype = i
     L.w4g128_gemm_add_rmsnorm.argtypes = [p, p, p, p, ctypes.c_float, p, p, i, i, i, i, p, sz, p]
-    _lib = L
     return L
 
 

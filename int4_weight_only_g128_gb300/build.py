@@ -12,6 +12,11 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libw4g128.so")
+# The same sources with -DW4G128_DEBUG: every global access the kernels derive
+# from the schedule is range-checked, a failed check is recorded in the status
+# word and the access skipped (for tests; slower, never used by the product).
+DEBUG_BUILD = os.path.join(BUILD, "debug")
+LIB_DEBUG = os.path.join(BUILD, "libw4g128_debug.so")
 
 SOURCES = ["w4g128_api.cu", "w4g128_pack.cu", "w4g128_stream.cu", "w4g128_probe.cu", "w4g128_noalloc.cu",
            "w4g128_quant.cu", "w4g128_selftest.cu", "w4g128_hostio.cu"]
@@ -32,8 +37,8 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(src, extra):
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+def _compile(src, extra, outdir=BUILD):
+    obj = os.path.join(outdir, os.path.splitext(src)[0] + ".o")
     deps = [os.path.join(CSRC, src)] + _headers()
     if _stale(obj, deps) or extra:
         cmd = ["nvcc", "-c", os.path.join(CSRC, src), "-o", obj] + ARCH + FLAGS + list(extra)
@@ -43,25 +48,42 @@ def _compile(src, extra):
     return obj
 
 
-def build(extra_flags=(), force=False, verbose=False):
-    """Compile (if stale) and return the path of libw4g128.so."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(extra_flags=(), force=False, verbose=False, debug=False):
+    """Compile (if stale) and return the path of libw4g128.so (debug: of
+    libw4g128_debug.so, the range-checked build)."""
+    outdir, lib = (DEBUG_BUILD, LIB_DEBUG) if debug else (BUILD, LIB)
+    os.makedirs(outdir, exist_ok=True)
     extra = list(extra_flags)
-    if force and os.path.exists(LIB):
-        os.remove(LIB)
+    flags = extra + (["-DW4G128_DEBUG"] if debug else [])
+    if force and os.path.exists(lib):
+        os.remove(lib)
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), SOURCES))
-    if _stale(LIB, objs) or extra:
+        objs = list(ex.map(lambda s: _compile(s, flags, outdir) if not debug else _compile_debug(s, flags, outdir),
+                           SOURCES))
+    if _stale(lib, objs) or extra:
         # -fvisibility=hidden keeps internal symbols out; the extern "C" API is
         # exported by the W4G128_API attribute on its declarations.
-        cmd = ["nvcc", "-shared", "-o", LIB] + objs + ARCH + ["-cudart", "static"]
+        cmd = ["nvcc", "-shared", "-o", lib] + objs + ARCH + ["-cudart", "static"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     if verbose:
-        print(LIB, file=sys.stderr)
-    return LIB
+        print(lib, file=sys.stderr)
+    return lib
+
+
+def _compile_debug(src, flags, outdir):
+    """Like _compile, but the define alone does not make a stale object."""
+    obj = os.path.join(outdir, os.path.splitext(src)[0] + ".o")
+    deps = [os.path.join(CSRC, src)] + _headers()
+    if _stale(obj, deps) or len(flags) > 1:
+        cmd = ["nvcc", "-c", os.path.join(CSRC, src), "-o", obj] + ARCH + FLAGS + list(flags)
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+    return obj
 
 
 if __name__ == "__main__":
     build(verbose=True)
+    build(verbose=True, debug=True)

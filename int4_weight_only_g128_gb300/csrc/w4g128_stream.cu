@@ -96,6 +96,41 @@ __host__ __device__ constexpr bool multi_row() { return MODE == kMMA || MODE == 
 constexpr int kNW = W4G128_WARPS_PER_CTA;  // warps per CTA
 constexpr int kDepth = W4G128_RING_DEPTH;  // ring slots per warp
 
+// ----------------------------------------------------------------- debug checks
+
+// Built with -DW4G128_DEBUG, the kernels check the index of every global
+// access they derive from the schedule (weight and package copies, x
+// staging, partial slots, tickets, y) against its buffer; a check that fails
+// records W4G128_ERR_INTERNAL in the status word and the access is skipped
+// (a skipped copy still completes its ring slot, so nothing waits for it).
+// Nothing traps.  Release builds compile the checks away.
+#ifdef W4G128_DEBUG
+constexpr bool kDebug = true;
+#else
+constexpr bool kDebug = false;
+#endif
+
+// cond, or (debug builds) false after recording the failure in a 32-bit
+// status word (the prep-kernel path's).
+__device__ __forceinline__ bool dbg_ok(unsigned* status, bool cond) {
+  if constexpr (kDebug) {
+    if (!cond) atomicCAS(status, 0u, static_cast<unsigned>(W4G128_ERR_INTERNAL));
+    return cond;
+  } else {
+    return true;
+  }
+}
+
+// Completes one arrival on an mbarrier without a copy (a skipped copy's slot).
+__device__ __forceinline__ void mbar_arrive_plain(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Bytes of the packed form of a K x N matrix.
+__host__ __device__ inline long long packed_bytes_of(int K, int N) {
+  return static_cast<long long>(N / kTileN) * (K / kGroup) * kBlockBytes;
+}
+
 // Activation package per group: rows x 4 lane classes c x (16 fp16-pair
 // words + 4 unused) = rows x 320 bytes, then per row m the pair
 // (X_g[m], f[m]) as fp32.  Row (m, c) word 2i holds x'[m][k0+2c],
@@ -314,15 +349,45 @@ __device__ __forceinline__ int owner_of(long long item, long long I, int W) {
 
 // ----------------------------------------------------------------- chunk copy
 
+// Debug builds: the chunk's weight blocks and activation package lie inside
+// their matrix's packed bytes and packages.
+template <int MODE, int MAXMAT>
+__device__ __forceinline__ bool chunk_in_range(const StreamParams<MAXMAT>& p, const Cursor& c) {
+  if constexpr (!kDebug) {
+    return true;
+  } else {
+    const MatParams& m = mat(p, c.mi);
+    const bool w = c.src >= m.packed && c.src + c.ntiles * kBlockBytes <= m.packed + packed_bytes_of(m.K, m.N);
+    const bool x = c.xsrc >= m.xpkg && c.xsrc + Pkg<MODE>::kBytes <= m.xpkg + static_cast<long long>(m.K / kGroup) *
+                                                                                 Pkg<MODE>::kBytes;
+    return dbg_ok(p.status, w && x);
+  }
+}
+
 // The chunk (quad q, group g) is nt(q) adjacent blocks: one bulk copy.
-template <int MODE>
-__device__ __forceinline__ void issue_weights(const Cursor& c, uint32_t slot, uint32_t bar, uint64_t pol) {
+// Debug builds skip a copy outside its buffers (an arrival completes the
+// slot instead).
+template <int MODE, int MAXMAT>
+__device__ __forceinline__ void issue_weights(const StreamParams<MAXMAT>& p, const Cursor& c, uint32_t slot,
+                                              uint32_t bar, uint64_t pol) {
+  if (!chunk_in_range<MODE>(p, c)) {
+    mbar_arrive_plain(bar);
+    return;
+  }
   mbar_arrive_expect_tx(bar, c.ntiles * kBlockBytes + Pkg<MODE>::kBytes);
   bulk_g2s(slot, c.src, c.ntiles * kBlockBytes, bar, pol);
 }
 
-template <int MODE>
-__device__ __forceinline__ void issue_package(const Cursor& c, uint32_t slot, uint32_t bar, uint64_t pol) {
+template <int MODE, int MAXMAT>
+__device__ __forceinline__ void issue_package(const StreamParams<MAXMAT>& p, const Cursor& c, uint32_t slot,
+                                              uint32_t bar, uint64_t pol) {
+  if constexpr (kDebug) {
+    const MatParams& m = mat(p, c.mi);
+    const bool w = c.src >= m.packed && c.src + c.ntiles * kBlockBytes <= m.packed + packed_bytes_of(m.K, m.N);
+    const bool x = c.xsrc >= m.xpkg && c.xsrc + Pkg<MODE>::kBytes <= m.xpkg + static_cast<long long>(m.K / kGroup) *
+                                                                                 Pkg<MODE>::kBytes;
+    if (!(w && x)) return;  // recorded (and the slot completed) by issue_weights
+  }
   bulk_g2s(slot + kQuadTiles * kBlockBytes, c.xsrc, Pkg<MODE>::kBytes, bar, pol);
 }
 
@@ -630,7 +695,7 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
 #pragma unroll
     for (int d = 0; d < kEarly; ++d) {
       if (ic.item < it_b) {
-        if (lane == 0) issue_weights<MODE>(ic, ring0 + d * kSlot, bar0 + 8 * d, pol_w);
+        if (lane == 0) issue_weights<MODE>(p, ic, ring0 + d * kSlot, bar0 + 8 * d, pol_w);
         pre[d] = ic;
         ++n_pre;
         cursor_next<MODE>(ic, p);
@@ -640,13 +705,13 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
     if (lane == 0) {
 #pragma unroll
       for (int d = 0; d < kEarly; ++d)
-        if (d < n_pre) issue_package<MODE>(pre[d], ring0 + d * kSlot, bar0 + 8 * d, pol_x);
+        if (d < n_pre) issue_package<MODE>(p, pre[d], ring0 + d * kSlot, bar0 + 8 * d, pol_x);
     }
     unsigned issued = static_cast<unsigned>(n_pre);
     while (issued < static_cast<unsigned>(D) && ic.item < it_b) {  // the rest of the ring
       if (lane == 0) {
-        issue_weights<MODE>(ic, ring0 + issued * kSlot, bar0 + 8 * issued, pol_w);
-        issue_package<MODE>(ic, ring0 + issued * kSlot, bar0 + 8 * issued, pol_x);
+        issue_weights<MODE>(p, ic, ring0 + issued * kSlot, bar0 + 8 * issued, pol_w);
+        issue_package<MODE>(p, ic, ring0 + issued * kSlot, bar0 + 8 * issued, pol_x);
       }
       cursor_next<MODE>(ic, p);
       ++issued;
@@ -694,8 +759,8 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
         if (lane == 0) {
           fence_proxy_async_smem();
           const uint32_t sa = ring0 + slot * kSlot, ba = bar0 + 8 * slot;
-          issue_weights<MODE>(ic, sa, ba, pol_w);
-          issue_package<MODE>(ic, sa, ba, pol_x);
+          issue_weights<MODE>(p, ic, sa, ba, pol_w);
+          issue_package<MODE>(p, ic, sa, ba, pol_x);
         }
         cursor_next<MODE>(ic, p);
         ++issued;
@@ -724,7 +789,7 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
 #pragma unroll
             for (int e = 0; e < NA; ++e) tot[t][e] = (cc.s == 0) ? seg[t][e] : tot[t][e] + seg[t][e];
         }
-        if (!owned && (!prefix || cc.item + 1 == it_b)) {
+        if (!owned && (!prefix || cc.item + 1 == it_b) && dbg_ok(p.status, cc.item < I)) {
           // one slot per (matrix, quad, segment): the segment sum, or at the last
           // segment of a prefix run the fold of segments 0 .. s
           float* part = p.partials + cc.item * rows * 64;
@@ -768,7 +833,7 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
         const bool quad_end = (cc.s == S - 1) || (cc.item + 1 == it_b);
         if (quad_end) {
           const int n0 = kQuadTiles * kTileN * cc.q;
-          if (owned) {
+          if (owned && dbg_ok(p.status, n0 + kTileN * ntiles <= m.N)) {
             if constexpr (MODE == kMMA1) {
               if (c == 0) {
 #pragma unroll
@@ -838,7 +903,7 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
       // contributor's partials visible to this CTA (its threads are ordered
       // after it by the barrier before the fold).  No full fence is needed.
       __syncwarp();
-      if (lane == 0) {
+      if (lane == 0 && dbg_ok(p.status, pend_q0 < p.total_quads && (n_pend < 2 || pend_q1 < p.total_quads))) {
         // the warp holding a quad's last ticket hands the quad to its CTA's fold
         if (ticket_acq_rel(p.tickets + pend_q0) + 1 == pend_e0) fold_ref[atomicAdd(&fold_n, 1)] = 2 * warp;
         if (n_pend > 1 && ticket_acq_rel(p.tickets + pend_q1) + 1 == pend_e1)
@@ -857,6 +922,7 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
     const PendFold& f = pend_info[fold_ref[idx >> 4]];
     const int col = 4 * (idx & 15);
     if (col >= f.cols) continue;  // ragged last quad
+    if (!dbg_ok(p.status, f.first >= 0 && f.first + f.nslot <= I)) continue;
     const int nslot = f.nslot;
     const float4* part = reinterpret_cast<const float4*>(p.partials + f.first * 64 + col);
     const uint32_t r0 = residual2<NORM>(p, f.n0 + col), r1 = residual2<NORM>(p, f.n0 + col + 2);
@@ -1185,6 +1251,29 @@ __device__ __forceinline__ void status_fail(unsigned* status, unsigned code) {
   }
 }
 
+// cond, or (debug builds) false after recording the failure in a local
+// call's tagged status word.
+__device__ __forceinline__ bool dbg_ok_local(unsigned* status, bool cond) {
+  if constexpr (kDebug) {
+    if (!cond) status_fail(status, W4G128_ERR_INTERNAL);
+    return cond;
+  } else {
+    return true;
+  }
+}
+
+// Debug builds: a chunk's weight blocks lie inside their matrix's packed bytes.
+template <int MAXMAT>
+__device__ __forceinline__ bool weights_in_range(const StreamParams<MAXMAT>& p, const Cursor& c) {
+  if constexpr (!kDebug) {
+    return true;
+  } else {
+    const MatParams& m = mat(p, c.mi);
+    return dbg_ok_local(p.status, c.src >= m.packed &&
+                                      c.src + c.ntiles * kBlockBytes <= m.packed + packed_bytes_of(m.K, m.N));
+  }
+}
+
 // A fold the CTA does at its end: slots [first, first + nslot) of its
 // shared-memory partial area (indices relative to its first item), written
 // to y (a quad inside the CTA's range) or, for the quad that continues into
@@ -1272,8 +1361,12 @@ __global__ void __maxnreg__(120) stream1_local_kernel(const __grid_constant__ St
     while (issued < static_cast<unsigned>(D) && ic.item < it_b) {
       if (lane == 0) {
         const uint32_t sa = ring0 + (issued * cw + warp) * kLocalSlot, ba = bars + 8 * (warp * D + issued);
-        mbar_arrive_expect_tx(ba, ic.ntiles * kBlockBytes);
-        bulk_g2s(sa, ic.src, ic.ntiles * kBlockBytes, ba, pol_w);
+        if (weights_in_range(p, ic)) {
+          mbar_arrive_expect_tx(ba, ic.ntiles * kBlockBytes);
+          bulk_g2s(sa, ic.src, ic.ntiles * kBlockBytes, ba, pol_w);
+        } else {
+          mbar_arrive_plain(ba);
+        }
       }
       cursor_next<kMMA1>(ic, p);
       ++issued;
@@ -1288,8 +1381,9 @@ __global__ void __maxnreg__(120) stream1_local_kernel(const __grid_constant__ St
     int e = 0;
     while (e + 1 < tbl_n && tbl[e + 1].pkg <= t) ++e;
     const int g = tbl[e].g_lo + (t - tbl[e].pkg);
-    cp_async16(smem_addr(stage + t * kStageStride + part * 16),
-               mat(p, tbl[e].mi).x + static_cast<long long>(g) * kGroup + part * 8);
+    if (dbg_ok_local(p.status, g >= 0 && g < mat(p, tbl[e].mi).K / kGroup))
+      cp_async16(smem_addr(stage + t * kStageStride + part * 16),
+                 mat(p, tbl[e].mi).x + static_cast<long long>(g) * kGroup + part * 8);
   }
   cp_async_wait_all();
   // the status word is cleared by a thread of the second warp (thread 0 of a
@@ -1345,8 +1439,12 @@ __global__ void __maxnreg__(120) stream1_local_kernel(const __grid_constant__ St
         if (lane == 0) {
           fence_proxy_async_smem();
           const uint32_t sa = ring0 + (slot * cw + warp) * kLocalSlot, ba = bars + 8 * (warp * D + slot);
-          mbar_arrive_expect_tx(ba, ic.ntiles * kBlockBytes);
-          bulk_g2s(sa, ic.src, ic.ntiles * kBlockBytes, ba, pol_w);
+          if (weights_in_range(p, ic)) {
+            mbar_arrive_expect_tx(ba, ic.ntiles * kBlockBytes);
+            bulk_g2s(sa, ic.src, ic.ntiles * kBlockBytes, ba, pol_w);
+          } else {
+            mbar_arrive_plain(ba);
+          }
         }
         cursor_next<kMMA1>(ic, p);
         ++issued;
@@ -1371,7 +1469,7 @@ __global__ void __maxnreg__(120) stream1_local_kernel(const __grid_constant__ St
 #pragma unroll
             for (int e = 0; e < NA; ++e) tot[t][e] = (cc.s == 0) ? seg[t][e] : tot[t][e] + seg[t][e];
         }
-        if (!owned && (!prefix || cc.item + 1 == it_b)) {
+        if (!owned && (!prefix || cc.item + 1 == it_b) && dbg_ok_local(p.status, cc.item >= A && cc.item < B)) {
           // a quad that began before this CTA: the segment sum goes to its
           // global slot for the boundary fold; otherwise to this CTA's slot
           float* part = (q_first < A) ? p.partials + cc.item * 64 : part_area + (cc.item - A) * 64;
@@ -1393,7 +1491,7 @@ __global__ void __maxnreg__(120) stream1_local_kernel(const __grid_constant__ St
         const bool quad_end = (cc.s == S - 1) || (cc.item + 1 == it_b);
         if (quad_end) {
           const int n0 = kQuadTiles * kTileN * cc.q;
-          if (owned) {
+          if (owned && dbg_ok_local(p.status, n0 + kTileN * ntiles <= m.N)) {
             if (c == 0) {
 #pragma unroll
               for (int t = 0; t < kQuadTiles; ++t) {
@@ -1437,6 +1535,7 @@ __global__ void __maxnreg__(120) stream1_local_kernel(const __grid_constant__ St
     const LocalFold& f = folds[idx >> 4];
     const int col = 4 * (idx & 15);
     if (col >= f.cols) continue;
+    if (!dbg_ok_local(p.status, f.first >= 0 && f.first + f.nslot <= B - A)) continue;
     const float4* part = reinterpret_cast<const float4*>(part_area + f.first * 64 + col);
     uint32_t r0 = 0u, r1 = 0u;
     if (f.y != nullptr) {
@@ -1493,6 +1592,10 @@ __global__ void __launch_bounds__(32) fold1_kernel(const __grid_constant__ Strea
     return;
   }
   const int nslot = S - s + 1;  // CTA cb - 1's slot (item Ac - 1), then segments s .. S - 1
+  if (!dbg_ok_local(p.status, Ac - 1 + nslot <= I && nslot <= kMaxFoldSlots)) {
+    if (blockIdx.x + 1 == gridDim.x) grid_dependency_wait();
+    return;
+  }
   const int cols = kTileN * min(kQuadTiles, m.N / kTileN - kQuadTiles * q);
   const int col = 4 * threadIdx.x;
   const bool active = col < cols && threadIdx.x < 16;
@@ -1577,6 +1680,10 @@ __global__ void __launch_bounds__(kRedThreads) reduce_quads_kernel(const __grid_
   // segments before it) to the quad's last segment.
   const long long first = I * (wf + 1) / p.W - 1;
   const int nslot = static_cast<int>(q_first + S - first);
+  if (!dbg_ok(p.status, first >= 0 && first + nslot <= I && gq < p.total_quads)) {
+    grid_dependency_wait();
+    return;
+  }
 
   grid_dependency_wait();  // every partial of the streaming kernel is written and visible
   const int per_quad = p.M * 64;  // floats per partial slot
@@ -1694,6 +1801,10 @@ __global__ void __launch_bounds__(kRedThreads) reduce_warps_kernel(const __grid_
   const MatParams& m = mat(p, mi);
   const int S = div_up(m.K / kGroup, kSegGroups);
   const int nslot = S - s + 1;
+  if (!dbg_ok(p.status, it_a - 1 >= 0 && it_a - 1 + nslot <= I && mi < p.count)) {
+    grid_dependency_wait();
+    return;
+  }
   const int cols = kTileN * min(kQuadTiles, m.N / kTileN - kQuadTiles * q);
   const int u = threadIdx.x, row = u >> 4, col = 4 * (u & 15);
   const bool active = row < p.M && col < cols;

@@ -189,3 +189,12 @@ def test_decode_step_host_argument_errors(L):
     assert L.w4g128_decode_step_host(mats, 0, 1, FAKE, FAKE, 16, FAKE, FAKE, 16, FAKE, 1 << 20, None) == E_INVALID
     mats[0] = w._Matrix(FAKE, FAKE, FAKE, 128, 24)
     assert L.w4g128_decode_step_host(mats, 1, 1, FAKE, FAKE, 16, FAKE, FAKE, 16, FAKE, 1 << 20, None) == E_SHAPE
+
+
+def test_debug_library_exports_every_symbol():
+    """The range-checked build (W4G128_DEBUG) loads beside the release one and
+    exports the same entry points, with the same argument checks."""
+    D = w.lib_debug()
+    for n in w.exported_symbols():
+        assert hasattr(D, n), n
+    assert D.w4g128_gemv(FAKE, FAKE, FAKE, 100, 16, FAKE, 1 << 20, None) == E_SHAPE
