@@ -506,7 +506,12 @@ template <int MODE> struct Acc {
 
 // One chunk: every tile of the quad for one group (weights in the ring slot
 // sl, the group's activation package at pk), added into seg[t][*].
-template <int MODE>
+// ILP (M <= 8): 0 -- tile by tile; 1 -- a whole quad's tiles in pairs, both
+// tiles' MMAs interleaved; 2 -- all four tiles interleaved.  Each
+// accumulator receives the same MMAs in the same order in every form: the
+// same bits; the interleaved forms hold more registers and keep a warp that
+// is alone on its scheduler from waiting on one tile's dependent chain.
+template <int MODE, int ILP = 0>
 __device__ __forceinline__ void compute_chunk(const uint8_t* sl, const uint8_t* pk, int ntiles, int lane,
                                               float (&seg)[kQuadTiles][Acc<MODE>::kN]) {
   const int r = lane >> 2, c = lane & 3;
@@ -583,6 +588,96 @@ __device__ __forceinline__ void compute_chunk(const uint8_t* sl, const uint8_t* 
     const float2 Xab = make_float2(xq.x, xq.z);
     const float2 fab = make_float2(xq.y, xq.w);
     const float2 fab16 = make_float2(xq.y * 0.0625f, xq.w * 0.0625f);
+    // Tile t's sums: (1024 + q) x' (columns r) and (1024 + 16q) x' (columns
+    // r + 8) as (column, row) fragments in two chains, words 0, 2, 4, 6 into
+    // d0 and 1, 3, 5, 7 into d1; then its scale/min epilogue into seg[t].
+    auto epilogue = [&](int t, uint2 me, const float (&d0)[4], const float (&d1)[4]) {
+      const float sl0 = bf16_lo(me.x), sh0 = bf16_lo(me.y);
+      const float ml0 = fmaf(-1024.f, sl0, bf16_hi(me.x));
+      const float mh0 = fmaf(-64.f, sh0, bf16_hi(me.y));
+      if constexpr (MODE == kMMA1) {
+        // the first lane of each pair below, alone: the same roundings
+        seg[t][0] = __fmaf_rn(__fmul_rn(sl0, fab.x), d0[0] + d1[0], __fmaf_rn(ml0, Xab.x, seg[t][0]));
+        seg[t][1] = __fmaf_rn(__fmul_rn(sh0, fab16.x), d0[2] + d1[2], __fmaf_rn(mh0, Xab.x, seg[t][1]));
+      } else {
+        float2 lo2 = ffma2(make_float2(ml0, ml0), Xab, make_float2(seg[t][0], seg[t][1]));
+        lo2 = ffma2(fmul2(make_float2(sl0, sl0), fab), make_float2(d0[0] + d1[0], d0[1] + d1[1]), lo2);
+        float2 hi2 = ffma2(make_float2(mh0, mh0), Xab, make_float2(seg[t][2], seg[t][3]));
+        hi2 = ffma2(fmul2(make_float2(sh0, sh0), fab16), make_float2(d0[2] + d1[2], d0[3] + d1[3]), hi2);
+        seg[t][0] = lo2.x;
+        seg[t][1] = lo2.y;
+        seg[t][2] = hi2.x;
+        seg[t][3] = hi2.y;
+      }
+    };
+    if (ILP == 2 && ntiles == kQuadTiles) {
+      uint4 u0[kQuadTiles], u1[kQuadTiles];
+      uint2 me[kQuadTiles];
+#pragma unroll
+      for (int t = 0; t < kQuadTiles; ++t) {
+        const uint8_t* blk = sl + t * kBlockBytes;
+        u0[t] = *reinterpret_cast<const uint4*>(blk + 16 * lane);
+        u1[t] = *reinterpret_cast<const uint4*>(blk + 512 + 16 * lane);
+        me[t] = *reinterpret_cast<const uint2*>(blk + kCodeBytes + 8 * r);
+      }
+      float d0[kQuadTiles][4], d1[kQuadTiles][4];
+#pragma unroll
+      for (int t = 0; t < kQuadTiles; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d0[t][e] = d1[t][e] = 0.f;
+#pragma unroll
+      for (int t = 0; t < kQuadTiles; ++t) mma_word(u0[t].x, xw[0], xw[1], d0[t]);
+#pragma unroll
+      for (int t = 0; t < kQuadTiles; ++t) mma_word(u0[t].y, xw[2], xw[3], d1[t]);
+#pragma unroll
+      for (int t = 0; t < kQuadTiles; ++t) mma_word(u0[t].z, xw[4], xw[5], d0[t]);
+#pragma unroll
+      for (int t = 0; t < kQuadTiles; ++t) mma_word(u0[t].w, xw[6], xw[7], d1[t]);
+#pragma unroll
+      for (int t = 0; t < kQuadTiles; ++t) mma_word(u1[t].x, xw[8], xw[9], d0[t]);
+#pragma unroll
+      for (int t = 0; t < kQuadTiles; ++t) mma_word(u1[t].y, xw[10], xw[11], d1[t]);
+#pragma unroll
+      for (int t = 0; t < kQuadTiles; ++t) mma_word(u1[t].z, xw[12], xw[13], d0[t]);
+#pragma unroll
+      for (int t = 0; t < kQuadTiles; ++t) mma_word(u1[t].w, xw[14], xw[15], d1[t]);
+#pragma unroll
+      for (int t = 0; t < kQuadTiles; ++t) epilogue(t, me[t], d0[t], d1[t]);
+      return;
+    }
+    if (ILP == 1 && ntiles == kQuadTiles) {
+#pragma unroll
+      for (int t = 0; t < kQuadTiles; t += 2) {
+        const uint8_t* blk = sl + t * kBlockBytes;
+        const uint4 a0 = *reinterpret_cast<const uint4*>(blk + 16 * lane);
+        const uint4 a1 = *reinterpret_cast<const uint4*>(blk + 512 + 16 * lane);
+        const uint2 ma = *reinterpret_cast<const uint2*>(blk + kCodeBytes + 8 * r);
+        const uint4 b0 = *reinterpret_cast<const uint4*>(blk + kBlockBytes + 16 * lane);
+        const uint4 b1 = *reinterpret_cast<const uint4*>(blk + kBlockBytes + 512 + 16 * lane);
+        const uint2 mb = *reinterpret_cast<const uint2*>(blk + kBlockBytes + kCodeBytes + 8 * r);
+        float da0[4] = {0.f, 0.f, 0.f, 0.f}, da1[4] = {0.f, 0.f, 0.f, 0.f};
+        float db0[4] = {0.f, 0.f, 0.f, 0.f}, db1[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_word(a0.x, xw[0], xw[1], da0);
+        mma_word(b0.x, xw[0], xw[1], db0);
+        mma_word(a0.y, xw[2], xw[3], da1);
+        mma_word(b0.y, xw[2], xw[3], db1);
+        mma_word(a0.z, xw[4], xw[5], da0);
+        mma_word(b0.z, xw[4], xw[5], db0);
+        mma_word(a0.w, xw[6], xw[7], da1);
+        mma_word(b0.w, xw[6], xw[7], db1);
+        mma_word(a1.x, xw[8], xw[9], da0);
+        mma_word(b1.x, xw[8], xw[9], db0);
+        mma_word(a1.y, xw[10], xw[11], da1);
+        mma_word(b1.y, xw[10], xw[11], db1);
+        mma_word(a1.z, xw[12], xw[13], da0);
+        mma_word(b1.z, xw[12], xw[13], db0);
+        mma_word(a1.w, xw[14], xw[15], da1);
+        mma_word(b1.w, xw[14], xw[15], db1);
+        epilogue(t, ma, da0, da1);
+        epilogue(t + 1, mb, db0, db1);
+      }
+      return;
+    }
 #pragma unroll
     for (int t = 0; t < kQuadTiles; ++t) {
       if (t < ntiles) {
@@ -590,8 +685,6 @@ __device__ __forceinline__ void compute_chunk(const uint8_t* sl, const uint8_t* 
         const uint4 u0 = *reinterpret_cast<const uint4*>(blk + 16 * lane);
         const uint4 u1 = *reinterpret_cast<const uint4*>(blk + 512 + 16 * lane);
         const uint2 me = *reinterpret_cast<const uint2*>(blk + kCodeBytes + 8 * r);
-        // sum_k (1024 + q) x' (columns r) and (1024 + 16q) x' (columns r + 8) as
-        // (column, row) fragments, two chains
         float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
         mma_word(u0.x, xw[0], xw[1], d0);
         mma_word(u0.y, xw[2], xw[3], d1);
@@ -601,23 +694,7 @@ __device__ __forceinline__ void compute_chunk(const uint8_t* sl, const uint8_t* 
         mma_word(u1.y, xw[10], xw[11], d1);
         mma_word(u1.z, xw[12], xw[13], d0);
         mma_word(u1.w, xw[14], xw[15], d1);
-        const float sl0 = bf16_lo(me.x), sh0 = bf16_lo(me.y);
-        const float ml0 = fmaf(-1024.f, sl0, bf16_hi(me.x));
-        const float mh0 = fmaf(-64.f, sh0, bf16_hi(me.y));
-        if constexpr (MODE == kMMA1) {
-          // the first lane of each pair below, alone: the same roundings
-          seg[t][0] = __fmaf_rn(__fmul_rn(sl0, fab.x), d0[0] + d1[0], __fmaf_rn(ml0, Xab.x, seg[t][0]));
-          seg[t][1] = __fmaf_rn(__fmul_rn(sh0, fab16.x), d0[2] + d1[2], __fmaf_rn(mh0, Xab.x, seg[t][1]));
-        } else {
-          float2 lo2 = ffma2(make_float2(ml0, ml0), Xab, make_float2(seg[t][0], seg[t][1]));
-          lo2 = ffma2(fmul2(make_float2(sl0, sl0), fab), make_float2(d0[0] + d1[0], d0[1] + d1[1]), lo2);
-          float2 hi2 = ffma2(make_float2(mh0, mh0), Xab, make_float2(seg[t][2], seg[t][3]));
-          hi2 = ffma2(fmul2(make_float2(sh0, sh0), fab16), make_float2(d0[2] + d1[2], d0[3] + d1[3]), hi2);
-          seg[t][0] = lo2.x;
-          seg[t][1] = lo2.y;
-          seg[t][2] = hi2.x;
-          seg[t][3] = hi2.y;
-        }
+        epilogue(t, me, d0, d1);
       }
     }
   }
@@ -751,7 +828,7 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
       }
       const int ntiles = cc.ntiles;
       const uint8_t* sl = ring + slot * kSlot;
-      compute_chunk<MODE>(sl, sl + kQuadTiles * kBlockBytes, ntiles, lane, seg);
+      compute_chunk<MODE, MODE == kMMA ? 1 : 0>(sl, sl + kQuadTiles * kBlockBytes, ntiles, lane, seg);
 
       // Slot consumed: refill it with the chunk D ahead.
       __syncwarp();
@@ -1145,6 +1222,7 @@ __global__ void __launch_bounds__(32) prep1_kernel(const __grid_constant__ Strea
 constexpr int kLocalMaxEntries = 8;                       // matrices one CTA's range may touch
 constexpr int kLocalSlot = kQuadTiles * kBlockBytes;      // ring slot: weights only (4352 bytes)
 constexpr int kLocalSlots = 2 * kNW;                      // ring slots per CTA: 2 per warp at 16 warps
+constexpr int kWideWarps = 12;                            // at most this many warps per CTA: the 168-register form
 constexpr int kLocalBarBytes = 512;                       // ring mbarriers (32 x 8)
 constexpr int kLocalRing = kLocalSlots * kLocalSlot;      // slot d of warp w at (d * warps + w)
 constexpr int kLocalDyn = 232448 - 4096;                  // dynamic shared memory (static use stays below 4 KB)
@@ -1289,9 +1367,12 @@ struct LocalFold {
 };
 
 // 120 registers (no spills), as the prep-kernel M = 1 path: 512 threads fit,
-// with registers left for fold1_kernel's small CTAs beside them.
-template <int MAXMAT, bool NORM>
-__global__ void __maxnreg__(120) stream1_local_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
+// with registers left for fold1_kernel's small CTAs beside them.  The WIDE
+// form (CTAs of at most kWideWarps warps: calls too small to give every SM
+// 16 warps) takes 168 registers and interleaves a quad's four tiles, since
+// there a warp is often alone on its scheduler.
+template <int MAXMAT, bool NORM, bool WIDE>
+__global__ void __maxnreg__(WIDE ? 168 : 120) stream1_local_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int NA = Acc<kMMA1>::kN;
   __shared__ LocalEntry tbl[kLocalMaxEntries];
@@ -1433,7 +1514,7 @@ __global__ void __maxnreg__(120) stream1_local_kernel(const __grid_constant__ St
       }
       const int ntiles = cc.ntiles;
       const uint8_t* sl = smem + kLocalBarBytes + (slot * cw + warp) * kLocalSlot;
-      compute_chunk<kMMA1>(sl, cc.xsrc, ntiles, lane, seg);
+      compute_chunk<kMMA1, WIDE ? 2 : 0>(sl, cc.xsrc, ntiles, lane, seg);
       __syncwarp();
       if (ic.item < it_b) {
         if (lane == 0) {
@@ -1951,12 +2032,14 @@ void setup_local() {
   cudaFuncSetAttribute(fold1_kernel<kFewMatrices, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFoldSmem);
   cudaFuncSetAttribute(fold1_kernel<W4G128_MAX_MATRICES, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        kFoldSmem);
-  cudaFuncSetAttribute(stream1_local_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalDyn);
-  cudaFuncSetAttribute(stream1_local_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalDyn);
-  cudaFuncSetAttribute(stream1_local_kernel<kFewMatrices, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaFuncSetAttribute(stream1_local_kernel<1, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalDyn);
+  cudaFuncSetAttribute(stream1_local_kernel<1, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalDyn);
+  cudaFuncSetAttribute(stream1_local_kernel<1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalDyn);
+  cudaFuncSetAttribute(stream1_local_kernel<1, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalDyn);
+  cudaFuncSetAttribute(stream1_local_kernel<kFewMatrices, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        kLocalDyn);
-  cudaFuncSetAttribute(stream1_local_kernel<W4G128_MAX_MATRICES, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       kLocalDyn);
+  cudaFuncSetAttribute(stream1_local_kernel<W4G128_MAX_MATRICES, false, false>,
+                       cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalDyn);
 }
 
 template <int MODE>
@@ -2167,7 +2250,7 @@ void fill_params(StreamParams<MAXMAT>& sp, const HostMatrix* mats, int count, in
 // M = 1 with CTA-local packages: the streaming kernel (a programmatic
 // dependent of whatever precedes it), the boundary fold behind it when there
 // is more than one CTA, and the norm behind that.
-template <int MAXMAT, bool NORM>
+template <int MAXMAT, bool NORM, bool WIDE>
 int launch_local(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -2179,7 +2262,7 @@ int launch_local(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, cudaSt
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(cta_warps * 32);
   cfg.dynamicSmemBytes = kLocalDyn;
-  if (cudaLaunchKernelEx(&cfg, stream1_local_kernel<MAXMAT, NORM>, sp) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, stream1_local_kernel<MAXMAT, NORM, WIDE>, sp) != cudaSuccess) {
     cudaGetLastError();
     return W4G128_ERR_CUDA;
   }
@@ -2289,9 +2372,13 @@ int launch_with(const HostMatrix* mats, int count, int M, const Plan& pl, const 
   if (pl.local && x_aligned(mats, count)) {
     sp.depth = pl.local_depth;
     if constexpr (MAXMAT == 1) {
-      if (norm != nullptr) return launch_local<1, true>(sp, pl.grid, pl.cta_warps, stream);
+      if (pl.cta_warps <= kWideWarps) {
+        if (norm != nullptr) return launch_local<1, true, true>(sp, pl.grid, pl.cta_warps, stream);
+        return launch_local<1, false, true>(sp, pl.grid, pl.cta_warps, stream);
+      }
+      if (norm != nullptr) return launch_local<1, true, false>(sp, pl.grid, pl.cta_warps, stream);
     }
-    return launch_local<MAXMAT, false>(sp, pl.grid, pl.cta_warps, stream);
+    return launch_local<MAXMAT, false, false>(sp, pl.grid, pl.cta_warps, stream);
   }
   if constexpr (MAXMAT == 1) {
     if (norm != nullptr) {
