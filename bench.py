@@ -12,8 +12,9 @@ min = -8 scale (1 + U(-0.1, 0.1)), x ~ N(0, 1)).
 Before timing, sampled outputs of both M = 1 and M = 8 are checked against the
 fp64 oracle; a mismatch voids the run (exit status 1, no number printed).
 
-`--target layer|lm_head` instead runs a few untimed calls of one workload
-and exits: the launch target for profiler captures (no JSON line).
+`--target layer|lm_head|single` instead runs a few untimed calls of one
+workload (`single`: the matrix `--shape K,N`) and exits: the launch target
+for profiler captures (no JSON line).
 
 Prints ONE JSON line.  `--impl reference` times the fp64 CPU oracle instead
 (the reference arm: the plain dequantise-then-multiply definition on the host
@@ -768,8 +769,10 @@ def record(args, out):
 
 def run_target(args):
     """Untimed calls of one workload for a profiler to capture: the layer set
-    through w4g128_decode_step, or the 5120 x 248320 lm_head through
-    w4g128_gemv (M = 1) / w4g128_gemm_verify (M > 1); each M in --m in turn."""
+    through w4g128_decode_step, or one matrix (the 5120 x 248320 lm_head, or
+    --shape K,N) through w4g128_gemv (M = 1) / w4g128_gemm_verify (M > 1);
+    each M in --m in turn.  Single matrices rotate over enough copies to
+    exceed twice the L2, as in the timed run."""
     import numpy as np
     import torch
 
@@ -777,7 +780,13 @@ def run_target(args):
     import synth
 
     st = torch.cuda.current_stream().cuda_stream
-    shapes = [(K, N) for _, K, N in LAYER] if args.target == "layer" else [(5120, 248320)]
+    if args.target == "layer":
+        shapes = [(K, N) for _, K, N in LAYER]
+    elif args.target == "single":
+        K, N = (int(v) for v in args.shape.split(","))
+        shapes = [(K, N)]
+    else:
+        shapes = [(5120, 248320)]
     packed = []
     for i, (K, N) in enumerate(shapes):
         codes = torch.empty((K // 8) * N, dtype=torch.int32, device="cuda")
@@ -798,12 +807,15 @@ def run_target(args):
                 w.w4g128_decode_step(descs, M, ws, stream=st)
         else:
             (pk, x, y, K, N), = descs
+            ncopy = max(1, -(-2 * L2_BYTES // weight_bytes(K, N)))
+            mats = [pk] + [pk.clone() for _ in range(ncopy - 1)]
             ws = torch.empty(w.w4g128_workspace_bytes(M, K, N), dtype=torch.uint8, device="cuda")
-            for _ in range(args.calls):
+            for c in range(args.calls):
                 if M == 1:
-                    w.w4g128_gemv(pk, x, y, K, N, ws, stream=st)
+                    w.w4g128_gemv(mats[c % ncopy], x, y, K, N, ws, stream=st)
                 else:
-                    w.w4g128_gemm_verify(pk, x, y, M, K, N, ws, stream=st)
+                    w.w4g128_gemm_verify(mats[c % ncopy], x, y, M, K, N, ws, stream=st)
+            del mats
         torch.cuda.synchronize()
         if w.w4g128_workspace_status(ws, st) != 0:
             print("device status word set", file=sys.stderr)
@@ -821,7 +833,8 @@ def main():
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of identical untimed steps before timing")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--target", choices=["layer", "lm_head"], help="profiler target: untimed calls, no JSON")
+    ap.add_argument("--target", choices=["layer", "lm_head", "single"], help="profiler target: untimed calls, no JSON")
+    ap.add_argument("--shape", default="4096,4096", help="with --target single: K,N of the matrix")
     ap.add_argument("--m", default="1", help="with --target: comma-separated M values")
     ap.add_argument("--calls", type=int, default=2, help="with --target: calls per M")
     ap.add_argument("--record", default=None, help="append the JSON line to DIR/<date>-<host>/bench.jsonl")

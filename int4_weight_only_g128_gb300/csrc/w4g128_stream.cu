@@ -506,8 +506,8 @@ template <int MODE> struct Acc {
 
 // One chunk: every tile of the quad for one group (weights in the ring slot
 // sl, the group's activation package at pk), added into seg[t][*].
-// ILP (M <= 8): 0 -- tile by tile; 1 -- a whole quad's tiles in pairs, both
-// tiles' MMAs interleaved; 2 -- all four tiles interleaved.  Each
+// ILP: 0 -- tile by tile; 1 -- a whole quad's tiles in pairs, both tiles'
+// MMAs interleaved; 2 (M <= 8) -- all four tiles interleaved.  Each
 // accumulator receives the same MMAs in the same order in every form: the
 // same bits; the interleaved forms hold more registers and keep a warp that
 // is alone on its scheduler from waiting on one tile's dependent chain.
@@ -537,6 +537,63 @@ __device__ __forceinline__ void compute_chunk(const uint8_t* sl, const uint8_t* 
     const float* tl = reinterpret_cast<const float*>(pk + Pkg<MODE>::kRows * Pkg<MODE>::kRowBytes);
     const float4 xq0 = *reinterpret_cast<const float4*>(tl + 4 * c);
     const float4 xq1 = *reinterpret_cast<const float4*>(tl + 16 + 4 * c);
+    // tile t's scale/min epilogue of one 8-row half (accumulator chains a, b)
+    auto epilogue = [&](uint2 me, const float (&a)[4], const float (&b)[4], const float4 xq, float& s0, float& s1,
+                        float& s2, float& s3) {
+      const float sl0 = bf16_lo(me.x), sh0 = bf16_lo(me.y);
+      const float ml0 = fmaf(-1024.f, sl0, bf16_hi(me.x));
+      const float mh0 = fmaf(-64.f, sh0, bf16_hi(me.y));
+      const float2 Xab = make_float2(xq.x, xq.z);
+      const float2 fab = make_float2(xq.y, xq.w);
+      const float2 fab16 = make_float2(xq.y * 0.0625f, xq.w * 0.0625f);
+      float2 lo2 = ffma2(make_float2(ml0, ml0), Xab, make_float2(s0, s1));
+      lo2 = ffma2(fmul2(make_float2(sl0, sl0), fab), make_float2(a[0] + b[0], a[1] + b[1]), lo2);
+      float2 hi2 = ffma2(make_float2(mh0, mh0), Xab, make_float2(s2, s3));
+      hi2 = ffma2(fmul2(make_float2(sh0, sh0), fab16), make_float2(a[2] + b[2], a[3] + b[3]), hi2);
+      s0 = lo2.x;
+      s1 = lo2.y;
+      s2 = hi2.x;
+      s3 = hi2.y;
+    };
+    if (ILP > 0 && ntiles == kQuadTiles) {
+      // A whole quad, tiles in pairs with their MMAs interleaved; every
+      // accumulator receives the same MMAs in the same order as below.
+#pragma unroll
+      for (int t = 0; t < kQuadTiles; t += 2) {
+        const uint8_t* blk = sl + t * kBlockBytes;
+        const uint4 a0 = *reinterpret_cast<const uint4*>(blk + 16 * lane);
+        const uint4 a1 = *reinterpret_cast<const uint4*>(blk + 512 + 16 * lane);
+        const uint2 ma = *reinterpret_cast<const uint2*>(blk + kCodeBytes + 8 * r);
+        const uint4 b0 = *reinterpret_cast<const uint4*>(blk + kBlockBytes + 16 * lane);
+        const uint4 b1 = *reinterpret_cast<const uint4*>(blk + kBlockBytes + 512 + 16 * lane);
+        const uint2 mb = *reinterpret_cast<const uint2*>(blk + kBlockBytes + kCodeBytes + 8 * r);
+        float da0[4] = {0.f, 0.f, 0.f, 0.f}, da1[4] = {0.f, 0.f, 0.f, 0.f};
+        float ea0[4] = {0.f, 0.f, 0.f, 0.f}, ea1[4] = {0.f, 0.f, 0.f, 0.f};
+        float db0[4] = {0.f, 0.f, 0.f, 0.f}, db1[4] = {0.f, 0.f, 0.f, 0.f};
+        float eb0[4] = {0.f, 0.f, 0.f, 0.f}, eb1[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_word2(a0.x, xw[0], xw[1], yw[0], yw[1], da0, ea0);
+        mma_word2(b0.x, xw[0], xw[1], yw[0], yw[1], db0, eb0);
+        mma_word2(a0.y, xw[2], xw[3], yw[2], yw[3], da1, ea1);
+        mma_word2(b0.y, xw[2], xw[3], yw[2], yw[3], db1, eb1);
+        mma_word2(a0.z, xw[4], xw[5], yw[4], yw[5], da0, ea0);
+        mma_word2(b0.z, xw[4], xw[5], yw[4], yw[5], db0, eb0);
+        mma_word2(a0.w, xw[6], xw[7], yw[6], yw[7], da1, ea1);
+        mma_word2(b0.w, xw[6], xw[7], yw[6], yw[7], db1, eb1);
+        mma_word2(a1.x, xw[8], xw[9], yw[8], yw[9], da0, ea0);
+        mma_word2(b1.x, xw[8], xw[9], yw[8], yw[9], db0, eb0);
+        mma_word2(a1.y, xw[10], xw[11], yw[10], yw[11], da1, ea1);
+        mma_word2(b1.y, xw[10], xw[11], yw[10], yw[11], db1, eb1);
+        mma_word2(a1.z, xw[12], xw[13], yw[12], yw[13], da0, ea0);
+        mma_word2(b1.z, xw[12], xw[13], yw[12], yw[13], db0, eb0);
+        mma_word2(a1.w, xw[14], xw[15], yw[14], yw[15], da1, ea1);
+        mma_word2(b1.w, xw[14], xw[15], yw[14], yw[15], db1, eb1);
+        epilogue(ma, da0, da1, xq0, seg[t][0], seg[t][1], seg[t][2], seg[t][3]);
+        epilogue(ma, ea0, ea1, xq1, seg[t][4], seg[t][5], seg[t][6], seg[t][7]);
+        epilogue(mb, db0, db1, xq0, seg[t + 1][0], seg[t + 1][1], seg[t + 1][2], seg[t + 1][3]);
+        epilogue(mb, eb0, eb1, xq1, seg[t + 1][4], seg[t + 1][5], seg[t + 1][6], seg[t + 1][7]);
+      }
+      return;
+    }
 #pragma unroll
     for (int t = 0; t < kQuadTiles; ++t) {
       if (t < ntiles) {
@@ -554,25 +611,8 @@ __device__ __forceinline__ void compute_chunk(const uint8_t* sl, const uint8_t* 
         mma_word2(u1.y, xw[10], xw[11], yw[10], yw[11], d1, e1);
         mma_word2(u1.z, xw[12], xw[13], yw[12], yw[13], d0, e0);
         mma_word2(u1.w, xw[14], xw[15], yw[14], yw[15], d1, e1);
-        const float sl0 = bf16_lo(me.x), sh0 = bf16_lo(me.y);
-        const float ml0 = fmaf(-1024.f, sl0, bf16_hi(me.x));
-        const float mh0 = fmaf(-64.f, sh0, bf16_hi(me.y));
-        auto epilogue = [&](const float (&a)[4], const float (&b)[4], const float4 xq, float& s0, float& s1,
-                            float& s2, float& s3) {
-          const float2 Xab = make_float2(xq.x, xq.z);
-          const float2 fab = make_float2(xq.y, xq.w);
-          const float2 fab16 = make_float2(xq.y * 0.0625f, xq.w * 0.0625f);
-          float2 lo2 = ffma2(make_float2(ml0, ml0), Xab, make_float2(s0, s1));
-          lo2 = ffma2(fmul2(make_float2(sl0, sl0), fab), make_float2(a[0] + b[0], a[1] + b[1]), lo2);
-          float2 hi2 = ffma2(make_float2(mh0, mh0), Xab, make_float2(s2, s3));
-          hi2 = ffma2(fmul2(make_float2(sh0, sh0), fab16), make_float2(a[2] + b[2], a[3] + b[3]), hi2);
-          s0 = lo2.x;
-          s1 = lo2.y;
-          s2 = hi2.x;
-          s3 = hi2.y;
-        };
-        epilogue(d0, d1, xq0, seg[t][0], seg[t][1], seg[t][2], seg[t][3]);
-        epilogue(e0, e1, xq1, seg[t][4], seg[t][5], seg[t][6], seg[t][7]);
+        epilogue(me, d0, d1, xq0, seg[t][0], seg[t][1], seg[t][2], seg[t][3]);
+        epilogue(me, e0, e1, xq1, seg[t][4], seg[t][5], seg[t][6], seg[t][7]);
       }
     }
   } else {
@@ -828,7 +868,7 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
       }
       const int ntiles = cc.ntiles;
       const uint8_t* sl = ring + slot * kSlot;
-      compute_chunk<MODE, MODE == kMMA ? 1 : 0>(sl, sl + kQuadTiles * kBlockBytes, ntiles, lane, seg);
+      compute_chunk<MODE, MODE == kMMA1 ? 0 : 1>(sl, sl + kQuadTiles * kBlockBytes, ntiles, lane, seg);
 
       // Slot consumed: refill it with the chunk D ahead.
       __syncwarp();
