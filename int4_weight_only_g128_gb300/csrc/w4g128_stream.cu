@@ -287,7 +287,8 @@ __device__ __forceinline__ void cursor_seek(Cursor& c, const StreamParams<MAXMAT
   cursor_load<MODE>(c, p, lo);
   const long long local = item - mat(p, lo).item_begin;
   c.item = item;
-  c.q = static_cast<int>(local / c.S);
+  c.q = local < (1ll << 31) ? static_cast<int>(static_cast<unsigned>(local) / static_cast<unsigned>(c.S))
+                            : static_cast<int>(local / c.S);
   c.s = static_cast<int>(local - static_cast<long long>(c.q) * c.S);
   c.g = c.s * kSegGroups;
   c.g_end = min(c.g + kSegGroups, c.G);
@@ -342,9 +343,23 @@ __device__ __forceinline__ unsigned ticket_acq_rel(unsigned* t) {
   return prev;
 }
 
+// floor(I w / W) for 0 <= w <= W, the first item of warp w under the
+// balanced split: in 32-bit arithmetic when I W fits (any call short of
+// about 1.7 million items at 2432 warps), since a 64-bit division is a
+// long instruction sequence on the path to a warp's first copy.
+__device__ __forceinline__ long long split_at(long long I, long long w, int W) {
+  if (w >= W) return I;
+  if (I * W < (1ll << 32))
+    return static_cast<long long>(static_cast<unsigned>(I * w) / static_cast<unsigned>(W));
+  return I * w / W;
+}
+
 // Owner warp of an item under the balanced split [floor(wI/W), floor((w+1)I/W)).
 __device__ __forceinline__ int owner_of(long long item, long long I, int W) {
-  return static_cast<int>(((item + 1) * W + I - 1) / I) - 1;
+  const long long n = (item + 1) * W + I - 1;
+  if (n < (1ll << 32) && I < (1ll << 32))
+    return static_cast<int>(static_cast<unsigned>(n) / static_cast<unsigned>(I)) - 1;
+  return static_cast<int>(n / I) - 1;
 }
 
 // ----------------------------------------------------------------- chunk copy
@@ -774,7 +789,7 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
   }
 
   const long long I = p.total_items;
-  const long long it_a = I * wg / p.W, it_b = I * (wg + 1) / p.W;
+  const long long it_a = split_at(I, wg, p.W), it_b = split_at(I, wg + 1, p.W);
   // A warp's contiguous range holds at most two split quads (its first and its
   // last); their tickets are taken after the stream, so no ticket stalls it.
   int pend_q0 = 0, pend_q1 = 0;  // global quad indices
@@ -1430,8 +1445,8 @@ __global__ void __maxnreg__(WIDE ? 168 : 120) stream1_local_kernel(const __grid_
   const int wg = blockIdx.x * cw + warp;
   const long long I = p.total_items;
   const int wl = min((static_cast<int>(blockIdx.x) + 1) * cw, p.W);
-  const long long A = I * (static_cast<long long>(blockIdx.x) * cw) / p.W;
-  const long long B = I * wl / p.W;
+  const long long A = split_at(I, static_cast<long long>(blockIdx.x) * cw, p.W);
+  const long long B = split_at(I, wl, p.W);
   const uint32_t bars = smem_addr(smem);
   const uint32_t ring0 = bars + kLocalBarBytes;
   uint8_t* const pkg_area = smem + p.local_pkg_off;
@@ -1469,7 +1484,7 @@ __global__ void __maxnreg__(WIDE ? 168 : 120) stream1_local_kernel(const __grid_
     return pkg_area + static_cast<long long>(e.pkg + g - e.g_lo) * kPkg1;
   };
 
-  const long long it_a = I * wg / p.W, it_b = I * (wg + 1) / p.W;
+  const long long it_a = split_at(I, wg, p.W), it_b = split_at(I, wg + 1, p.W);
   const bool streams = wg < p.W;
   uint64_t pol_w = 0;
   Cursor cc, ic;
@@ -1628,7 +1643,7 @@ __global__ void __maxnreg__(WIDE ? 168 : 120) stream1_local_kernel(const __grid_
             // range (fold it to y), or the CTA's last item inside a quad that
             // continues in the next CTA (fold the CTA's share to one global slot)
             if (lane == 0) {
-              const long long first = I * (owner_of(q_first, I, p.W) + 1) / p.W - 1;
+              const long long first = split_at(I, owner_of(q_first, I, p.W) + 1, p.W) - 1;
               LocalFold& f = folds[atomicAdd(&fold_n, 1)];
               const bool inner = cc.s == S - 1;
               f.first = first - A;
@@ -1693,8 +1708,8 @@ __global__ void __launch_bounds__(32) fold1_kernel(const __grid_constant__ Strea
   grid_dependents_launch();
   const int cb = blockIdx.x + 1;
   const long long I = p.total_items;
-  const long long Ac = I * (static_cast<long long>(cb) * p.cta_warps) / p.W;
-  const long long Ap = I * (static_cast<long long>(cb - 1) * p.cta_warps) / p.W;
+  const long long Ac = split_at(I, min(static_cast<long long>(cb) * p.cta_warps, static_cast<long long>(p.W)), p.W);
+  const long long Ap = split_at(I, static_cast<long long>(cb - 1) * p.cta_warps, p.W);
   int lo = 0;
   if constexpr (MAXMAT > 1) {
     int hi = p.count - 1;
