@@ -66,6 +66,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <mutex>
 #include <vector>
 
@@ -207,6 +208,15 @@ __host__ __device__ constexpr unsigned long long split_rec(bool split, int mi, i
 }
 static_assert(W4G128_MAX_MATRICES <= 512, "9 bits of matrix index in a split-quad record");
 
+// Calls of up to kFewMatrices matrices (a decoder layer's projections) use a
+// kernel whose parameter block holds that many descriptors: about 0.6 KB
+// instead of 28 KB to copy per launch, and the constant cache keeps all of it.
+constexpr int kFewMatrices = 8;
+
+// Local calls of up to kFewMatrices matrices take their CTAs' item ranges
+// from a table the host computes; it holds up to kMaxLocalCtas CTAs.
+constexpr int kMaxLocalCtas = 192;
+
 template <int MAXMAT>
 struct StreamParams {
   long long total_items;
@@ -228,15 +238,14 @@ struct StreamParams {
   int cta_warps;         // warps per streaming CTA
   int local_pkg_off;     // M = 1 with CTA-local packages: shared-memory offsets of the package area
   int local_part_off;    //   and of the partial-slot area
+  // local calls of up to kFewMatrices matrices: CTA c streams items
+  // [cta_begin[c], cta_begin[c + 1]), split evenly over its warps
+  long long cta_begin[MAXMAT <= kFewMatrices ? kMaxLocalCtas + 1 : 1];
   MatParams mats[MAXMAT];
 };
 
 static_assert(sizeof(StreamParams<W4G128_MAX_MATRICES>) <= 32000, "kernel parameter limit");
 
-// Calls of up to kFewMatrices matrices (a decoder layer's projections) use a
-// kernel whose parameter block holds that many descriptors: about 0.6 KB
-// instead of 28 KB to copy per launch, and the constant cache keeps all of it.
-constexpr int kFewMatrices = 8;
 
 // A matrix of the call.  With one matrix the index is the constant 0, so every
 // read of its descriptor is at a fixed offset of the kernel parameters: those
@@ -1444,9 +1453,31 @@ __global__ void __maxnreg__(WIDE ? 168 : 120) stream1_local_kernel(const __grid_
   const int D = p.depth;
   const int wg = blockIdx.x * cw + warp;
   const long long I = p.total_items;
-  const int wl = min((static_cast<int>(blockIdx.x) + 1) * cw, p.W);
-  const long long A = split_at(I, static_cast<long long>(blockIdx.x) * cw, p.W);
-  const long long B = split_at(I, wl, p.W);
+  // The CTA's items [A, B): from the host's table (calls of up to
+  // kFewMatrices matrices), else the balanced split.
+  long long A, B;
+  if constexpr (MAXMAT <= kFewMatrices) {
+    A = p.cta_begin[blockIdx.x];
+    B = p.cta_begin[blockIdx.x + 1];
+  } else {
+    A = split_at(I, static_cast<long long>(blockIdx.x) * cw, p.W);
+    B = split_at(I, min((static_cast<int>(blockIdx.x) + 1) * cw, p.W), p.W);
+  }
+  // With the table, warp w of the CTA streams [A + n w / cw, A + n (w + 1) / cw),
+  // n = B - A; the last item of the warp that holds item i of [A, B):
+  const unsigned n_cta = static_cast<unsigned>(B - A);
+  auto warp_first = [&](int w) -> long long {
+    if constexpr (MAXMAT <= kFewMatrices) return A + static_cast<long long>(n_cta * static_cast<unsigned>(w) / cw);
+    else return split_at(I, static_cast<long long>(blockIdx.x) * cw + w, p.W);
+  };
+  auto owner_last = [&](long long i) -> long long {
+    if constexpr (MAXMAT <= kFewMatrices) {
+      const int wo = static_cast<int>((static_cast<unsigned>(i - A + 1) * cw - 1u) / n_cta);
+      return warp_first(wo + 1) - 1;
+    } else {
+      return split_at(I, owner_of(i, I, p.W) + 1, p.W) - 1;
+    }
+  };
   const uint32_t bars = smem_addr(smem);
   const uint32_t ring0 = bars + kLocalBarBytes;
   uint8_t* const pkg_area = smem + p.local_pkg_off;
@@ -1468,6 +1499,7 @@ __global__ void __maxnreg__(WIDE ? 168 : 120) stream1_local_kernel(const __grid_
   // (the same table function); a CTA that does not fit records the error and
   // touches nothing.
   if (tbl_n <= 0 || p.M != 1 || p.local_pkg_off != kLocalBarBytes + kLocalRing || D < 2 || D * cw > kLocalSlots ||
+      A < 0 || B < A || B > I || (B - A) * cw >= (1ll << 31) ||
       p.local_pkg_off + static_cast<long long>(tbl_npkg) * kPkg1 > p.local_part_off ||
       p.local_part_off + (B - A) * 64 * 4 > kLocalDyn) {
     if (threadIdx.x == 0) status_fail(p.status, W4G128_ERR_INTERNAL);
@@ -1484,8 +1516,8 @@ __global__ void __maxnreg__(WIDE ? 168 : 120) stream1_local_kernel(const __grid_
     return pkg_area + static_cast<long long>(e.pkg + g - e.g_lo) * kPkg1;
   };
 
-  const long long it_a = split_at(I, wg, p.W), it_b = split_at(I, wg + 1, p.W);
-  const bool streams = wg < p.W;
+  const long long it_a = warp_first(warp), it_b = warp_first(warp + 1);
+  const bool streams = (MAXMAT <= kFewMatrices) ? it_a < it_b : wg < p.W;
   uint64_t pol_w = 0;
   Cursor cc, ic;
   unsigned issued = 0u;
@@ -1643,7 +1675,7 @@ __global__ void __maxnreg__(WIDE ? 168 : 120) stream1_local_kernel(const __grid_
             // range (fold it to y), or the CTA's last item inside a quad that
             // continues in the next CTA (fold the CTA's share to one global slot)
             if (lane == 0) {
-              const long long first = split_at(I, owner_of(q_first, I, p.W) + 1, p.W) - 1;
+              const long long first = owner_last(q_first);
               LocalFold& f = folds[atomicAdd(&fold_n, 1)];
               const bool inner = cc.s == S - 1;
               f.first = first - A;
@@ -1708,8 +1740,14 @@ __global__ void __launch_bounds__(32) fold1_kernel(const __grid_constant__ Strea
   grid_dependents_launch();
   const int cb = blockIdx.x + 1;
   const long long I = p.total_items;
-  const long long Ac = split_at(I, min(static_cast<long long>(cb) * p.cta_warps, static_cast<long long>(p.W)), p.W);
-  const long long Ap = split_at(I, static_cast<long long>(cb - 1) * p.cta_warps, p.W);
+  long long Ac, Ap;
+  if constexpr (MAXMAT <= kFewMatrices) {
+    Ac = p.cta_begin[cb];
+    Ap = p.cta_begin[cb - 1];
+  } else {
+    Ac = split_at(I, min(static_cast<long long>(cb) * p.cta_warps, static_cast<long long>(p.W)), p.W);
+    Ap = split_at(I, static_cast<long long>(cb - 1) * p.cta_warps, p.W);
+  }
   int lo = 0;
   if constexpr (MAXMAT > 1) {
     int hi = p.count - 1;
@@ -2178,6 +2216,7 @@ struct Plan {
   size_t off_tickets = 0, off_recs = 0, off_xpkg = 0, off_partials = 0, bytes = 0;
   std::vector<long long> item_begin, xpkg_off;
   std::vector<int> quad_begin, g_begin;
+  std::vector<long long> cta_begin;  // local calls of 2..kFewMatrices matrices: the CTAs' first items
 };
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -2228,6 +2267,16 @@ bool make_plan(const HostMatrix* mats, int count, int M, const DeviceInfo& dev, 
   pl.per_warp_reduce = M >= 2 && pl.total_quads > pl.W &&
                        static_cast<long long>(pl.total_quads) > static_cast<long long>(dev.red_occ[M]) * dev.sms;
 
+  // Local calls of up to kFewMatrices matrices take the CTAs' item ranges
+  // from a table in the kernel parameters (the balanced split), which each
+  // CTA reads before its dependency wait instead of deriving it.
+  const bool cta_table = pl.mode == kMMA1 && count <= kFewMatrices;
+  if (cta_table && pl.grid <= kMaxLocalCtas) {
+    pl.cta_begin.resize(pl.grid + 1);
+    for (int c = 0; c <= pl.grid; ++c)
+      pl.cta_begin[c] = items * std::min<long long>(static_cast<long long>(c) * pl.cta_warps, pl.W) / pl.W;
+  }
+
   // M = 1: can every CTA hold its packages and partial slots in shared memory?
   if (pl.mode == kMMA1) {
     struct HostMats {
@@ -2240,9 +2289,11 @@ bool make_plan(const HostMatrix* mats, int count, int M, const DeviceInfo& dev, 
     int pmax = 0;
     long long smax = 0;
     bool ok = true;
+    if (cta_table && pl.cta_begin.empty()) ok = false;  // more CTAs than the table holds
     for (int c = 0; c < pl.grid && ok; ++c) {
-      const long long A = items * (static_cast<long long>(c) * pl.cta_warps) / pl.W;
-      const long long B = items * std::min((c + 1) * pl.cta_warps, pl.W) / pl.W;
+      const long long A = cta_table ? pl.cta_begin[c] : items * (static_cast<long long>(c) * pl.cta_warps) / pl.W;
+      const long long B = cta_table ? pl.cta_begin[c + 1]
+                                    : items * std::min((c + 1) * pl.cta_warps, pl.W) / pl.W;
       LocalEntry t[kLocalMaxEntries];
       int np = 0;
       if (local_table(A, B, count, at, t, np) < 0) ok = false;
@@ -2286,6 +2337,10 @@ void fill_params(StreamParams<MAXMAT>& sp, const HostMatrix* mats, int count, in
   sp.cta_warps = pl.cta_warps;
   sp.local_pkg_off = pl.local_pkg_off;
   sp.local_part_off = pl.local_part_off;
+  if constexpr (MAXMAT <= kFewMatrices) {
+    const int nb = std::min(static_cast<int>(pl.cta_begin.size()), kMaxLocalCtas + 1);
+    for (int c = 0; c < nb; ++c) sp.cta_begin[c] = pl.cta_begin[c];
+  }
   sp.total_quads = pl.total_quads;
   sp.total_groups = pl.total_groups;
   for (int i = 0; i < count; ++i) {
