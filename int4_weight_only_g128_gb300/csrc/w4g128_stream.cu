@@ -766,12 +766,18 @@ __device__ __forceinline__ void compute_chunk(const uint8_t* sl, const uint8_t* 
 
 // ----------------------------------------------------------------- the streaming kernel
 
-template <int MODE, int MAXMAT, bool NORM>
+// CTAs of at most kWideWarps warps (calls too small to give every SM 16
+// warps) run forms of the streaming kernels with 168 registers, which
+// interleave all four tiles of a quad: there a warp is often alone on its
+// scheduler.
+constexpr int kWideWarps = 12;
+
+template <int MODE, int MAXMAT, bool NORM, bool WIDE = false>
 // M = 1 is held to 120 registers (no spills): 4096 of the
 // SM's 65536 registers stay free for the next call's one-warp prep CTAs.
-// M <= 16 (8 warps) may use up to 255.
-__global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
-    __maxnreg__(MODE == kMMA1 ? 120 : (MODE == kMMA16 ? 255 : 128))
+// M <= 16 (8 warps) may use up to 255; the WIDE form of M <= 8 168.
+__global__ void __launch_bounds__((WIDE ? kWideWarps : cta_warps_max<MODE>()) * 32, 1)
+    __maxnreg__(WIDE ? 168 : (MODE == kMMA1 ? 120 : (MODE == kMMA16 ? 255 : 128)))
     stream_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int NA = Acc<MODE>::kN;
@@ -892,7 +898,7 @@ __global__ void __launch_bounds__(cta_warps_max<MODE>() * 32, 1)
       }
       const int ntiles = cc.ntiles;
       const uint8_t* sl = ring + slot * kSlot;
-      compute_chunk<MODE, MODE == kMMA1 ? 0 : 1>(sl, sl + kQuadTiles * kBlockBytes, ntiles, lane, seg);
+      compute_chunk<MODE, MODE == kMMA1 ? 0 : (WIDE ? 2 : 1)>(sl, sl + kQuadTiles * kBlockBytes, ntiles, lane, seg);
 
       // Slot consumed: refill it with the chunk D ahead.
       __syncwarp();
@@ -1286,7 +1292,6 @@ __global__ void __launch_bounds__(32) prep1_kernel(const __grid_constant__ Strea
 constexpr int kLocalMaxEntries = 8;                       // matrices one CTA's range may touch
 constexpr int kLocalSlot = kQuadTiles * kBlockBytes;      // ring slot: weights only (4352 bytes)
 constexpr int kLocalSlots = 2 * kNW;                      // ring slots per CTA: 2 per warp at 16 warps
-constexpr int kWideWarps = 12;                            // at most this many warps per CTA: the 168-register form
 constexpr int kLocalBarBytes = 512;                       // ring mbarriers (32 x 8)
 constexpr int kLocalRing = kLocalSlots * kLocalSlot;      // slot d of warp w at (d * warps + w)
 constexpr int kLocalDyn = 232448 - 4096;                  // dynamic shared memory (static use stays below 4 KB)
@@ -2140,6 +2145,10 @@ void setup_mode(DeviceInfo& d) {
   const int smem = smem_bytes<MODE>();
   cudaFuncSetAttribute(stream_kernel<MODE, 1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   cudaFuncSetAttribute(stream_kernel<MODE, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if constexpr (MODE == kMMA) {
+    cudaFuncSetAttribute(stream_kernel<MODE, 1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncSetAttribute(stream_kernel<MODE, 1, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  }
   cudaFuncSetAttribute(stream_kernel<MODE, kFewMatrices, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   cudaFuncSetAttribute(stream_kernel<MODE, W4G128_MAX_MATRICES, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        smem);
@@ -2432,7 +2441,16 @@ int launch_mode(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, int max
   // call with few warps still spreads over every SM instead of packing two
   // CTAs onto one
   cfg.dynamicSmemBytes = smem_bytes<MODE>();
-  if (cudaLaunchKernelEx(&cfg, stream_kernel<MODE, MAXMAT, NORM>, sp) != cudaSuccess) {
+  bool wide = false;
+  if constexpr (MODE == kMMA && MAXMAT == 1) wide = cta_warps <= kWideWarps;
+  cudaError_t es;
+  if constexpr (MODE == kMMA && MAXMAT == 1) {
+    es = wide ? cudaLaunchKernelEx(&cfg, stream_kernel<MODE, 1, NORM, true>, sp)
+              : cudaLaunchKernelEx(&cfg, stream_kernel<MODE, 1, NORM>, sp);
+  } else {
+    es = cudaLaunchKernelEx(&cfg, stream_kernel<MODE, MAXMAT, NORM>, sp);
+  }
+  if (es != cudaSuccess) {
     cudaGetLastError();
     return W4G128_ERR_CUDA;
   }
