@@ -233,6 +233,8 @@ struct StreamParams {
   float eps;
   int count, M, W, total_quads, total_groups;
   int per_warp_reduce;   // M >= 2: the split quads are folded per streaming warp (else per quad)
+  int red_chunk;         // M >= 2, per-quad fold: partial slots per bulk copy (8 or 16)
+  int red_reverse;       // M >= 2, per-quad fold: fold CTA b takes quad total_quads - 1 - b
   int depth;             // ring slots per warp (ring_depth of the mode)
   unsigned long long wait_ns;  // limit of every device-side wait
   int cta_warps;         // warps per streaming CTA
@@ -1832,13 +1834,20 @@ constexpr int kRedStageBytes = kRedChunk * kMaxRows * 64 * 4;  // the largest st
 constexpr int kRedSmem = 2 * kRedStageBytes + 16;          // two stages + two mbarriers, at most
 // a call's reduce CTAs: 16 M threads (one per row and 4 columns), two stages of M rows
 __host__ __device__ constexpr int red_threads(int M) { return ((16 * M + 31) / 32) * 32; }
-__host__ __device__ constexpr int red_smem(int M) { return 2 * kRedChunk * M * 64 * 4 + 16; }
+__host__ __device__ constexpr int red_smem(int M, int chunk = kRedChunk) { return 2 * chunk * M * 64 * 4 + 16; }
+// Calls whose quads are deeper than kRedChunk segments and whose fold CTAs
+// all fit one wave at the larger stage copy kRedChunkDeep slots at a time
+// (M <= 8; the same shared memory as M = 16 at kRedChunk).
+constexpr int kRedChunkDeep = 16;
+static_assert(red_smem(8, kRedChunkDeep) <= kRedSmem, "deep stages fit the reduce kernel's shared memory");
 
 template <int MAXMAT, bool NORM>
 __global__ void __launch_bounds__(kRedThreads) reduce_quads_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
   extern __shared__ __align__(128) uint8_t rsm[];
   __shared__ int ok;
-  const int gq = blockIdx.x;
+  // deepest quads first when the host says they come last (a layer's down
+  // projection): their folds take the most copy rounds
+  const int gq = p.red_reverse ? p.total_quads - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
   int lo = 0;
   if constexpr (MAXMAT > 1) lo = static_cast<int>(__ldcg(p.tickets + gq));  // written by the prep kernel
   const MatParams& m = mat(p, lo);
@@ -1865,16 +1874,17 @@ __global__ void __launch_bounds__(kRedThreads) reduce_quads_kernel(const __grid_
   }
 
   grid_dependency_wait();  // every partial of the streaming kernel is written and visible
+  const int chunk = p.red_chunk;
   const int per_quad = p.M * 64;  // floats per partial slot
   const uint32_t slot_bytes = static_cast<uint32_t>(per_quad) * 4u;
-  const int stage_floats = kRedChunk * per_quad;
+  const int stage_floats = chunk * per_quad;
   const float* buf = reinterpret_cast<const float*>(rsm);
   const uint32_t buf0 = smem_addr(rsm), bar0 = smem_addr(rsm + 2 * stage_floats * 4);
   const float* src = p.partials + first * per_quad;
-  const int nchunks = div_up(nslot, kRedChunk);
+  const int nchunks = div_up(nslot, chunk);
   uint64_t pol = 0;
   auto issue = [&](int ch) {
-    const int ns = min(kRedChunk, nslot - ch * kRedChunk);
+    const int ns = min(chunk, nslot - ch * chunk);
     const uint32_t bar = bar0 + 8 * (ch & 1);
     mbar_arrive_expect_tx(bar, ns * slot_bytes);
     bulk_g2s(buf0 + (ch & 1) * stage_floats * 4, src + static_cast<long long>(ch) * stage_floats, ns * slot_bytes,
@@ -1911,7 +1921,7 @@ __global__ void __launch_bounds__(kRedThreads) reduce_quads_kernel(const __grid_
     if (!ok) return;
     if (active) {
       const float* b = buf + (ch & 1) * stage_floats + row * 64 + col;
-      const int ns = min(kRedChunk, nslot - ch * kRedChunk);
+      const int ns = min(chunk, nslot - ch * chunk);
       for (int s = 0; s < ns; ++s) {
         const float4 v = *reinterpret_cast<const float4*>(b + s * per_quad);
         if (ch == 0 && s == 0) {
@@ -2117,6 +2127,7 @@ struct DeviceInfo {
   int sms = 0;
   int occ[4] = {0, 0, 0, 0};        // CTAs per SM per mode
   int red_occ[kMaxRows + 1] = {};   // per-quad reduce CTAs per SM per M
+  int red_occ_deep[kMaxRows + 1] = {};  // the same at kRedChunkDeep slots per copy
   bool ok = false;
 };
 
@@ -2194,6 +2205,10 @@ const DeviceInfo* device_info() {
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, reduce_quads_kernel<W4G128_MAX_MATRICES, false>,
                                                       red_threads(M), red_smem(M));
         d.red_occ[M] = n > 0 ? n : 1;
+        n = 0;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, reduce_quads_kernel<W4G128_MAX_MATRICES, false>,
+                                                      red_threads(M), red_smem(M, kRedChunkDeep));
+        d.red_occ_deep[M] = n;
       }
       if (cudaGetLastError() != cudaSuccess) d.ok = false;
     }
@@ -2217,6 +2232,8 @@ void forget_device() {
 struct Plan {
   int mode = 0, rows = 1, pkg = 0, depth = 2;
   bool per_warp_reduce = false;
+  int red_chunk = kRedChunk;  // per-quad fold: slots per bulk copy
+  bool red_reverse = false;   // per-quad fold: deepest (last) quads first
   bool local = false;   // M = 1 with CTA-local packages (when x is 16-byte aligned)
   int local_depth = 2;  // ring slots per warp of a local call
   int local_pkg_off = 0, local_part_off = 0;
@@ -2275,6 +2292,25 @@ bool make_plan(const HostMatrix* mats, int count, int M, const DeviceInfo& dev, 
   // each and than one wave of resident reduce CTAs
   pl.per_warp_reduce = M >= 2 && pl.total_quads > pl.W &&
                        static_cast<long long>(pl.total_quads) > static_cast<long long>(dev.red_occ[M]) * dev.sms;
+  // Per-quad fold: quads deeper than kRedChunk segments are copied
+  // kRedChunkDeep slots at a time when every fold CTA still fits one wave at
+  // that stage size (fewer dependent copy rounds; measured 17408x5120 at
+  // M = 8 18.8 -> 17.4 us, 6144x5120 9.8 -> 9.0 us); a call whose last matrix
+  // is its deepest (a layer: down) folds from the last quad back, so the
+  // longest folds start first (layer step M = 8 43.0 -> 42.5 us, M = 16
+  // 69.8 -> 68.7 us).
+  if (M >= 2 && !pl.per_warp_reduce) {
+    int smax = 0, slast = 0;
+    for (int i = 0; i < count; ++i) {
+      const int S = div_up(mats[i].K / kGroup, kSegGroups);
+      smax = std::max(smax, S);
+      slast = S;
+    }
+    if (M <= 8 && smax > kRedChunk &&
+        static_cast<long long>(pl.total_quads) <= static_cast<long long>(dev.red_occ_deep[M]) * dev.sms)
+      pl.red_chunk = kRedChunkDeep;
+    pl.red_reverse = count > 1 && slast == smax;
+  }
 
   // Local calls of up to kFewMatrices matrices take the CTAs' item ranges
   // from a table in the kernel parameters (the balanced split), which each
@@ -2341,6 +2377,8 @@ void fill_params(StreamParams<MAXMAT>& sp, const HostMatrix* mats, int count, in
   sp.M = M;
   sp.W = pl.W;
   sp.per_warp_reduce = pl.per_warp_reduce ? 1 : 0;
+  sp.red_chunk = pl.red_chunk;
+  sp.red_reverse = pl.red_reverse ? 1 : 0;
   sp.depth = pl.depth;
   sp.wait_ns = kDefaultWaitNs;
   sp.cta_warps = pl.cta_warps;
@@ -2463,7 +2501,7 @@ int launch_mode(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, int max
       er = cudaLaunchKernelEx(&cfg, reduce_warps_kernel<MAXMAT, NORM>, sp);
     } else {
       cfg.gridDim = dim3(static_cast<unsigned>(sp.total_quads));  // one CTA per quad
-      cfg.dynamicSmemBytes = red_smem(sp.M);
+      cfg.dynamicSmemBytes = red_smem(sp.M, sp.red_chunk);
       er = cudaLaunchKernelEx(&cfg, reduce_quads_kernel<MAXMAT, NORM>, sp);
     }
     if (er != cudaSuccess) {
