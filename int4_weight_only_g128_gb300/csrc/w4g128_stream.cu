@@ -1100,6 +1100,10 @@ __global__ void __launch_bounds__((WIDE ? kWideWarps : cta_warps_max<MODE>()) * 
 
 // ----------------------------------------------------------------- prep kernel
 
+// A group of one x row staged in shared memory (272 bytes: the eight lane
+// quads of a warp reading eight staged rows land on distinct banks).
+constexpr int kStageStride = kGroup * 2 + 16;
+
 // Lane class c of one (group, x row) package row, built by four consecutive
 // lanes (lane & ~3 .. + 3, one per class), which agree on the row's scale 2^s
 // from the largest magnitude among their 128 values: x' = x 2^s as fp16 pairs
@@ -1224,14 +1228,40 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Strea
   const int lane = threadIdx.x & 31;
   const int row = lane >> 2, c = lane & 3;
   const int nwarp = blockDim.x >> 5;
-  for (int g = nwarp * blockIdx.x + (threadIdx.x >> 5); g < G; g += nwarp * gridDim.x) {
+  // A warp's group: its M rows of x are staged in shared memory with 16-byte
+  // loads (rows kStageStride bytes apart: the eight lane quads then read
+  // eight rows on distinct banks), then built from there -- the same words
+  // as reading them from global memory one by one, in a quarter of the load
+  // instructions (layer step M = 8 42.6 -> 41.8 us, M = 16 68.9 -> 67.6 us).
+  // x only 4-byte aligned is read directly.
+  __shared__ __align__(16) uint8_t xs[8][kRows][kStageStride];
+  const bool staged = (reinterpret_cast<uintptr_t>(m.x) & 15u) == 0;
+  const int wp = threadIdx.x >> 5;
+  for (int g = nwarp * blockIdx.x + wp; g < G; g += nwarp * gridDim.x) {
     uint8_t* out = m.xpkg + static_cast<long long>(g) * Pkg<MODE>::kBytes;
     float* tail = reinterpret_cast<float*>(out + kRows * Pkg<MODE>::kRowBytes);
+    if (staged) {
+      for (int j = lane; j < p.M * 16; j += 32) {
+        const int rr = j >> 4, part = j & 15;
+        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(m.x + static_cast<long long>(rr) * m.K + kGroup * g) + part);
+        *reinterpret_cast<uint4*>(&xs[wp][rr][part * 16]) = v;
+      }
+      __syncwarp();
 #pragma unroll
-    for (int row8 = 0; row8 < kRows; row8 += 8) {
-      const int rw = row8 + row;
-      build_row_class(rw < p.M ? m.x + static_cast<long long>(rw) * m.K + kGroup * g : nullptr, c, lane,
-                      out + rw * Pkg<MODE>::kRowBytes, tail + 2 * rw);
+      for (int row8 = 0; row8 < kRows; row8 += 8) {
+        const int rw = row8 + row;
+        uint32_t w[16];
+        load_row_class<true>(rw < p.M ? reinterpret_cast<const uint16_t*>(&xs[wp][rw][0]) : nullptr, c, w);
+        finish_row_class(w, c, lane, out + rw * Pkg<MODE>::kRowBytes, tail + 2 * rw);
+      }
+      __syncwarp();  // the rows are read before the next group's overwrite them
+    } else {
+#pragma unroll
+      for (int row8 = 0; row8 < kRows; row8 += 8) {
+        const int rw = row8 + row;
+        build_row_class(rw < p.M ? m.x + static_cast<long long>(rw) * m.K + kGroup * g : nullptr, c, lane,
+                        out + rw * Pkg<MODE>::kRowBytes, tail + 2 * rw);
+      }
     }
   }
 }
@@ -1299,7 +1329,6 @@ constexpr int kLocalRing = kLocalSlots * kLocalSlot;      // slot d of warp w at
 constexpr int kLocalDyn = 232448 - 4096;                  // dynamic shared memory (static use stays below 4 KB)
 constexpr int kLocalSpace = kLocalDyn - kLocalBarBytes - kLocalRing;  // packages + partial slots
 constexpr int kPkg1 = Pkg<kMMA1>::kBytes;                 // one M = 1 package (336 bytes)
-constexpr int kStageStride = kGroup * 2 + 16;             // a staged group of x (272 bytes)
 constexpr int kMaxFoldSlots = 65536 / (kGroup * kSegGroups) + 1;  // slots of one boundary fold, at most
 constexpr int kFoldSmem = kMaxFoldSlots * 64 * 4 + 16;    // fold1_kernel: the slots and an mbarrier
 static_assert(kLocalSpace > 0 && kLocalRing % 128 == 0, "local layout");
