@@ -186,10 +186,15 @@ def measured_peaks():
 
 
 def kernel_source_sha():
+    """Hash of the kernel sources with comments and blank lines removed, so
+    that a comment edit does not invalidate the profiled traffic."""
     h = hashlib.sha256()
     for p in KERNEL_SOURCES:
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p, encoding="utf-8") as f:
+            for line in f:
+                code = line.split("//", 1)[0].strip()
+                if code:
+                    h.update(code.encode("utf-8") + b"\n")
     return h.hexdigest()[:16]
 
 

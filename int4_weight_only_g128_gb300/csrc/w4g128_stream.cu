@@ -1849,13 +1849,16 @@ __global__ void __launch_bounds__(32) fold1_kernel(const __grid_constant__ Strea
 // M >= 2: folds the segment partials of every quad the schedule split between
 // warps.  Two forms; a call takes the one with the smaller grid.
 //
-// Per quad (calls with no more quads than streaming warps): one CTA per quad: the quad's partial slots -- the fold of the
-// segments its first warp held, then one slot per later segment -- are one
-// contiguous run of M x 64 fp32 slots, pulled into shared memory by 1-D bulk
-// copies of up to kRedChunk slots (two stages), and each thread folds one
-// (row, 4 adjacent columns) unit over them in order -- the left fold a single
-// warp would have made.  Quads owned by one warp were written by the streaming
-// kernel; their CTAs exit before waiting for it.
+// Per quad (calls with no more quads than streaming warps): one CTA per
+// quad.  The quad's partial slots -- the fold of the segments its first warp
+// held, then one slot per later segment -- are one contiguous run of M x 64
+// fp32 slots, pulled into shared memory by 1-D bulk copies of up to
+// kRedChunk slots (kRedChunkDeep for calls with deep quads whose fold CTAs
+// fit one wave at that size; two stages), and each thread folds one (row, 4
+// adjacent columns) unit over them in order -- the left fold a single warp
+// would have made.  CTAs take quads from the last back when the call's last
+// matrix is its deepest.  Quads owned by one warp were written by the
+// streaming kernel; their CTAs exit before waiting for it.
 constexpr int kMaxRows = W4G128_MAX_M;
 constexpr int kRedChunk = 8;                               // segments per bulk copy
 constexpr int kRedThreads = kMaxRows * 16;                 // one per (row, 4 columns)
