@@ -2274,7 +2274,8 @@ struct Plan {
   size_t off_tickets = 0, off_recs = 0, off_xpkg = 0, off_partials = 0, bytes = 0;
   std::vector<long long> item_begin, xpkg_off;
   std::vector<int> quad_begin, g_begin;
-  std::vector<long long> cta_begin;  // local calls of 2..kFewMatrices matrices: the CTAs' first items
+  std::vector<long long> cta_begin;  // local calls of up to kFewMatrices matrices: the CTAs' first items
+  bool whole_quads = false;          // M = 1, one matrix: one CTA per quad, no boundary fold
 };
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -2348,6 +2349,22 @@ bool make_plan(const HostMatrix* mats, int count, int M, const DeviceInfo& dev, 
   // from a table in the kernel parameters (the balanced split), which each
   // CTA reads before its dependency wait instead of deriving it.
   const bool cta_table = pl.mode == kMMA1 && count <= kFewMatrices;
+  // A single matrix of between sms / 4 and sms quads of at most
+  // kWholeQuadSegs segments runs one CTA per quad, one warp per segment: no
+  // quad straddles two CTAs, so the boundary fold kernel is not launched
+  // (measured: 4096^2 6.8 -> 6.5 us, 5120x6144 8.8 -> 8.1 us; at 12 segments,
+  // 6144x5120, the larger per-SM share cancels the gain).
+  constexpr int kWholeQuadSegs = 10;
+  if (cta_table && count == 1) {
+    const int S1 = div_up(mats[0].K / kGroup, kSegGroups);
+    const int NQ1 = div_up(mats[0].N, kTileN * kQuadTiles);
+    if (S1 <= kWholeQuadSegs && NQ1 <= dev.sms && 4 * NQ1 >= dev.sms) {
+      pl.grid = NQ1;
+      pl.cta_warps = S1;
+      pl.W = NQ1 * S1;
+      pl.whole_quads = true;
+    }
+  }
   if (cta_table && pl.grid <= kMaxLocalCtas) {
     pl.cta_begin.resize(pl.grid + 1);
     for (int c = 0; c <= pl.grid; ++c)
@@ -2437,10 +2454,10 @@ void fill_params(StreamParams<MAXMAT>& sp, const HostMatrix* mats, int count, in
 }
 
 // M = 1 with CTA-local packages: the streaming kernel (a programmatic
-// dependent of whatever precedes it), the boundary fold behind it when there
-// is more than one CTA, and the norm behind that.
+// dependent of whatever precedes it), the boundary fold behind it when CTA
+// boundaries can split quads, and the norm behind that.
 template <int MAXMAT, bool NORM, bool WIDE>
-int launch_local(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, cudaStream_t stream) {
+int launch_local(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, bool boundary_fold, cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -2455,7 +2472,7 @@ int launch_local(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, cudaSt
     cudaGetLastError();
     return W4G128_ERR_CUDA;
   }
-  if (grid > 1) {
+  if (grid > 1 && boundary_fold) {
     cfg.gridDim = dim3(grid - 1);
     cfg.blockDim = dim3(32);
     cfg.dynamicSmemBytes = kFoldSmem;
@@ -2571,12 +2588,12 @@ int launch_with(const HostMatrix* mats, int count, int M, const Plan& pl, const 
     sp.depth = pl.local_depth;
     if constexpr (MAXMAT == 1) {
       if (pl.cta_warps <= kWideWarps) {
-        if (norm != nullptr) return launch_local<1, true, true>(sp, pl.grid, pl.cta_warps, stream);
-        return launch_local<1, false, true>(sp, pl.grid, pl.cta_warps, stream);
+        if (norm != nullptr) return launch_local<1, true, true>(sp, pl.grid, pl.cta_warps, !pl.whole_quads, stream);
+        return launch_local<1, false, true>(sp, pl.grid, pl.cta_warps, !pl.whole_quads, stream);
       }
-      if (norm != nullptr) return launch_local<1, true, false>(sp, pl.grid, pl.cta_warps, stream);
+      if (norm != nullptr) return launch_local<1, true, false>(sp, pl.grid, pl.cta_warps, !pl.whole_quads, stream);
     }
-    return launch_local<MAXMAT, false, false>(sp, pl.grid, pl.cta_warps, stream);
+    return launch_local<MAXMAT, false, false>(sp, pl.grid, pl.cta_warps, !pl.whole_quads, stream);
   }
   if constexpr (MAXMAT == 1) {
     if (norm != nullptr) {
