@@ -9,8 +9,11 @@
 //    previous kernel has finished (that kernel may still read the old x);
 //  * download: once the step's last kernel has finished, copies y to host
 //    memory with 16-byte stores.
-// Each thread moves 16 bytes per iteration; one CTA of 256 threads per 64 KB
-// at most, up to one per SM.
+// One CTA of 256 threads per 4 KB (one 16-byte unit per thread), up to one
+// per SM; beyond that each thread moves further units.  Spreading the bytes
+// over more CTAs shortens both moves: every thread's host access is a full
+// round trip over the chip-to-host link, so fewer accesses per thread means
+// less latency on the step's critical path.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -66,7 +69,7 @@ int launch_io(bool up, const void* src, void* dst, size_t bytes, cudaStream_t st
     cudaGetLastError();
     return W4G128_ERR_CUDA;
   }
-  const size_t per_cta = static_cast<size_t>(kIoThreads) * 4;  // 16 KB per CTA before a CTA takes more
+  const size_t per_cta = kIoThreads;  // 4 KB per CTA before a CTA takes more
   const unsigned grid = static_cast<unsigned>(std::max<size_t>(1, std::min<size_t>(sms, (n16 + per_cta - 1) / per_cta)));
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -138,3 +138,39 @@ def test_decode_step_host_buffers(M, pinned):
         expect = decode_step(mats, [to_dev(x) for x in xh], M)
         for i in range(len(shapes)):
             assert np.array_equal(got[yoff[i]:yoff[i + 1]].reshape(M, -1), expect[i])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("units", [5, 256 * 152 + 1, 256 * 152 * 16 + 3, 256 * 152 * 16 * 2 + 256 * 7 + 9])
+def test_decode_step_host_moves_whole_ranges(units):
+    """The upload and download kernels move every 16-byte unit of the ranges
+    they are given, whatever the count: part of one CTA, just over one unit
+    per thread on every SM, and over one and two rounds of the loads each
+    thread keeps in flight.  The x range holds (the start of) one matrix's x
+    and arbitrary bytes after it; the y range holds that matrix's y and bytes
+    the step does not write.  After the call x_dev equals x_host and y_host
+    equals y_dev over the whole ranges, and the matrix's y is the plain step's."""
+    K, N, M = 640, 80, 1
+    mat = DevMatrix(K, N, matrix_id=1400)
+    nx = units * 8  # int16 elements, 16 bytes a unit
+    ny = max(units * 8, M * N)
+    ny += (-ny) % 8
+    rng = np.random.default_rng(units)
+    x_host = torch.from_numpy(rng.integers(-2**15, 2**15, nx, dtype=np.int16)).pin_memory()
+    xh = synth.x(SEED, 1401, M, K).ravel().view(np.int16)
+    head = min(nx, M * K)  # the tiny range covers only the start of x; the rest of x_dev stays zero
+    x_host[:head].copy_(torch.from_numpy(xh[:head]))
+    y_fill = rng.integers(-2**15, 2**15, ny, dtype=np.int16)
+    y_dev = torch.from_numpy(y_fill).cuda()
+    x_dev = torch.zeros(max(nx, M * K), dtype=torch.int16, device="cuda")
+    y_host = torch.zeros(ny, dtype=torch.int16).pin_memory()
+    descs = [(mat.packed, x_dev[:M * K], y_dev[:M * N], K, N)]
+    ws = torch.empty(w.w4g128_decode_step_workspace_bytes(descs, M), dtype=torch.uint8, device="cuda")
+    w.w4g128_decode_step_host(descs, M, x_host, x_dev, nx * 2, y_host, y_dev, ny * 2, ws)
+    torch.cuda.synchronize()
+    assert w.w4g128_workspace_status(ws) == 0
+    assert torch.equal(x_dev[:nx].cpu(), x_host)
+    assert torch.equal(y_host, y_dev.cpu())
+    assert np.array_equal(y_fill[M * N:], y_host.numpy()[M * N:])
+    expect = decode_step([mat], [x_dev[:M * K].clone()], M)[0]  # the plain step on the x the call moved in
+    assert np.array_equal(y_host.numpy()[:M * N].view(np.uint16).reshape(M, N), expect)
