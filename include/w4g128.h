@@ -309,6 +309,28 @@ W4G128_API int w4g128_workspace_status(const void* ws, int* status_out, void* st
  * `stream`. */
 W4G128_API int w4g128_noalloc_status(int* status_out, void* stream);
 
+/* The schedule w4g128_decode_step (count matrices; count = 1 for
+ * w4g128_gemv / w4g128_gemm_verify) takes for these shapes at M rows on the
+ * current device, for diagnostics and tests; launches nothing and reads only
+ * K, N and x of `mats` (a HOST array; x may be NULL, read as 16-byte
+ * aligned).  No counterpart in the pages: it reports how this library lays
+ * the weight stream over the SMs.  Writes min(n, W4G128_SCHEDULE_FIELDS)
+ * values to out (host):
+ *   [0] 1 when every streaming CTA builds its own activation packages
+ *       (M = 1), 0 with the separate package kernel;
+ *   [1] streaming CTAs;  [2] warps per streaming CTA;
+ *   [3] second pass: 0 none, 1 boundary fold of quads split between CTAs
+ *       (M = 1), 2 per-quad reduce, 3 per-warp reduce (M >= 2);
+ *   [4] 1 when each quad is split over the two CTAs of a thread-block
+ *       cluster and folded in the first one's shared memory, else 0;
+ *   [5] ring slots per streaming warp;  [6] workspace bytes;
+ *   [7] work items (quad, 512-row segment) of all matrices.
+ * Returns W4G128_OK, W4G128_ERR_INVALID_ARG / W4G128_ERR_SHAPE for the
+ * arguments w4g128_decode_step would reject, W4G128_ERR_DEVICE without an
+ * sm_103 device. */
+#define W4G128_SCHEDULE_FIELDS 8
+W4G128_API int w4g128_schedule(const w4g128_matrix* mats, int count, int M, long long* out, int n);
+
 /* Workspace bytes w4g128_selftest_wait needs. */
 #define W4G128_SELFTEST_WS_BYTES 512u
 

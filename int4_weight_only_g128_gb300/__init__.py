@@ -17,8 +17,8 @@ __all__ = [
     "w4g128_decode_step_workspace_bytes", "w4g128_decode_step", "w4g128_verify_step", "w4g128_workspace_status",
     "w4g128_probe_read", "w4g128_probe_copy", "w4g128_probe_sink_bytes", "w4g128_gemv_noalloc",
     "w4g128_noalloc_status", "w4g128_selftest_wait", "w4g128_gemm_add_rmsnorm", "w4g128_decode_step_host",
-    "DecodeStep",
-    "MAX_M", "MAX_MATRICES", "SELFTEST_WS_BYTES",
+    "w4g128_schedule", "DecodeStep",
+    "MAX_M", "MAX_MATRICES", "SELFTEST_WS_BYTES", "SCHEDULE_FIELDS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -26,6 +26,7 @@ _INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
 MAX_M = 16          # W4G128_MAX_M
 MAX_MATRICES = 512  # W4G128_MAX_MATRICES
 SELFTEST_WS_BYTES = 512  # W4G128_SELFTEST_WS_BYTES
+SCHEDULE_FIELDS = 8  # W4G128_SCHEDULE_FIELDS
 
 _lib = None
 
@@ -130,6 +131,8 @@ def _declare(L):
     L.w4g128_selftest_wait.argtypes = [p, sz, ctypes.c_ulonglong, i, p]
     L.w4g128_gemm_add_rmsnorm.restype = i
     L.w4g128_gemm_add_rmsnorm.argtypes = [p, p, p, p, ctypes.c_float, p, p, i, i, i, i, p, sz, p]
+    L.w4g128_schedule.restype = i
+    L.w4g128_schedule.argtypes = [ctypes.POINTER(_Matrix), i, i, ctypes.POINTER(ctypes.c_longlong), i]
     return L
 
 
@@ -223,6 +226,17 @@ def w4g128_verify_step(mats, M, ws, ws_bytes=None, stream=None):
     arr = _matrices(mats)
     wb = _nbytes(ws) if ws_bytes is None else ws_bytes
     _check("w4g128_verify_step", lib().w4g128_verify_step(arr, len(mats), M, _ptr(ws), wb, _stream(stream)))
+
+
+def w4g128_schedule(mats, M):
+    """The schedule a decode_step of mats (sequence of (packed, x, y, K, N);
+    only K, N and x are read, pointers may be None) takes at M rows: a dict
+    of the W4G128_SCHEDULE_FIELDS values."""
+    arr = _matrices(mats)
+    out = (ctypes.c_longlong * SCHEDULE_FIELDS)()
+    _check("w4g128_schedule", lib().w4g128_schedule(arr, len(mats), M, out, SCHEDULE_FIELDS))
+    keys = ("local", "ctas", "cta_warps", "second_pass", "pair_quads", "ring_depth", "workspace_bytes", "items")
+    return dict(zip(keys, (int(v) for v in out)))
 
 
 def w4g128_gemm_add_rmsnorm(packed, x, residual, gamma, eps, h, out, M, K, N, verify, ws, ws_bytes=None,

@@ -139,6 +139,19 @@ size_t w4g128_decode_step_workspace_bytes(const w4g128_matrix* mats, int count, 
   return stream_bytes(mats, count, M);
 }
 
+int w4g128_schedule(const w4g128_matrix* mats, int count, int M, long long* out, int n) {
+  if (mats == nullptr || out == nullptr || n < 1 || count < 1 || count > W4G128_MAX_MATRICES || M < 1 ||
+      M > W4G128_MAX_M)
+    return W4G128_ERR_INVALID_ARG;
+  HostMatrix hm[W4G128_MAX_MATRICES];
+  for (int i = 0; i < count; ++i) {
+    if (!shape_ok(mats[i].K, mats[i].N)) return W4G128_ERR_SHAPE;
+    hm[i] = HostMatrix{mats[i].packed, mats[i].x, mats[i].y, mats[i].K, mats[i].N};
+  }
+  if (!w4g128::device_is_sm103()) return W4G128_ERR_DEVICE;
+  return w4g128::describe_schedule(hm, count, M, out, n);
+}
+
 int w4g128_decode_step(const w4g128_matrix* mats, int count, int M, void* ws, size_t ws_bytes, void* stream) {
   return run_stream(mats, count, M, ws, ws_bytes, stream);
 }

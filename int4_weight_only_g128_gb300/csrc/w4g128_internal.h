@@ -64,6 +64,9 @@ int launch_stream(const HostMatrix* mats, int count, int M, const NormArgs* norm
 
 int read_workspace_status(const void* ws, int* status_out, cudaStream_t stream);
 
+// The schedule of a call (the fields of w4g128_schedule), launching nothing.
+int describe_schedule(const HostMatrix* mats, int count, int M, long long* out, int n);
+
 // Device address of a pinned, device-mapped host buffer (16-byte aligned,
 // `bytes` a multiple of 16), or nullptr when the GPU cannot reach it.
 const void* mapped_host(const void* host, size_t bytes);

@@ -1,7 +1,8 @@
 // Inline-PTX building blocks for the sm_103a kernels: mbarriers, 1-D bulk
 // (TMA) copies global -> shared, programmatic-dependent-launch control,
-// relaxed flag words and bounded waits.  Every wait here is bounded by the
-// global nanosecond timer so that no kernel of this library can spin forever.
+// relaxed flag words, bounded waits and the cluster barrier.  Every wait on
+// a flag or an mbarrier here is bounded by the global nanosecond timer so that
+// no kernel of this library can spin forever.
 #pragma once
 #include <cstdint>
 
@@ -89,6 +90,43 @@ __device__ __forceinline__ bool wait_nonzero_bounded(const unsigned long long* a
     if (seen != 0ull) return true;
     if (global_timer_ns() - t0 > limit_ns) return false;
   }
+}
+
+// Thread-block clusters.  The cluster barrier is a hardware barrier like
+// __syncthreads, for every thread of every CTA of the cluster: arrive, then
+// wait for the phase (a kernel using it lets every thread reach every phase
+// on every path, so no wait is left without its arrivals).  The forms
+// without .aligned: a warp need not be converged when it arrives.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// The address in CTA `rank`'s shared memory of this CTA's shared address `a`
+// (the same offset in the other CTA of the cluster).
+__device__ __forceinline__ uint32_t cluster_map(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+// 16-byte store into another CTA's shared memory (an address from cluster_map).
+__device__ __forceinline__ void st_cluster_v4(uint32_t a, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
 }
 
 // 1-D bulk copy global -> shared (this CTA), completion counted in bytes on

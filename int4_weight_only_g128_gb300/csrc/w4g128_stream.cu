@@ -240,6 +240,7 @@ struct StreamParams {
   int cta_warps;         // warps per streaming CTA
   int local_pkg_off;     // M = 1 with CTA-local packages: shared-memory offsets of the package area
   int local_part_off;    //   and of the partial-slot area
+  int pair;              // M = 1, one matrix: quad q runs on CTAs 2q and 2q + 1, a cluster of two
   // local calls of up to kFewMatrices matrices: CTA c streams items
   // [cta_begin[c], cta_begin[c + 1]), split evenly over its warps
   long long cta_begin[MAXMAT <= kFewMatrices ? kMaxLocalCtas + 1 : 1];
@@ -1481,6 +1482,13 @@ __global__ void __maxnreg__(WIDE ? 168 : 120) stream1_local_kernel(const __grid_
   __shared__ LocalFold folds[2 * kNW];
   __shared__ int fold_fail;
 
+  // Paired quads (one matrix): CTA 2q (the leader, cluster rank 0) streams
+  // the first half of quad q's segments and CTA 2q + 1 the rest; at the end
+  // the partner stores its segment sums into the leader's partial slots and
+  // the leader folds all of them in segment order.  Every thread of both CTAs
+  // arrives here and passes the two cluster barrier phases below on every path.
+  const bool pair = MAXMAT == 1 && p.pair != 0;
+  if (pair) cluster_arrive_relaxed();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane >> 2, c = lane & 3;
   const int cw = blockDim.x >> 5;
@@ -1518,6 +1526,16 @@ __global__ void __maxnreg__(WIDE ? 168 : 120) stream1_local_kernel(const __grid_
   const uint32_t ring0 = bars + kLocalBarBytes;
   uint8_t* const pkg_area = smem + p.local_pkg_off;
   float* const part_area = reinterpret_cast<float*>(smem + p.local_part_off);
+  // the pair's items [Aq, Bq): one quad, whose slots all sit in the leader
+  long long Aq = A, Bq = B;
+  if constexpr (MAXMAT <= kFewMatrices) {
+    if (pair && (gridDim.x & 1u) == 0u && gridDim.x <= static_cast<unsigned>(kMaxLocalCtas)) {
+      Aq = p.cta_begin[blockIdx.x & ~1u];
+      Bq = p.cta_begin[(blockIdx.x | 1u) + 1u];
+    }
+  }
+  // the slots this CTA's folds may read
+  const long long slot_cap = pair ? Bq - Aq : B - A;
 
   if (threadIdx.x == 0) {
     fold_n = 0;
@@ -1534,11 +1552,24 @@ __global__ void __maxnreg__(WIDE ? 168 : 120) stream1_local_kernel(const __grid_
   // The host launches this kernel only for M = 1 calls whose every CTA fits
   // (the same table function); a CTA that does not fit records the error and
   // touches nothing.
-  if (tbl_n <= 0 || p.M != 1 || p.local_pkg_off != kLocalBarBytes + kLocalRing || D < 2 || D * cw > kLocalSlots ||
-      A < 0 || B < A || B > I || (B - A) * cw >= (1ll << 31) ||
+  // A pair must be CTAs 2q, 2q + 1 of a two-CTA cluster holding exactly the
+  // segments of one quad, in that order, with room for all of them in the
+  // leader (both CTAs take the same decision from the same words).
+  const bool pair_bad =
+      pair && ((gridDim.x & 1u) != 0u || cluster_nctarank() != 2u || cluster_ctarank() != (blockIdx.x & 1u) ||
+               Aq < 0 || Bq > I || Bq - Aq != div_up(mat(p, 0).K / kGroup, kSegGroups) ||
+               (Aq - mat(p, 0).item_begin) % (Bq - Aq) != 0 || A < Aq || B > Bq ||
+               p.local_part_off + (Bq - Aq) * 64 * 4 > kLocalDyn);
+  if (pair_bad || tbl_n <= 0 || p.M != 1 || p.local_pkg_off != kLocalBarBytes + kLocalRing || D < 2 ||
+      D * cw > kLocalSlots || A < 0 || B < A || B > I || (B - A) * cw >= (1ll << 31) ||
       p.local_pkg_off + static_cast<long long>(tbl_npkg) * kPkg1 > p.local_part_off ||
       p.local_part_off + (B - A) * 64 * 4 > kLocalDyn) {
     if (threadIdx.x == 0) status_fail(p.status, W4G128_ERR_INTERNAL);
+    if (pair) {  // the partner CTA still passes both phases
+      cluster_wait_acquire();
+      cluster_arrive_release();
+      cluster_wait_acquire();
+    }
     return;
   }
   const int mi_a = tbl[0].mi;
@@ -1676,7 +1707,8 @@ __global__ void __maxnreg__(WIDE ? 168 : 120) stream1_local_kernel(const __grid_
         if (!owned && (!prefix || cc.item + 1 == it_b) && dbg_ok_local(p.status, cc.item >= A && cc.item < B)) {
           // a quad that began before this CTA: the segment sum goes to its
           // global slot for the boundary fold; otherwise to this CTA's slot
-          float* part = (q_first < A) ? p.partials + cc.item * 64 : part_area + (cc.item - A) * 64;
+          // (a pair's partner keeps its slots in shared memory for the leader)
+          float* part = (q_first < A && !pair) ? p.partials + cc.item * 64 : part_area + (cc.item - A) * 64;
           if (c == 0) {
 #pragma unroll
             for (int t = 0; t < kQuadTiles; ++t) {
@@ -1713,7 +1745,7 @@ __global__ void __maxnreg__(WIDE ? 168 : 120) stream1_local_kernel(const __grid_
             if (lane == 0) {
               const long long first = owner_last(q_first);
               LocalFold& f = folds[atomicAdd(&fold_n, 1)];
-              const bool inner = cc.s == S - 1;
+              const bool inner = cc.s == S - 1 || pair;  // a pair's leader folds the whole quad
               f.first = first - A;
               f.nslot = static_cast<int>((inner ? q_last : B - 1) + 1 - first);
               f.y = inner ? m.y + n0 : nullptr;
@@ -1731,6 +1763,17 @@ __global__ void __maxnreg__(WIDE ? 168 : 120) stream1_local_kernel(const __grid_
     if (failed && lane == 0) atomicOr(&fold_fail, 1);
   }
   __syncthreads();  // every warp's slots are written
+  if (pair) {
+    cluster_wait_acquire();  // both CTAs of the pair have started: the leader's shared memory is there
+    if (blockIdx.x & 1u) {   // the partner: its slots to the leader's, after the leader's own
+      const uint32_t dst = cluster_map(smem_addr(part_area), 0u) + static_cast<uint32_t>(A - Aq) * 256u;
+      const float4* src = reinterpret_cast<const float4*>(part_area);
+      const int n16 = static_cast<int>(B - A) * 16;
+      for (int i = threadIdx.x; i < n16; i += blockDim.x) st_cluster_v4(dst + 16u * i, src[i]);
+    }
+    cluster_arrive_release();
+    cluster_wait_acquire();  // the partner's slots are in the leader's shared memory
+  }
   if (fold_fail) return;  // a timed-out warp left its quads unreduced (the status word says so)
 
   // ---- the CTA's folds: one thread per (fold, 4 columns), slots in order
@@ -1739,7 +1782,7 @@ __global__ void __maxnreg__(WIDE ? 168 : 120) stream1_local_kernel(const __grid_
     const LocalFold& f = folds[idx >> 4];
     const int col = 4 * (idx & 15);
     if (col >= f.cols) continue;
-    if (!dbg_ok_local(p.status, f.first >= 0 && f.first + f.nslot <= B - A)) continue;
+    if (!dbg_ok_local(p.status, f.first >= 0 && f.first + f.nslot <= slot_cap)) continue;
     const float4* part = reinterpret_cast<const float4*>(part_area + f.first * 64 + col);
     uint32_t r0 = 0u, r1 = 0u;
     if (f.y != nullptr) {
@@ -2160,6 +2203,7 @@ struct DeviceInfo {
   int occ[4] = {0, 0, 0, 0};        // CTAs per SM per mode
   int red_occ[kMaxRows + 1] = {};   // per-quad reduce CTAs per SM per M
   int red_occ_deep[kMaxRows + 1] = {};  // the same at kRedChunkDeep slots per copy
+  int pair_clusters = 0;            // clusters of two local M = 1 CTAs resident at once
   bool ok = false;
 };
 
@@ -2232,6 +2276,32 @@ const DeviceInfo* device_info() {
       setup_mode<kMMA1>(d);
       setup_mode<kMMA16>(d);
       setup_local();
+      {
+        // how many two-CTA clusters of the local kernel (both forms paired
+        // quads use) fit on the device at once
+        cudaLaunchAttribute ca[1];
+        ca[0].id = cudaLaunchAttributeClusterDimension;
+        ca[0].val.clusterDim.x = 2;
+        ca[0].val.clusterDim.y = 1;
+        ca[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cc = {};
+        cc.gridDim = dim3(2);
+        cc.blockDim = dim3(kWideWarps * 32);
+        cc.dynamicSmemBytes = kLocalDyn;
+        cc.attrs = ca;
+        cc.numAttrs = 1;
+        int n = 0, n16 = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, stream1_local_kernel<1, false, true>, &cc) != cudaSuccess) {
+          cudaGetLastError();
+          n = 0;
+        }
+        cc.blockDim = dim3(kNW * 32);
+        if (cudaOccupancyMaxActiveClusters(&n16, stream1_local_kernel<1, false, false>, &cc) != cudaSuccess) {
+          cudaGetLastError();
+          n16 = 0;
+        }
+        d.pair_clusters = std::min(n, n16);
+      }
       for (int M = 2; M <= kMaxRows; ++M) {
         int n = 0;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, reduce_quads_kernel<W4G128_MAX_MATRICES, false>,
@@ -2276,6 +2346,7 @@ struct Plan {
   std::vector<int> quad_begin, g_begin;
   std::vector<long long> cta_begin;  // local calls of up to kFewMatrices matrices: the CTAs' first items
   bool whole_quads = false;          // M = 1, one matrix: one CTA per quad, no boundary fold
+  bool pair_quads = false;           // M = 1, one matrix: two CTAs (a cluster) per quad, no boundary fold
 };
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -2364,8 +2435,37 @@ bool make_plan(const HostMatrix* mats, int count, int M, const DeviceInfo& dev, 
       pl.W = NQ1 * S1;
       pl.whole_quads = true;
     }
+    // Deeper quads (up to two CTAs' worth of warps), when clusters of two
+    // CTAs fit once per quad: quad q's segments are split between CTAs 2q and
+    // 2q + 1, which fold through the first one's shared memory, so no quad
+    // needs the boundary fold kernel.  The pairs leave sms - 2 NQ SMs idle
+    // that the balanced split would use; they are taken while the extra
+    // bytes each streaming SM then pulls, ceil(S / 2) items x (1 - 2 NQ /
+    // sms), stay within 4 items (measured, us, pairs against the balanced
+    // split with its fold kernel: 8192x4096 8.37 / 8.94, 11392x4080 9.48 /
+    // 10.73, 16384x4096 11.45 / 12.40, 10240x3072 8.54 / 8.76, 5632x2432
+    // 6.77 / 6.84; 16384x2432, 16 items x 1/2, 10.15 / 8.86).  Not for quads
+    // one CTA holds: there each warp's chunks are a latency-bound sequence
+    // whatever the CTAs per SM, and pairs only add the cluster barrier
+    // (4096^2 6.58 against 6.07 us with one CTA per quad).
+    else if (S1 > kWholeQuadSegs && S1 <= 2 * kNW && NQ1 <= dev.pair_clusters && 4 * NQ1 >= dev.sms &&
+             div_up(S1, 2) * (dev.sms - 2 * NQ1) <= 4 * dev.sms) {
+      pl.grid = 2 * NQ1;
+      pl.cta_warps = div_up(S1, 2);
+      pl.W = pl.grid * pl.cta_warps;
+      pl.whole_quads = true;
+      pl.pair_quads = true;
+    }
   }
-  if (cta_table && pl.grid <= kMaxLocalCtas) {
+  if (pl.pair_quads) {
+    const int S1 = div_up(mats[0].K / kGroup, kSegGroups);
+    pl.cta_begin.resize(pl.grid + 1);
+    for (int q = 0; q < pl.grid / 2; ++q) {
+      pl.cta_begin[2 * q] = static_cast<long long>(q) * S1;
+      pl.cta_begin[2 * q + 1] = static_cast<long long>(q) * S1 + div_up(S1, 2);
+    }
+    pl.cta_begin[pl.grid] = items;
+  } else if (cta_table && pl.grid <= kMaxLocalCtas) {
     pl.cta_begin.resize(pl.grid + 1);
     for (int c = 0; c <= pl.grid; ++c)
       pl.cta_begin[c] = items * std::min<long long>(static_cast<long long>(c) * pl.cta_warps, pl.W) / pl.W;
@@ -2394,6 +2494,7 @@ bool make_plan(const HostMatrix* mats, int count, int M, const DeviceInfo& dev, 
       pmax = std::max(pmax, np);
       smax = std::max(smax, B - A);
     }
+    if (pl.pair_quads) smax = std::max<long long>(smax, div_up(mats[0].K / kGroup, kSegGroups));  // the leader
     ok = ok && static_cast<long long>(pmax) * kPkg1 + smax * 64 * 4 <= kLocalSpace;
     pl.local = ok;
     pl.local_depth = std::min(8, kLocalSlots / pl.cta_warps);
@@ -2433,6 +2534,7 @@ void fill_params(StreamParams<MAXMAT>& sp, const HostMatrix* mats, int count, in
   sp.cta_warps = pl.cta_warps;
   sp.local_pkg_off = pl.local_pkg_off;
   sp.local_part_off = pl.local_part_off;
+  sp.pair = 0;  // set by the local launch
   if constexpr (MAXMAT <= kFewMatrices) {
     const int nb = std::min(static_cast<int>(pl.cta_begin.size()), kMaxLocalCtas + 1);
     for (int c = 0; c < nb; ++c) sp.cta_begin[c] = pl.cta_begin[c];
@@ -2458,13 +2560,17 @@ void fill_params(StreamParams<MAXMAT>& sp, const HostMatrix* mats, int count, in
 // boundaries can split quads, and the norm behind that.
 template <int MAXMAT, bool NORM, bool WIDE>
 int launch_local(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, bool boundary_fold, cudaStream_t stream) {
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;  // paired quads: clusters of two CTAs
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = sp.pair ? 2 : 1;
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(cta_warps * 32);
   cfg.dynamicSmemBytes = kLocalDyn;
@@ -2472,6 +2578,7 @@ int launch_local(const StreamParams<MAXMAT>& sp, int grid, int cta_warps, bool b
     cudaGetLastError();
     return W4G128_ERR_CUDA;
   }
+  cfg.numAttrs = 1;
   if (grid > 1 && boundary_fold) {
     cfg.gridDim = dim3(grid - 1);
     cfg.blockDim = dim3(32);
@@ -2586,6 +2693,7 @@ int launch_with(const HostMatrix* mats, int count, int M, const Plan& pl, const 
   fill_params(sp, mats, count, M, pl, norm, ws);
   if (pl.local && x_aligned(mats, count)) {
     sp.depth = pl.local_depth;
+    sp.pair = pl.pair_quads ? 1 : 0;
     if constexpr (MAXMAT == 1) {
       if (pl.cta_warps <= kWideWarps) {
         if (norm != nullptr) return launch_local<1, true, true>(sp, pl.grid, pl.cta_warps, !pl.whole_quads, stream);
@@ -2680,6 +2788,31 @@ int launch_stream(const HostMatrix* mats, int count, int M, const NormArgs* norm
   // attributes were set: the next call sets them up again.
   if (rc == W4G128_ERR_CUDA) forget_device();
   return rc;
+}
+
+int describe_schedule(const HostMatrix* mats, int count, int M, long long* out, int n) {
+  const DeviceInfo* d = device_info();
+  if (d == nullptr || !d->ok) return W4G128_ERR_DEVICE;
+  const Plan* cached = cached_plan(mats, count, M, *d);
+  if (cached == nullptr) return W4G128_ERR_SHAPE;
+  const Plan& pl = *cached;
+  bool xa = true;
+  for (int i = 0; i < count; ++i)
+    if (mats[i].x != nullptr && (reinterpret_cast<uintptr_t>(mats[i].x) & 15u) != 0u) xa = false;
+  const bool local = pl.local && xa;
+  long long v[8];
+  v[0] = local ? 1 : 0;
+  v[1] = pl.grid;
+  v[2] = pl.cta_warps;
+  if (local) v[3] = (pl.grid > 1 && !pl.whole_quads) ? 1 : 0;
+  else if (M == 1) v[3] = 0;  // the package-kernel path at M = 1 folds split quads inside the stream
+  else v[3] = pl.per_warp_reduce ? 3 : 2;
+  v[4] = (local && pl.pair_quads) ? 1 : 0;
+  v[5] = local ? pl.local_depth : pl.depth;
+  v[6] = static_cast<long long>(pl.bytes);
+  v[7] = pl.items;
+  for (int i = 0; i < n && i < 8; ++i) out[i] = v[i];
+  return W4G128_OK;
 }
 
 int read_workspace_status(const void* ws, int* status_out, cudaStream_t stream) {

@@ -17,7 +17,7 @@ def L():
 
 def test_every_header_symbol_is_exported(L):
     names = w.exported_symbols()
-    assert len(names) == 20
+    assert len(names) == 21
     for n in names:
         assert hasattr(L, n), n
 
@@ -95,6 +95,24 @@ def test_decode_step_argument_errors(L):
     assert L.w4g128_decode_step(mats, 2, 1, FAKE, 1 << 20, None) == E_INVALID
 
 
+def test_schedule_argument_errors(L):
+    mats = (w._Matrix * 2)()
+    mats[0] = w._Matrix(None, None, None, 128, 16)
+    mats[1] = w._Matrix(None, None, None, 256, 48)
+    out = (ctypes.c_longlong * 8)()
+    assert L.w4g128_schedule(None, 1, 1, out, 8) == E_INVALID
+    assert L.w4g128_schedule(mats, 0, 1, out, 8) == E_INVALID
+    assert L.w4g128_schedule(mats, 513, 1, out, 8) == E_INVALID
+    assert L.w4g128_schedule(mats, 2, 0, out, 8) == E_INVALID
+    assert L.w4g128_schedule(mats, 2, 17, out, 8) == E_INVALID
+    assert L.w4g128_schedule(mats, 2, 1, None, 8) == E_INVALID
+    assert L.w4g128_schedule(mats, 2, 1, out, 0) == E_INVALID
+    mats[1] = w._Matrix(None, None, None, 200, 48)
+    assert L.w4g128_schedule(mats, 2, 1, out, 8) == E_SHAPE
+    with open(w._INCLUDE + "/w4g128.h") as f:
+        assert "#define W4G128_SCHEDULE_FIELDS %d" % w.SCHEDULE_FIELDS in f.read()
+
+
 def test_pack_argument_errors(L):
     assert L.w4g128_pack(None, FAKE, FAKE, 128, 16, FAKE, None) == E_INVALID
     assert L.w4g128_pack(FAKE, FAKE, FAKE, 128, 17, FAKE, None) == E_SHAPE
@@ -124,6 +142,10 @@ def test_no_device_is_reported_not_faked():
     assert L.w4g128_gemm_add_rmsnorm(FAKE, FAKE + 0x800, FAKE + 0x1000, FAKE + 0x2000, 1e-6, FAKE + 0x1000,
                                      FAKE + 0x3000, 1, 128, 16, 0, FAKE, 1 << 20, None) == E_DEVICE
     assert w.w4g128_workspace_bytes(1, 128, 16) == 0
+    mats = (w._Matrix * 1)()
+    mats[0] = w._Matrix(None, None, None, 128, 16)
+    out = (ctypes.c_longlong * 8)()
+    assert L.w4g128_schedule(mats, 1, 1, out, 8) == E_DEVICE
 
 
 def test_error_raises_in_binding():

@@ -3,7 +3,8 @@ every global access the kernels derive from the schedule -- weight and
 package copies, x staging, partial slots, tickets, y -- is checked against
 its buffer, and a failed check is recorded as W4G128_ERR_INTERNAL in the
 status word (the access is skipped; nothing traps).  A spread of calls
-covering every kernel path (CTA-local M = 1, the prep-kernel path at M = 1
+covering every kernel path (CTA-local M = 1, quads split over a two-CTA
+cluster, the prep-kernel path at M = 1
 and M >= 2, both reduce forms, many matrices, the fused norm, the
 workspace-free entry point) must pass every check, give the release
 library's bits, and leave guard bytes around each y and each workspace
@@ -66,6 +67,9 @@ CASES = [
     ("gemv local", [(17408, 5120)], 1, "gemv", False),
     ("gemv prep path (x 4-byte aligned)", [(5120, 6144)], 1, "gemv", True),
     ("gemv largest K", [(65536, 208)], 1, "gemv", False),
+    ("gemv paired quads", [(8192, 4096)], 1, "gemv", False),
+    ("gemv paired quads, odd and ragged segments, ragged quad", [(11392, 4080)], 1, "gemv", False),
+    ("gemv paired quads, 16 warps", [(16384, 4864)], 1, "gemv", False),
     ("verify M=2", [(6144, 5120)], 2, "verify", False),
     ("verify M=8", [(17408, 5120)], 8, "verify", False),
     ("verify M=16", [(5120, 6144)], 16, "verify", False),
