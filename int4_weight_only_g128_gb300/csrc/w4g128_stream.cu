@@ -2347,6 +2347,12 @@ struct Plan {
   std::vector<long long> cta_begin;  // local calls of up to kFewMatrices matrices: the CTAs' first items
   bool whole_quads = false;          // M = 1, one matrix: one CTA per quad, no boundary fold
   bool pair_quads = false;           // M = 1, one matrix: two CTAs (a cluster) per quad, no boundary fold
+  // The balanced split (W <= items: every warp has an item), which the
+  // package-kernel path takes when the local kernel cannot (x not 16-byte
+  // aligned): the paired quads give a warp no item when S is odd, and that
+  // path's ticket count takes every warp between a quad's owners to hold
+  // some of it.
+  int gen_grid = 0, gen_cta_warps = 0, gen_W = 0;
 };
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -2391,6 +2397,9 @@ bool make_plan(const HostMatrix* mats, int count, int M, const DeviceInfo& dev, 
   // holds warps gets smaller CTAs rather than fewer SMs.
   pl.cta_warps = std::min(nw, div_up(pl.W, dev.sms));
   pl.grid = div_up(pl.W, pl.cta_warps);
+  pl.gen_grid = pl.grid;
+  pl.gen_cta_warps = pl.cta_warps;
+  pl.gen_W = pl.W;
   pl.depth = (pl.mode == kMMA1) ? ring_depth<kMMA1>() : ring_depth<kMMA>();
   // M >= 2: fold per quad unless that grid is larger than one streaming warp
   // each and than one wave of resident reduce CTAs
@@ -2703,17 +2712,20 @@ int launch_with(const HostMatrix* mats, int count, int M, const Plan& pl, const 
     }
     return launch_local<MAXMAT, false, false>(sp, pl.grid, pl.cta_warps, !pl.whole_quads, stream);
   }
+  // the package-kernel path, over the balanced split
+  sp.W = pl.gen_W;
+  sp.cta_warps = pl.gen_cta_warps;
+  const int grid = pl.gen_grid, cw = pl.gen_cta_warps;
   if constexpr (MAXMAT == 1) {
     if (norm != nullptr) {
-      if (pl.mode == kMMA16) return launch_mode<kMMA16, 1, true>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
-      if (pl.mode == kMMA) return launch_mode<kMMA, 1, true>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
-      return launch_mode<kMMA1, 1, true>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
+      if (pl.mode == kMMA16) return launch_mode<kMMA16, 1, true>(sp, grid, cw, pl.max_groups, stream);
+      if (pl.mode == kMMA) return launch_mode<kMMA, 1, true>(sp, grid, cw, pl.max_groups, stream);
+      return launch_mode<kMMA1, 1, true>(sp, grid, cw, pl.max_groups, stream);
     }
   }
-  if (pl.mode == kMMA16)
-    return launch_mode<kMMA16, MAXMAT, false>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
-  if (pl.mode == kMMA) return launch_mode<kMMA, MAXMAT, false>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
-  return launch_mode<kMMA1, MAXMAT, false>(sp, pl.grid, pl.cta_warps, pl.max_groups, stream);
+  if (pl.mode == kMMA16) return launch_mode<kMMA16, MAXMAT, false>(sp, grid, cw, pl.max_groups, stream);
+  if (pl.mode == kMMA) return launch_mode<kMMA, MAXMAT, false>(sp, grid, cw, pl.max_groups, stream);
+  return launch_mode<kMMA1, MAXMAT, false>(sp, grid, cw, pl.max_groups, stream);
 }
 
 // The last few plans of this host thread, keyed by device, M and the list of
@@ -2802,8 +2814,8 @@ int describe_schedule(const HostMatrix* mats, int count, int M, long long* out, 
   const bool local = pl.local && xa;
   long long v[8];
   v[0] = local ? 1 : 0;
-  v[1] = pl.grid;
-  v[2] = pl.cta_warps;
+  v[1] = local ? pl.grid : pl.gen_grid;
+  v[2] = local ? pl.cta_warps : pl.gen_cta_warps;
   if (local) v[3] = (pl.grid > 1 && !pl.whole_quads) ? 1 : 0;
   else if (M == 1) v[3] = 0;  // the package-kernel path at M = 1 folds split quads inside the stream
   else v[3] = pl.per_warp_reduce ? 3 : 2;

@@ -10,8 +10,9 @@ output is within the oracle's bound; the exact-integer case is bf16_rn of
 the oracle bit for bit (a segment sum dropped, repeated or placed in the
 wrong slot changes an output by at least one unit); the outputs are bitwise
 those of the same matrix streamed through the multi-matrix schedule (other
-CTAs, other folds, the same summation order); back-to-back calls on one
-stream without synchronisation; the residual add + RMS norm entry point's h."""
+CTAs, other folds, the same summation order) and through the package-kernel
+path that an x only 4-byte aligned takes; back-to-back calls on one stream
+without synchronisation; the residual add + RMS norm entry point's h."""
 import numpy as np
 import pytest
 
@@ -81,6 +82,29 @@ def test_pairs_match_oracle_and_multi_matrix_path(K, N):
     check_against_oracle(y, x, mat.codes, mat.scales, mat.mins)
     assert np.array_equal(y, multi_matrix(mat, x))
     assert np.array_equal(run(mat, x, verify=True), y)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("K,N", SHAPES)
+def test_pair_shapes_with_misaligned_x(K, N):
+    """x only 4-byte aligned: the call takes the package-kernel path over the
+    balanced split (paired quads leave a warp without an item when the
+    segment count is odd, which that path's ticket count does not allow) and
+    gives the aligned call's bits."""
+    mat = DevMatrix(K, N, matrix_id=3050 + K // 128)
+    xb = synth.x(SEED, 3051 + K, 1, K)
+    buf = torch.zeros(K + 8, dtype=torch.int16, device="cuda")
+    xm = buf[2:2 + K]  # 4 bytes past a 16-byte boundary
+    xm.copy_(to_dev(xb).view(-1))
+    sch = w.w4g128_schedule([(None, xm, None, K, N)], 1)
+    assert sch["local"] == 0 and sch["pair_quads"] == 0, sch
+    assert sch["ctas"] * sch["cta_warps"] <= sch["items"] + sch["cta_warps"], sch
+    y = torch.empty(N, dtype=torch.int16, device="cuda")
+    ws = workspace(1, K, N)
+    w.w4g128_gemv(mat.packed, xm, y, K, N, ws)
+    torch.cuda.synchronize()
+    assert w.w4g128_workspace_status(ws) == 0
+    assert np.array_equal(to_host(y, np.uint16).reshape(1, N), run(mat, xb))
 
 
 @pytest.mark.gpu
