@@ -1467,13 +1467,19 @@ struct LocalFold {
   int pad;
 };
 
-// 120 registers (no spills), as the prep-kernel M = 1 path: 512 threads fit,
-// with registers left for fold1_kernel's small CTAs beside them.  The WIDE
-// form (CTAs of at most kWideWarps warps: calls too small to give every SM
-// 16 warps) takes 168 registers and interleaves a quad's four tiles, since
-// there a warp is often alone on its scheduler.
+// CTAs of 13-16 warps: the several-matrix forms (a decoder layer's step)
+// take 128 registers, a 16-warp CTA then holding the SM's whole register
+// file, and interleave a quad's tiles in pairs (spilling a few words); the
+// one-matrix form keeps 120 registers and goes tile by tile, which leaves
+// room for fold1_kernel's small CTAs beside the stream.  Measured on one
+// GPU: the layer step 36.70 -> 36.40 us with the pairs, the 5120x248320
+// lm_head 101.9 -> 103.7 us.  The WIDE form (CTAs of at most kWideWarps
+// warps: calls too small to give every SM 16 warps) takes 168 registers and
+// interleaves all four tiles, since there a warp is often alone on its
+// scheduler.
 template <int MAXMAT, bool NORM, bool WIDE>
-__global__ void __maxnreg__(WIDE ? 168 : 120) stream1_local_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
+__global__ void __maxnreg__(WIDE ? 168 : (MAXMAT == 1 ? 120 : 128))
+    stream1_local_kernel(const __grid_constant__ StreamParams<MAXMAT> p) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int NA = Acc<kMMA1>::kN;
   __shared__ LocalEntry tbl[kLocalMaxEntries];
@@ -1678,7 +1684,7 @@ __global__ void __maxnreg__(WIDE ? 168 : 120) stream1_local_kernel(const __grid_
       }
       const int ntiles = cc.ntiles;
       const uint8_t* sl = smem + kLocalBarBytes + (slot * cw + warp) * kLocalSlot;
-      compute_chunk<kMMA1, WIDE ? 2 : 0>(sl, cc.xsrc, ntiles, lane, seg);
+      compute_chunk<kMMA1, WIDE ? 2 : (MAXMAT == 1 ? 0 : 1)>(sl, cc.xsrc, ntiles, lane, seg);
       __syncwarp();
       if (ic.item < it_b) {
         if (lane == 0) fence_proxy_async_smem();  // the slot's reads are done before the copy rewrites it
