@@ -61,11 +61,12 @@ def test_noalloc_matches_gemv_on_consecutive_calls():
 
 @pytest.mark.gpu
 def test_noalloc_back_to_back_without_synchronising():
-    """Three calls on one stream with no synchronisation between them: each
+    """Four calls on one stream with no synchronisation between them (one on
+    the paired-quad schedule, each quad on a two-CTA cluster): each
     call's first kernel waits for the previous call before it rewrites the
     shared scratch, so every output is still bitwise w4g128_gemv's."""
-    mats = [DevMatrix(5120, 6144, matrix_id=511), DevMatrix(6144, 5120, matrix_id=512),
-            DevMatrix(1152, 208, matrix_id=513)]
+    mats = [DevMatrix(5120, 6144, matrix_id=511), DevMatrix(8192, 4096, matrix_id=514),  # paired quads
+            DevMatrix(6144, 5120, matrix_id=512), DevMatrix(1152, 208, matrix_id=513)]
     xs = [synth.x(SEED, 620 + i, 1, m.K) for i, m in enumerate(mats)]
     pending = [noalloc(m, x, sync=False) for m, x in zip(mats, xs)]
     torch.cuda.synchronize()
